@@ -1,0 +1,230 @@
+"""Plain fp64 CPU oracle for striped causal attention -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never loads it and
+shares no code with it.
+
+The arithmetic lives in ``oracle.c`` (plain C, fp64, POSIX threads over
+rows); this module compiles it with gcc on first use and wraps it with ctypes
+over numpy float64 arrays.  Every function works on ONE head stored [S, D]
+row-major in *position* (unpermuted) order.
+
+Definitions followed (pages on "Striped Attention: Faster Ring Attention for
+Causal Transformers"):
+
+* exact causal attention -- research.elamur.ai summary page, §Summary and
+  §Key points ("results remain exact"); pith.science paper page, abstract
+  ("an exact attention algorithm");
+* stripe placement "every N-th token" -- research.elamur.ai, §Summary;
+* contiguous placement and per-round work of Ring Attention -- §Summary,
+  first paragraph; per-round balance -- §Key points "Imbalance".
+
+Pins: every function here is checked in ``tests/test_oracle.py`` against
+things other than itself (closed forms, special cases, library routines,
+finite differences, brute force).  No function is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+STRIPED = 0
+CONTIGUOUS = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into _build/liboracle.so (gcc -O2, no BLAS)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                           _SRC, "-o", tmp, "-lm"])
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I64 = ctypes.c_int64
+            I = ctypes.c_int
+            Dbl = ctypes.c_double
+            lib.oracle_position_of_row.argtypes = [I64, I64, I, I]
+            lib.oracle_position_of_row.restype = I64
+            lib.oracle_stripe_positions.argtypes = [I64, I, P]
+            lib.oracle_attn_fwd.argtypes = [P, P, P, I64, I64, Dbl, P, I64, P, P, P, I]
+            lib.oracle_bwd_rows.argtypes = [P, P, P, P, I64, I64, Dbl, P, I64, P, P, P, I]
+            lib.oracle_bwd_keys.argtypes = [P, P, P, P, I64, I64, Dbl, P, P, I64, P, I64, P, P, I]
+            lib.oracle_attn_bwd.argtypes = [P, P, P, P, I64, I64, Dbl, P, P, P, I]
+            lib.oracle_tile_counts_bruteforce.argtypes = [I64, I, I64, I64, I, P, P]
+            lib.oracle_tile_counts_closed.argtypes = [I64, I, I64, I, P, P]
+            lib.oracle_critical_path.argtypes = [P, P, I]
+            lib.oracle_critical_path.restype = I64
+            _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return max(1, os.cpu_count() or 1)
+
+
+def _f64(x) -> np.ndarray:
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    return a
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+# --------------------------------------------------------------------------
+# placement
+# --------------------------------------------------------------------------
+def position_of_row(row: int, S: int, N: int, layout: int = STRIPED) -> int:
+    """Global position held by layout row ``row`` (striped: d*L+i -> i*N+d)."""
+    return int(_load().oracle_position_of_row(row, S, N, layout))
+
+
+def stripe_positions(S: int, N: int) -> np.ndarray:
+    """pos[row] for the striped layout, built by enumerating p mod N == d."""
+    out = np.empty(S, dtype=np.int64)
+    _load().oracle_stripe_positions(S, N, _ptr(out))
+    return out
+
+
+# --------------------------------------------------------------------------
+# forward / backward (one head, position order)
+# --------------------------------------------------------------------------
+def attn_fwd(q, k, v, scale: float, rows=None, key_in_set=None, nthreads: int | None = None):
+    """Return (O [n, D], LSE [n]) for query positions ``rows`` (all if None).
+
+    ``key_in_set`` (bool [S]) restricts the keys (one ring round's partial
+    result); rows with no kept key get O = 0 and LSE = -inf.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    S, D = q.shape
+    r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = S if r is None else r.shape[0]
+    ks = None if key_in_set is None else np.ascontiguousarray(np.asarray(key_in_set, dtype=np.uint8))
+    o = np.empty((n, D), dtype=np.float64)
+    lse = np.empty(n, dtype=np.float64)
+    _load().oracle_attn_fwd(_ptr(q), _ptr(k), _ptr(v), S, D, float(scale), _ptr(r), n, _ptr(ks),
+                            _ptr(o), _ptr(lse), nthreads or default_threads())
+    return o, lse
+
+
+def bwd_rows(q, k, v, dO, scale: float, rows=None, want_dq: bool = True,
+             nthreads: int | None = None):
+    """Return (LSE [n], J [n], dQ [n, D] or None) for query positions ``rows``."""
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    S, D = q.shape
+    r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = S if r is None else r.shape[0]
+    lse = np.empty(n, dtype=np.float64)
+    J = np.empty(n, dtype=np.float64)
+    dq = np.empty((n, D), dtype=np.float64) if want_dq else None
+    _load().oracle_bwd_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), S, D, float(scale), _ptr(r), n,
+                            _ptr(lse), _ptr(J), _ptr(dq), nthreads or default_threads())
+    return lse, J, dq
+
+
+def bwd_keys(q, k, v, dO, scale: float, keys, nthreads: int | None = None):
+    """Return (dK [n, D], dV [n, D]) for key positions ``keys``.
+
+    Computes the needed LSE_p and J_p for every query p >= min(keys) first.
+    """
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    S, D = q.shape
+    keys = np.ascontiguousarray(np.asarray(keys, dtype=np.int64))
+    nt = nthreads or default_threads()
+    p_lo = int(keys.min()) if keys.size else S
+    rows = np.arange(p_lo, S, dtype=np.int64)
+    lse, J, _ = bwd_rows(q, k, v, dO, scale, rows=rows, want_dq=False, nthreads=nt)
+    dk = np.empty((keys.shape[0], D), dtype=np.float64)
+    dv = np.empty((keys.shape[0], D), dtype=np.float64)
+    _load().oracle_bwd_keys(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), S, D, float(scale), _ptr(lse),
+                            _ptr(J), p_lo, _ptr(keys), keys.shape[0], _ptr(dk), _ptr(dv), nt)
+    return dk, dv
+
+
+def attn_bwd(q, k, v, dO, scale: float, nthreads: int | None = None):
+    """Full backward of one head: (dQ, dK, dV), each [S, D]."""
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    S, D = q.shape
+    dq = np.empty((S, D), dtype=np.float64)
+    dk = np.empty((S, D), dtype=np.float64)
+    dv = np.empty((S, D), dtype=np.float64)
+    _load().oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), S, D, float(scale), _ptr(dq),
+                            _ptr(dk), _ptr(dv), nthreads or default_threads())
+    return dq, dk, dv
+
+
+# --------------------------------------------------------------------------
+# per-round tile accounting
+# --------------------------------------------------------------------------
+def tile_counts_bruteforce(S: int, N: int, Tq: int, Tk: int, layout: int = STRIPED):
+    """(full [N rounds, N devices], partial [N, N]) by enumerating every pair."""
+    full = np.zeros(N * N, dtype=np.int64)
+    part = np.zeros(N * N, dtype=np.int64)
+    _load().oracle_tile_counts_bruteforce(S, N, Tq, Tk, layout, _ptr(full), _ptr(part))
+    return full.reshape(N, N), part.reshape(N, N)
+
+
+def tile_counts_closed(S: int, N: int, T: int, layout: int = STRIPED):
+    """Closed-form (full, partial) tables for T dividing L = S / N."""
+    full = np.zeros(N * N, dtype=np.int64)
+    part = np.zeros(N * N, dtype=np.int64)
+    _load().oracle_tile_counts_closed(S, N, T, layout, _ptr(full), _ptr(part))
+    return full.reshape(N, N), part.reshape(N, N)
+
+
+def critical_path(full: np.ndarray, partial: np.ndarray) -> int:
+    """Sum over rounds of the busiest device's tile count."""
+    f = np.ascontiguousarray(full, dtype=np.int64)
+    p = np.ascontiguousarray(partial, dtype=np.int64)
+    return int(_load().oracle_critical_path(_ptr(f), _ptr(p), f.shape[0]))
+
+
+def merge_rounds(o_a, lse_a, o_b, lse_b):
+    """Merge two normalised partial results (O, LSE) of disjoint key sets.
+
+    The combination of per-round softmax partials is the log-sum-exp rule:
+    lse = log(e^a + e^b); O = (e^a O_a + e^b O_b) / e^lse.  A side whose LSE
+    is -inf (no kept key) contributes nothing.  Written in numpy here (fp64)
+    because it is three lines; it is pinned in the tests by merging the
+    per-round results of every stripe back into the full attention.
+    """
+    o_a = np.asarray(o_a, dtype=np.float64)
+    o_b = np.asarray(o_b, dtype=np.float64)
+    lse_a = np.asarray(lse_a, dtype=np.float64)
+    lse_b = np.asarray(lse_b, dtype=np.float64)
+    m = np.maximum(lse_a, lse_b)
+    safe = np.where(np.isfinite(m), m, 0.0)
+    wa = np.exp(lse_a - safe)
+    wb = np.exp(lse_b - safe)
+    w = wa + wb
+    with np.errstate(divide="ignore", invalid="ignore"):
+        lse = np.where(np.isfinite(m), safe + np.log(w), -np.inf)
+        o = np.where(np.isfinite(m)[:, None],
+                     (wa[:, None] * o_a + wb[:, None] * o_b) / np.where(w > 0, w, 1.0)[:, None],
+                     o_a)
+    return o, lse
