@@ -1,0 +1,192 @@
+/*
+ * striped.h -- C ABI of libstriped: striped causal attention on one GB300.
+ *
+ * The method (pages on "Striped Attention: Faster Ring Attention for Causal
+ * Transformers"; research.elamur.ai summary page, §Summary and §Key points;
+ * pith.science paper page, abstract):
+ *   Ring Attention splits a causal sequence of S tokens over N devices in a
+ *   ring; key/value blocks circulate so that in round r (0 <= r < N) device d
+ *   attends to the key/value stripe of device e = (d - r) mod N.  With a
+ *   contiguous split the causal mask leaves some devices fully masked and
+ *   others fully kept in each round.  Striped Attention gives device d every
+ *   N-th token (positions p with p mod N == d), so each device keeps about
+ *   half of every round's work; the output is unchanged because attention is
+ *   permutation-equivariant and the permutation is applied once.
+ *
+ * This library runs the N virtual devices of that ring on ONE GPU: the
+ * stripes are slices of one tensor, a "send to the next device" is a pointer
+ * to the next stripe, and no collective is issued.
+ *
+ * Conventions shared by every entry point below:
+ *  - Tensors are caller-owned DEVICE pointers, [B, H, S, D] row-major with D
+ *    contiguous (16-byte aligned base).  Row order is given by `layout`:
+ *      STRIPED_LAYOUT_STRIPED:    row d*L + i holds position i*N + d
+ *      STRIPED_LAYOUT_CONTIGUOUS: row r holds position r (device d owns rows
+ *                                 [d*L, (d+1)*L))
+ *    with L = S / N.  LSE arrays are fp32 [B, H, S] in the same row order.
+ *  - dtype: STRIPED_BF16 (bf16 storage, fp32 accumulation, tensor cores) or
+ *    STRIPED_FP32 (fp32 storage and arithmetic on the CUDA cores).
+ *  - Every call is asynchronous on the caller's stream (a cudaStream_t passed
+ *    as void*; NULL is the legacy default stream) and allocates nothing.
+ *  - Every call returns an int status (STRIPED_OK or a negative code) and
+ *    never throws.  Launch failures return STRIPED_ERR_CUDA (the CUDA error
+ *    code is kept in striped_last_cuda_error()).  A device-side bounded wait
+ *    that expires records STRIPED_ERR_TIMEOUT in a device error word that
+ *    striped_check_error() reads back.
+ *  - `scale` multiplies the scores q.k (pass 1/sqrt(D) for the usual scaled
+ *    dot product).
+ *  - `tile_stats`, when not NULL, is an int64 [2][N][N] DEVICE array that
+ *    the kernels ADD their processed-tile counts to: [0][r][d] full tiles
+ *    and [1][r][d] partial (diagonal) tiles of round r on device d, summed
+ *    over all B*H heads.  Tiles are T x T with T from striped_kernel_tile();
+ *    fully masked tiles are skipped and not counted.
+ */
+#ifndef STRIPED_H
+#define STRIPED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define STRIPED_OK 0
+#define STRIPED_ERR_INVALID_ARG (-1) /* NULL pointer, S % N != 0, N < 1, sizes < 1, bad enum */
+#define STRIPED_ERR_UNSUPPORTED (-2) /* head dim / dtype combination not built */
+#define STRIPED_ERR_ALIGN (-3)       /* pointer or stride not 16-byte aligned */
+#define STRIPED_ERR_CUDA (-4)        /* a CUDA call failed; see striped_last_cuda_error() */
+#define STRIPED_ERR_TIMEOUT (-5)     /* a device-side bounded wait expired */
+#define STRIPED_ERR_WORKSPACE (-6)   /* workspace NULL or smaller than striped_workspace_size() */
+
+/* dtypes */
+#define STRIPED_BF16 0
+#define STRIPED_FP32 1
+
+/* row orders */
+#define STRIPED_LAYOUT_STRIPED 0
+#define STRIPED_LAYOUT_CONTIGUOUS 1
+
+/*
+ * Stripe permutation (§Summary "every N-th token"; §Key points: applied once
+ * before the model).  y[b,h,d*L+i,:] = x[b,h,i*N+d,:] for every d < N,
+ * i < L.  x and y are [B,H,S,D] device tensors of `dtype`; they must not
+ * overlap.  Requires S % N == 0 and D * sizeof(dtype) a power of two >= 16.
+ * Pure data movement: the result is a bit copy.
+ */
+int striped_permute(const void *x, void *y, int64_t B, int64_t H, int64_t S, int64_t D, int N,
+                    int dtype, void *stream);
+
+/* Inverse of striped_permute: y[b,h,i*N+d,:] = x[b,h,d*L+i,:]. */
+int striped_unpermute(const void *x, void *y, int64_t B, int64_t H, int64_t S, int64_t D, int N,
+                      int dtype, void *stream);
+
+/*
+ * Causal attention forward over all N ring rounds in one launch (§Summary:
+ * each device attends to every circulating key/value stripe; exact result,
+ * pith.science abstract).  For each query row of stripe d, rounds
+ * r = 0..N-1 visit key stripe e = (d - r) mod N; a (query local i, key local
+ * j) pair is kept iff the key's position <= the query's position, which in
+ * the striped layout is  j < i  or  (j == i and e <= d),  and in the
+ * contiguous layout is  e < d,  or  e == d and j <= i.  Fully masked tiles
+ * are skipped; partial results of all rounds are merged by the online
+ * softmax, so o = softmax(scale * q k^T + causal mask) v exactly up to
+ * rounding, and lse = natural-log log-sum-exp of each row's kept scores.
+ *  q, k, v: [B,H,S,D] `dtype` inputs in `layout` order.
+ *  o:       [B,H,S,D] `dtype` output.      lse: [B,H,S] fp32 output.
+ * bf16 requires D == 128; fp32 requires D % 8 == 0 and D <= 128.
+ */
+int striped_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                     int64_t H, int64_t S, int64_t D, int N, int layout, int dtype, float scale,
+                     int64_t *tile_stats, void *stream);
+
+/* Bytes of device workspace striped_attn_bwd needs (fp32 dQ accumulator and
+ * per-row softmax statistics), or 0 for invalid sizes. */
+size_t striped_workspace_size(int64_t B, int64_t H, int64_t S, int64_t D, int dtype);
+
+/*
+ * Backward of striped_attn_fwd (training use, §Summary).  Given the forward
+ * inputs, its outputs o and lse, and the output cotangent dO, writes
+ *   dq = scale * dS k,  dk = scale * dS^T q,  dv = P^T dO,
+ * with P = exp(scale q k^T - lse) on kept pairs, dS = P * (dO v^T - Delta)
+ * and Delta_p = <dO_p, o_p>.  Same tile skipping as the forward.
+ *  q,k,v,o,dO: [B,H,S,D] `dtype`;  lse: [B,H,S] fp32 from the forward.
+ *  dq,dk,dv:   [B,H,S,D] `dtype` outputs (fully overwritten).
+ *  workspace:  caller-owned device buffer of >= striped_workspace_size()
+ *              bytes, 256-byte aligned; its contents on entry are ignored.
+ */
+int striped_attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                     const void *dO, void *dq, void *dk, void *dv, void *workspace,
+                     size_t ws_bytes, int64_t B, int64_t H, int64_t S, int64_t D, int N,
+                     int layout, int dtype, float scale, int64_t *tile_stats, void *stream);
+
+/*
+ * One ring round of one virtual device (§Summary: per round, a device's
+ * query block attends to the key/value block it currently holds; the
+ * partial results are merged into running output statistics).
+ * Computes the partial result (O_r, LSE_r) of query stripe d against key
+ * stripe e under the mask of `layout` (see striped_attn_fwd), then merges it
+ * into the running accumulator with the log-sum-exp rule
+ *     lse' = log(exp(lse_acc) + exp(LSE_r)),
+ *     o'   = exp(lse_acc - lse') o_acc + exp(LSE_r - lse') O_r;
+ * a side whose LSE is -inf (no kept key yet) contributes nothing.  With
+ * first_round != 0 the accumulator is overwritten by (O_r, LSE_r).
+ *  q_d, k_e, v_e: stripe slices, L rows per (b,h), consecutive (b,h) slices
+ *                 `stride_bh` ELEMENTS apart (S*D for slices of a full
+ *                 [B,H,S,D] tensor); `dtype`.
+ *  o_acc:   fp32, same geometry and stride as q_d (running normalised O).
+ *  lse_acc: fp32, L per (b,h), `lse_stride_bh` elements apart (natural log).
+ *  o_out:   optional (NULL to skip) `dtype` copy of the merged O, same
+ *           geometry as q_d.
+ *  tile_stats gets this round's counts at [.][r][d] with r = (d - e) mod N.
+ */
+int ring_round_fwd(const void *q_d, const void *k_e, const void *v_e, float *o_acc, float *lse_acc,
+                   void *o_out, int d, int e, int64_t B, int64_t H, int64_t L, int64_t D, int N,
+                   int64_t stride_bh, int64_t lse_stride_bh, int layout, int dtype, float scale,
+                   int first_round, int64_t *tile_stats, void *stream);
+
+/* Tile edge T (queries x keys) the kernels for (dtype, D) skip and count
+ * with; writes *Tq and *Tk.  Returns STRIPED_ERR_UNSUPPORTED if no kernel. */
+int striped_kernel_tile(int dtype, int64_t D, int *Tq, int *Tk);
+
+/*
+ * Host-only, exact: per-(b,h) processed-tile table of the ring (§Summary
+ * and §Key points "Imbalance": per-round work per device).  full and
+ * partial are HOST int64 arrays [N rounds][N devices]; a Tq x Tk tile of
+ * round r on device d (keys of stripe e = (d - r) mod N) is "full" when all
+ * of its in-range pairs are kept, "partial" when some are, and not counted
+ * when none are.  Either output may be NULL.
+ */
+int striped_tile_counts(int64_t S, int N, int Tq, int Tk, int layout, int64_t *full,
+                        int64_t *partial);
+
+/* Host-only: modelled ring critical path = sum over rounds of the largest
+ * per-device tile count (each round runs at the pace of its slowest
+ * device, §Summary).  Returns < 0 (a status code) on invalid arguments. */
+int64_t striped_critical_path(int64_t S, int N, int Tq, int Tk, int layout);
+
+/* Synchronises `stream`, then reads and clears the device error word.
+ * Returns STRIPED_OK, STRIPED_ERR_TIMEOUT or STRIPED_ERR_CUDA. */
+int striped_check_error(void *stream);
+
+/* Human-readable name of a status code (static string). */
+const char *striped_status_string(int status);
+
+/* The cudaError_t of the last failed CUDA call made by the library. */
+int striped_last_cuda_error(void);
+
+/*
+ * Self-test of the device-side timeout path: launches one tiny kernel that
+ * waits, with a bound of `spins` polls, on a device flag that nothing sets;
+ * when the bound runs out it records STRIPED_ERR_TIMEOUT in the device error
+ * word and returns.  Read the result with striped_check_error().  No fault,
+ * trap or hang is involved.
+ */
+int striped_selftest_timeout(int64_t spins, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* STRIPED_H */

@@ -1,0 +1,286 @@
+// api.cu -- the C entry points of libstriped (declared in include/striped.h):
+// argument validation, status codes, tensor-map construction, the host-side
+// tile/critical-path model and the device error word.
+#include <stdio.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace striped {
+
+__device__ int g_error_word = 0;
+
+int *device_error_word() {
+    static int *cache[256] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return nullptr;
+    if (!cache[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_error_word) != cudaSuccess) return nullptr;
+        cache[dev] = static_cast<int *>(ptr);
+    }
+    return cache[dev];
+}
+
+static thread_local int t_last_cuda_error = 0;
+
+int cuda_status(cudaError_t err) {
+    if (err == cudaSuccess) return STRIPED_OK;
+    t_last_cuda_error = (int)err;
+    return STRIPED_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- tensor maps
+typedef CUresult (*EncodeTiledFnT)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+int make_bf16_map(CUtensorMap *map, const void *base, int64_t D, int64_t L, int64_t N, int64_t BH,
+                  int64_t stripe_stride, int64_t stride_bh, int box_rows) {
+    static EncodeTiledFnT fn = nullptr;
+    static int resolved = 0;
+    if (!resolved) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !ptr)
+            return cuda_status(e != cudaSuccess ? e : cudaErrorNotSupported);
+        fn = reinterpret_cast<EncodeTiledFnT>(ptr);
+        resolved = 1;
+    }
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[3] = {(cuuint64_t)(D * 2), (cuuint64_t)(stripe_stride * 2),
+                             (cuuint64_t)(stride_bh * 2)};
+    cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        t_last_cuda_error = (int)r;
+        return STRIPED_ERR_CUDA;
+    }
+    return STRIPED_OK;
+}
+
+// ---------------------------------------------------------------- validation
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int check_sizes(int64_t B, int64_t H, int64_t S, int64_t D, int N) {
+    if (B < 1 || H < 1 || S < 1 || D < 1 || N < 1) return STRIPED_ERR_INVALID_ARG;
+    if (S % N != 0) return STRIPED_ERR_INVALID_ARG;
+    if (S > (1ll << 31) || B * H > (1ll << 31)) return STRIPED_ERR_UNSUPPORTED;
+    return STRIPED_OK;
+}
+
+static int check_attn(int64_t B, int64_t H, int64_t S, int64_t D, int N, int layout, int dtype) {
+    int st = check_sizes(B, H, S, D, N);
+    if (st) return st;
+    if (layout != STRIPED_LAYOUT_STRIPED && layout != STRIPED_LAYOUT_CONTIGUOUS)
+        return STRIPED_ERR_INVALID_ARG;
+    if (dtype == STRIPED_BF16) {
+        if (D != 128) return STRIPED_ERR_UNSUPPORTED;
+    } else if (dtype == STRIPED_FP32) {
+        if (D % 8 != 0 || D > 128) return STRIPED_ERR_UNSUPPORTED;
+    } else {
+        return STRIPED_ERR_INVALID_ARG;
+    }
+    return STRIPED_OK;
+}
+
+static AttnGeom full_geom(int64_t B, int64_t H, int64_t S, int64_t D, int N, int layout, float scale) {
+    AttnGeom g;
+    g.BH = B * H;
+    g.L = S / N;
+    g.D = D;
+    g.N = N;
+    g.layout = layout;
+    g.stride_bh = S * D;
+    g.stripe_stride = g.L * D;
+    g.lse_stride_bh = S;
+    g.lse_stripe_stride = g.L;
+    g.scale = scale;
+    return g;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ---------------------------------------------------------------- device kernels (tiny)
+// A device word that nothing ever sets: the self-test waits on it.
+__device__ int g_selftest_flag = 0;
+
+__global__ void selftest_wait_kernel(int64_t spins) {
+    const volatile int *flag = &g_selftest_flag;
+    for (int64_t it = 0; it < spins; ++it)
+        if (*flag != 0) return;
+    atomicExch(&g_error_word, STRIPED_ERR_TIMEOUT);
+}
+
+}  // namespace striped
+
+using namespace striped;
+
+extern "C" {
+
+const char *striped_status_string(int status) {
+    switch (status) {
+        case STRIPED_OK: return "ok";
+        case STRIPED_ERR_INVALID_ARG: return "invalid argument";
+        case STRIPED_ERR_UNSUPPORTED: return "unsupported configuration";
+        case STRIPED_ERR_ALIGN: return "misaligned pointer or stride";
+        case STRIPED_ERR_CUDA: return "CUDA error";
+        case STRIPED_ERR_TIMEOUT: return "device wait timed out";
+        case STRIPED_ERR_WORKSPACE: return "workspace missing or too small";
+        default: return "unknown status";
+    }
+}
+
+int striped_last_cuda_error(void) { return t_last_cuda_error; }
+
+int striped_check_error(void *stream) {
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_status(e);
+    int word = 0, zero = 0;
+    e = cudaMemcpyFromSymbol(&word, g_error_word, sizeof(int));
+    if (e != cudaSuccess) return cuda_status(e);
+    if (word != 0) {
+        e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int));
+        if (e != cudaSuccess) return cuda_status(e);
+        return word;
+    }
+    return STRIPED_OK;
+}
+
+int striped_selftest_timeout(int64_t spins, void *stream) {
+    if (spins < 0) return STRIPED_ERR_INVALID_ARG;
+    selftest_wait_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(spins);
+    return cuda_status(cudaGetLastError());
+}
+
+int striped_kernel_tile(int dtype, int64_t D, int *Tq, int *Tk) {
+    if (!Tq || !Tk) return STRIPED_ERR_INVALID_ARG;
+    if (dtype == STRIPED_BF16 && D == 128) {
+        *Tq = *Tk = kTcTile;
+        return STRIPED_OK;
+    }
+    if (dtype == STRIPED_FP32 && D % 8 == 0 && D <= 128 && D > 0) {
+        *Tq = *Tk = kSimtTile;
+        return STRIPED_OK;
+    }
+    return STRIPED_ERR_UNSUPPORTED;
+}
+
+// ---------------------------------------------------------------- permutation
+static int permute_common(const void *x, void *y, int64_t B, int64_t H, int64_t S, int64_t D, int N,
+                          int dtype, void *stream, bool gather) {
+    if (!x || !y) return STRIPED_ERR_INVALID_ARG;
+    int st = check_sizes(B, H, S, D, N);
+    if (st) return st;
+    int64_t esize;
+    if (dtype == STRIPED_BF16) esize = 2;
+    else if (dtype == STRIPED_FP32) esize = 4;
+    else return STRIPED_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y)) return STRIPED_ERR_ALIGN;
+    if ((D * esize) % 16 != 0) return STRIPED_ERR_ALIGN;
+    const char *xb = (const char *)x, *yb = (const char *)y;
+    const int64_t bytes = B * H * S * D * esize;
+    if (xb < yb + bytes && yb < xb + bytes) return STRIPED_ERR_INVALID_ARG;  // overlap
+    return launch_stripe_permute(x, y, B * H, S, D * esize, N, gather, (cudaStream_t)stream);
+}
+
+int striped_permute(const void *x, void *y, int64_t B, int64_t H, int64_t S, int64_t D, int N,
+                    int dtype, void *stream) {
+    return permute_common(x, y, B, H, S, D, N, dtype, stream, true);
+}
+
+int striped_unpermute(const void *x, void *y, int64_t B, int64_t H, int64_t S, int64_t D, int N,
+                      int dtype, void *stream) {
+    return permute_common(x, y, B, H, S, D, N, dtype, stream, false);
+}
+
+// ---------------------------------------------------------------- attention
+int striped_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                     int64_t H, int64_t S, int64_t D, int N, int layout, int dtype, float scale,
+                     int64_t *tile_stats, void *stream) {
+    if (!q || !k || !v || !o || !lse) return STRIPED_ERR_INVALID_ARG;
+    int st = check_attn(B, H, S, D, N, layout, dtype);
+    if (st) return st;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return STRIPED_ERR_ALIGN;
+    const AttnGeom g = full_geom(B, H, S, D, N, layout, scale);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (dtype == STRIPED_FP32)
+        return launch_simt_fwd((const float *)q, (const float *)k, (const float *)v, (float *)o, lse, g,
+                               tile_stats, s);
+    return launch_tc_fwd(q, k, v, o, lse, g, tile_stats, s);
+}
+
+size_t striped_workspace_size(int64_t B, int64_t H, int64_t S, int64_t D, int dtype) {
+    if (B < 1 || H < 1 || S < 1 || D < 1) return 0;
+    const size_t rows = (size_t)(B * H * S);
+    if (dtype == STRIPED_FP32) return align256(rows * sizeof(float));
+    if (dtype == STRIPED_BF16) return align256(rows * (size_t)D * sizeof(float)) + align256(rows * sizeof(float));
+    return 0;
+}
+
+int striped_attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                     const void *dO, void *dq, void *dk, void *dv, void *workspace,
+                     size_t ws_bytes, int64_t B, int64_t H, int64_t S, int64_t D, int N,
+                     int layout, int dtype, float scale, int64_t *tile_stats, void *stream) {
+    if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return STRIPED_ERR_INVALID_ARG;
+    int st = check_attn(B, H, S, D, N, layout, dtype);
+    if (st) return st;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return STRIPED_ERR_ALIGN;
+    const size_t need = striped_workspace_size(B, H, S, D, dtype);
+    if (!workspace || ws_bytes < need) return STRIPED_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return STRIPED_ERR_ALIGN;
+    const AttnGeom g = full_geom(B, H, S, D, N, layout, scale);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (dtype == STRIPED_FP32)
+        return launch_simt_bwd((const float *)q, (const float *)k, (const float *)v, (const float *)o, lse,
+                               (const float *)dO, (float *)dq, (float *)dk, (float *)dv,
+                               (float *)workspace, g, tile_stats, s);
+    float *dq_acc = (float *)workspace;
+    float *delta = (float *)((char *)workspace + align256((size_t)(B * H * S * D) * sizeof(float)));
+    return launch_tc_bwd(q, k, v, o, lse, dO, dq, dk, dv, dq_acc, delta, g, tile_stats, s);
+}
+
+int ring_round_fwd(const void *q_d, const void *k_e, const void *v_e, float *o_acc, float *lse_acc,
+                   void *o_out, int d, int e, int64_t B, int64_t H, int64_t L, int64_t D, int N,
+                   int64_t stride_bh, int64_t lse_stride_bh, int layout, int dtype, float scale,
+                   int first_round, int64_t *tile_stats, void *stream) {
+    if (!q_d || !k_e || !v_e || !o_acc || !lse_acc) return STRIPED_ERR_INVALID_ARG;
+    if (L < 1) return STRIPED_ERR_INVALID_ARG;
+    int st = check_attn(B, H, L * N, D, N, layout, dtype);
+    if (st) return st;
+    if (d < 0 || d >= N || e < 0 || e >= N) return STRIPED_ERR_INVALID_ARG;
+    if (stride_bh < L * D || lse_stride_bh < L) return STRIPED_ERR_INVALID_ARG;
+    if (!aligned16(q_d) || !aligned16(k_e) || !aligned16(v_e) || !aligned16(o_acc) ||
+        (o_out && !aligned16(o_out)))
+        return STRIPED_ERR_ALIGN;
+    const int64_t esize = dtype == STRIPED_BF16 ? 2 : 4;
+    if ((stride_bh * esize) % 16 != 0 || (stride_bh * 4) % 16 != 0) return STRIPED_ERR_ALIGN;
+    AttnGeom g;
+    g.BH = B * H;
+    g.L = L;
+    g.D = D;
+    g.N = N;
+    g.layout = layout;
+    g.stride_bh = stride_bh;
+    g.stripe_stride = 0;
+    g.lse_stride_bh = lse_stride_bh;
+    g.lse_stripe_stride = 0;
+    g.scale = scale;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (dtype == STRIPED_FP32)
+        return launch_simt_round((const float *)q_d, (const float *)k_e, (const float *)v_e, o_acc, lse_acc,
+                                 (float *)o_out, d, e, first_round ? 1 : 0, g, tile_stats, s);
+    return launch_tc_round(q_d, k_e, v_e, o_acc, lse_acc, o_out, d, e, first_round ? 1 : 0, g, tile_stats,
+                           s);
+}
+
+}  // extern "C"

@@ -1,0 +1,393 @@
+// attn_simt.cu -- fp32 striped causal attention on the CUDA cores.
+//
+// The fp32 path keeps every product in fp32 (TF32 tensor cores would round
+// the operands to 10 mantissa bits).  Same method and schedule as the
+// tensor-core path: the query tile of virtual device d visits, in ring
+// rounds r = 0..N-1, the key stripe e = (d - r) mod N (research.elamur.ai
+// summary page, §Summary); fully masked tiles are skipped; the rounds are
+// merged by an online softmax, so the result is exact causal attention
+// (pith.science paper page, abstract).
+//
+// Block = kSimtTile query (or key) rows x 8 threads per row; each thread
+// owns D/8 of the head dimension and dot products are reduced over the 8
+// threads of a row with warp shuffles.  Key/value (or query/dO) tiles are
+// staged in shared memory.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace striped {
+
+namespace {
+
+constexpr int T = kSimtTile;
+constexpr int kTPR = 8;             // threads per row
+constexpr int kThreads = T * kTPR;  // 128
+constexpr int kMaxDPT = 16;         // D <= 128
+
+__device__ __forceinline__ float group_sum(float x) {
+    x += __shfl_xor_sync(0xffffffffu, x, 4);
+    x += __shfl_xor_sync(0xffffffffu, x, 2);
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    return x;
+}
+
+__device__ __forceinline__ int rows_in_tile(int64_t L, int t) {
+    const int64_t r = L - (int64_t)t * T;
+    return r >= T ? T : (int)r;
+}
+
+// Stage tile t of a stripe (T rows of D floats) into smem, zero beyond L.
+__device__ __forceinline__ void stage_rows(float *dst, const float *src_stripe, int64_t L, int64_t D,
+                                           int t) {
+    const int rows = rows_in_tile(L, t);
+    for (int idx = threadIdx.x; idx < T * D; idx += kThreads) {
+        const int r = idx / (int)D;
+        dst[idx] = (r < rows) ? src_stripe[((int64_t)t * T + r) * D + (idx - r * (int)D)] : 0.f;
+    }
+}
+
+struct RowState {
+    float m, l;
+    float acc[kMaxDPT];
+};
+
+// Online-softmax forward of query tile a of stripe d over rounds
+// [r_lo, r_hi) (e_fixed >= 0: the single key stripe e_fixed).
+__device__ void fwd_tile(const float *__restrict__ q_stripe, const float *__restrict__ k_head,
+                         const float *__restrict__ v_head, const AttnGeom &g, int d, int a, int r_lo,
+                         int r_hi, int e_fixed, RowState &st, int64_t *tile_stats, float *sK,
+                         float *sV) {
+    const int64_t L = g.L, D = g.D;
+    const int dpt = (int)D / kTPR;
+    const int row = threadIdx.x / kTPR, sub = threadIdx.x % kTPR;
+    const int nq = (int)((L + T - 1) / T);
+    const int rows_a = rows_in_tile(L, a);
+    const int64_t i = (int64_t)a * T + row;
+    float qreg[kMaxDPT];
+#pragma unroll
+    for (int c = 0; c < kMaxDPT; ++c)
+        qreg[c] = (c < dpt && i < L) ? q_stripe[i * D + sub * dpt + c] : 0.f;
+    st.m = -INFINITY;
+    st.l = 0.f;
+#pragma unroll
+    for (int c = 0; c < kMaxDPT; ++c) st.acc[c] = 0.f;
+
+    for (int r = r_lo; r < r_hi; ++r) {
+        const int e = e_fixed >= 0 ? e_fixed : (d - r + g.N) % g.N;
+        const RoundSpan sp = round_span(g.layout, d, e, a, nq, rows_a);
+        const int ntiles = sp.nfull + sp.has_diag;
+        if (tile_stats && threadIdx.x == 0 && ntiles > 0) {
+            const int rr = ring_round_of(d, e, g.N);
+            atomicAdd((unsigned long long *)&tile_stats[rr * g.N + d], (unsigned long long)sp.nfull);
+            atomicAdd((unsigned long long *)&tile_stats[g.N * g.N + rr * g.N + d],
+                      (unsigned long long)sp.has_diag);
+        }
+        const float *k_stripe = k_head + (int64_t)e * g.stripe_stride;
+        const float *v_stripe = v_head + (int64_t)e * g.stripe_stride;
+        for (int b = 0; b < ntiles; ++b) {
+            __syncthreads();
+            stage_rows(sK, k_stripe, L, D, b);
+            stage_rows(sV, v_stripe, L, D, b);
+            __syncthreads();
+            const int rows_b = rows_in_tile(L, b);
+            const bool diag = sp.has_diag && b == sp.nfull;
+            for (int c = 0; c < rows_b; ++c) {
+                float part = 0.f;
+#pragma unroll
+                for (int u = 0; u < kMaxDPT; ++u)
+                    if (u < dpt) part += qreg[u] * sK[c * D + sub * dpt + u];
+                const float s = g.scale * group_sum(part);
+                const bool keep = !diag || (c <= row + sp.diag_off);
+                if (!keep) continue;
+                const float m_new = fmaxf(st.m, s);
+                const float alpha = expf(st.m - m_new);  // exp(-inf) = 0 on the first key
+                const float p = expf(s - m_new);
+                st.l = st.l * alpha + p;
+#pragma unroll
+                for (int u = 0; u < kMaxDPT; ++u)
+                    if (u < dpt) st.acc[u] = st.acc[u] * alpha + p * sV[c * D + sub * dpt + u];
+                st.m = m_new;
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) simt_fwd_kernel(const float *__restrict__ q,
+                                                             const float *__restrict__ k,
+                                                             const float *__restrict__ v,
+                                                             float *__restrict__ o,
+                                                             float *__restrict__ lse, AttnGeom g,
+                                                             int64_t *tile_stats) {
+    extern __shared__ float smem[];
+    float *sK = smem, *sV = smem + T * g.D;
+    const int nq = (int)((g.L + T - 1) / T);
+    const int a = nq - 1 - (int)(blockIdx.x % nq);  // heavy query tiles first
+    const int d = (int)(blockIdx.x / nq);
+    const int64_t bh = blockIdx.y;
+    const float *q_stripe = q + bh * g.stride_bh + (int64_t)d * g.stripe_stride;
+    RowState st;
+    fwd_tile(q_stripe, k + bh * g.stride_bh, v + bh * g.stride_bh, g, d, a, 0, g.N, -1, st,
+             tile_stats, sK, sV);
+    const int row = threadIdx.x / kTPR, sub = threadIdx.x % kTPR;
+    const int64_t i = (int64_t)a * T + row;
+    if (i >= g.L) return;
+    const int dpt = (int)g.D / kTPR;
+    float *orow = o + bh * g.stride_bh + (int64_t)d * g.stripe_stride + i * g.D + sub * dpt;
+    const float inv = 1.f / st.l;
+    for (int u = 0; u < dpt; ++u) orow[u] = st.acc[u] * inv;
+    if (sub == 0)
+        lse[bh * g.lse_stride_bh + (int64_t)d * g.lse_stripe_stride + i] = st.m + logf(st.l);
+}
+
+__global__ void __launch_bounds__(kThreads) simt_round_kernel(
+    const float *__restrict__ q_d, const float *__restrict__ k_e, const float *__restrict__ v_e,
+    float *__restrict__ o_acc, float *__restrict__ lse_acc, float *__restrict__ o_out, int d, int e,
+    int first, AttnGeom g, int64_t *tile_stats) {
+    extern __shared__ float smem[];
+    float *sK = smem, *sV = smem + T * g.D;
+    const int nq = (int)((g.L + T - 1) / T);
+    const int a = nq - 1 - (int)blockIdx.x;
+    const int64_t bh = blockIdx.y;
+    RowState st;
+    // the launcher sets stripe_stride = 0: k_e / v_e are the stripe slices
+    fwd_tile(q_d + bh * g.stride_bh, k_e + bh * g.stride_bh, v_e + bh * g.stride_bh, g, d, a, 0, 1,
+             e, st, tile_stats, sK, sV);
+    const int row = threadIdx.x / kTPR, sub = threadIdx.x % kTPR;
+    const int64_t i = (int64_t)a * T + row;
+    if (i >= g.L) return;
+    const int dpt = (int)g.D / kTPR;
+    // this round's normalised partial result; LSE_r = -inf when nothing kept
+    const bool empty = !(st.l > 0.f);
+    const float lse_r = empty ? -INFINITY : st.m + logf(st.l);
+    float *acc_row = o_acc + bh * g.stride_bh + i * g.D + sub * dpt;
+    float *lse_ptr = lse_acc + bh * g.lse_stride_bh + i;
+    const float lse_a = first ? -INFINITY : *lse_ptr;
+    const float mx = fmaxf(lse_a, lse_r);
+    float wa = 0.f, wr = 0.f, lse_new = -INFINITY;
+    if (mx != -INFINITY) {
+        wa = expf(lse_a - mx);
+        wr = expf(lse_r - mx);
+        lse_new = mx + logf(wa + wr);
+        const float inv = 1.f / (wa + wr);
+        wa *= inv;
+        wr *= inv;
+    }
+    const float inv_l = empty ? 0.f : 1.f / st.l;
+    for (int u = 0; u < dpt; ++u) {
+        const float o_r = st.acc[u] * inv_l;
+        float val;
+        if (mx == -INFINITY) val = first ? 0.f : acc_row[u];
+        else val = (first ? 0.f : wa * acc_row[u]) + wr * o_r;
+        acc_row[u] = val;
+        if (o_out) o_out[bh * g.stride_bh + i * g.D + sub * dpt + u] = val;
+    }
+    __syncwarp();
+    if (sub == 0) *lse_ptr = lse_new;
+}
+
+// Delta_p = <dO_p, O_p>: one warp per row.
+__global__ void simt_delta_kernel(const float *__restrict__ o, const float *__restrict__ dO,
+                                  float *__restrict__ delta, int64_t rows, int64_t D) {
+    const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    if (row >= rows) return;
+    float s = 0.f;
+    for (int64_t c = lane; c < D; c += 32) s += o[row * D + c] * dO[row * D + c];
+    for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) delta[row] = s;
+}
+
+// dQ: query tile of stripe d, same schedule as the forward.
+__global__ void __launch_bounds__(kThreads) simt_dq_kernel(
+    const float *__restrict__ q, const float *__restrict__ k, const float *__restrict__ v,
+    const float *__restrict__ lse, const float *__restrict__ dO, const float *__restrict__ delta,
+    float *__restrict__ dq, AttnGeom g, int64_t *tile_stats) {
+    extern __shared__ float smem[];
+    float *sK = smem, *sV = smem + T * g.D;
+    const int64_t L = g.L, D = g.D;
+    const int nq = (int)((L + T - 1) / T);
+    const int a = nq - 1 - (int)(blockIdx.x % nq);
+    const int d = (int)(blockIdx.x / nq);
+    const int64_t bh = blockIdx.y;
+    const int dpt = (int)D / kTPR;
+    const int row = threadIdx.x / kTPR, sub = threadIdx.x % kTPR;
+    const int64_t i = (int64_t)a * T + row;
+    const bool valid = i < L;
+    const int64_t qoff = bh * g.stride_bh + (int64_t)d * g.stripe_stride + i * D + sub * dpt;
+    const int64_t soff = bh * g.lse_stride_bh + (int64_t)d * g.lse_stripe_stride + i;
+    float qreg[kMaxDPT], doreg[kMaxDPT], acc[kMaxDPT];
+#pragma unroll
+    for (int u = 0; u < kMaxDPT; ++u) {
+        qreg[u] = (u < dpt && valid) ? q[qoff + u] : 0.f;
+        doreg[u] = (u < dpt && valid) ? dO[qoff + u] : 0.f;
+        acc[u] = 0.f;
+    }
+    const float lse_i = valid ? lse[soff] : 0.f;
+    const float delta_i = valid ? delta[soff] : 0.f;
+    const int rows_a = rows_in_tile(L, a);
+    for (int r = 0; r < g.N; ++r) {
+        const int e = (d - r + g.N) % g.N;
+        const RoundSpan sp = round_span(g.layout, d, e, a, nq, rows_a);
+        const int ntiles = sp.nfull + sp.has_diag;
+        if (tile_stats && threadIdx.x == 0 && ntiles > 0) {
+            atomicAdd((unsigned long long *)&tile_stats[r * g.N + d], (unsigned long long)sp.nfull);
+            atomicAdd((unsigned long long *)&tile_stats[g.N * g.N + r * g.N + d],
+                      (unsigned long long)sp.has_diag);
+        }
+        const float *k_stripe = k + bh * g.stride_bh + (int64_t)e * g.stripe_stride;
+        const float *v_stripe = v + bh * g.stride_bh + (int64_t)e * g.stripe_stride;
+        for (int b = 0; b < ntiles; ++b) {
+            __syncthreads();
+            stage_rows(sK, k_stripe, L, D, b);
+            stage_rows(sV, v_stripe, L, D, b);
+            __syncthreads();
+            const int rows_b = rows_in_tile(L, b);
+            const bool diag = sp.has_diag && b == sp.nfull;
+            for (int c = 0; c < rows_b; ++c) {
+                float ps = 0.f, pp = 0.f;
+#pragma unroll
+                for (int u = 0; u < kMaxDPT; ++u)
+                    if (u < dpt) {
+                        ps += qreg[u] * sK[c * D + sub * dpt + u];
+                        pp += doreg[u] * sV[c * D + sub * dpt + u];
+                    }
+                const float s = g.scale * group_sum(ps);
+                const float dp = group_sum(pp);
+                const bool keep = valid && (!diag || (c <= row + sp.diag_off));
+                if (!keep) continue;
+                const float P = expf(s - lse_i);
+                const float dS = P * (dp - delta_i);
+#pragma unroll
+                for (int u = 0; u < kMaxDPT; ++u)
+                    if (u < dpt) acc[u] += dS * sK[c * D + sub * dpt + u];
+            }
+        }
+    }
+    if (!valid) return;
+    for (int u = 0; u < dpt; ++u) dq[qoff + u] = g.scale * acc[u];
+}
+
+// dK, dV: key tile b of stripe e; visits every query tile that sees it, in
+// ring order (round r: the key stripe sits on device d = e + r).
+__global__ void __launch_bounds__(kThreads) simt_dkdv_kernel(
+    const float *__restrict__ q, const float *__restrict__ k, const float *__restrict__ v,
+    const float *__restrict__ lse, const float *__restrict__ dO, const float *__restrict__ delta,
+    float *__restrict__ dk, float *__restrict__ dv, AttnGeom g) {
+    extern __shared__ float smem[];
+    float *sQ = smem, *sdO = smem + T * g.D;
+    float *sL = smem + 2 * T * g.D, *sDel = sL + T;
+    const int64_t L = g.L, D = g.D;
+    const int nq = (int)((L + T - 1) / T);
+    const int b = nq - 1 - (int)(blockIdx.x % nq);
+    const int e = (int)(blockIdx.x / nq);
+    const int64_t bh = blockIdx.y;
+    const int dpt = (int)D / kTPR;
+    const int row = threadIdx.x / kTPR, sub = threadIdx.x % kTPR;  // key row in the tile
+    const int64_t j = (int64_t)b * T + row;
+    const bool valid = j < L;
+    const int64_t koff = bh * g.stride_bh + (int64_t)e * g.stripe_stride + j * D + sub * dpt;
+    float kreg[kMaxDPT], vreg[kMaxDPT], ak[kMaxDPT], av[kMaxDPT];
+#pragma unroll
+    for (int u = 0; u < kMaxDPT; ++u) {
+        kreg[u] = (u < dpt && valid) ? k[koff + u] : 0.f;
+        vreg[u] = (u < dpt && valid) ? v[koff + u] : 0.f;
+        ak[u] = av[u] = 0.f;
+    }
+    const int rows_b = rows_in_tile(L, b);
+    for (int r = 0; r < g.N; ++r) {
+        const int d = (e + r) % g.N;
+        const QuerySpan sp = query_span(g.layout, d, e, b, nq, rows_b);
+        const float *q_stripe = q + bh * g.stride_bh + (int64_t)d * g.stripe_stride;
+        const float *do_stripe = dO + bh * g.stride_bh + (int64_t)d * g.stripe_stride;
+        const float *l_stripe = lse + bh * g.lse_stride_bh + (int64_t)d * g.lse_stripe_stride;
+        const float *dl_stripe = delta + bh * g.lse_stride_bh + (int64_t)d * g.lse_stripe_stride;
+        for (int a = sp.a_lo; a < nq; ++a) {
+            __syncthreads();
+            stage_rows(sQ, q_stripe, L, D, a);
+            stage_rows(sdO, do_stripe, L, D, a);
+            const int rows_a = rows_in_tile(L, a);
+            if (threadIdx.x < T) {
+                sL[threadIdx.x] = threadIdx.x < rows_a ? l_stripe[(int64_t)a * T + threadIdx.x] : 0.f;
+                sDel[threadIdx.x] =
+                    threadIdx.x < rows_a ? dl_stripe[(int64_t)a * T + threadIdx.x] : 0.f;
+            }
+            __syncthreads();
+            const bool diag = sp.has_diag && a == sp.a_lo;
+            for (int c = 0; c < rows_a; ++c) {  // c = query row in tile a
+                float ps = 0.f, pp = 0.f;
+#pragma unroll
+                for (int u = 0; u < kMaxDPT; ++u)
+                    if (u < dpt) {
+                        ps += kreg[u] * sQ[c * D + sub * dpt + u];
+                        pp += vreg[u] * sdO[c * D + sub * dpt + u];
+                    }
+                const float s = g.scale * group_sum(ps);
+                const float dp = group_sum(pp);
+                // pair (query row c, key row `row`) kept iff row <= c + diag_off
+                const bool keep = valid && (!diag || (row <= c + sp.diag_off));
+                if (!keep) continue;
+                const float P = expf(s - sL[c]);
+                const float dS = P * (dp - sDel[c]);
+#pragma unroll
+                for (int u = 0; u < kMaxDPT; ++u)
+                    if (u < dpt) {
+                        ak[u] += dS * sQ[c * D + sub * dpt + u];
+                        av[u] += P * sdO[c * D + sub * dpt + u];
+                    }
+            }
+        }
+    }
+    if (!valid) return;
+    for (int u = 0; u < dpt; ++u) {
+        dk[koff + u] = g.scale * ak[u];
+        dv[koff + u] = av[u];
+    }
+}
+
+}  // namespace
+
+int launch_simt_fwd(const float *q, const float *k, const float *v, float *o, float *lse,
+                    const AttnGeom &g, int64_t *tile_stats, cudaStream_t stream) {
+    const int nq = (int)((g.L + T - 1) / T);
+    dim3 grid((unsigned)(nq * g.N), (unsigned)g.BH);
+    const size_t smem = 2 * T * g.D * sizeof(float);
+    simt_fwd_kernel<<<grid, kThreads, smem, stream>>>(q, k, v, o, lse, g, tile_stats);
+    return cuda_status(cudaGetLastError());
+}
+
+int launch_simt_round(const float *q_d, const float *k_e, const float *v_e, float *o_acc,
+                      float *lse_acc, float *o_out, int d, int e, int first, const AttnGeom &g,
+                      int64_t *tile_stats, cudaStream_t stream) {
+    const int nq = (int)((g.L + T - 1) / T);
+    dim3 grid((unsigned)nq, (unsigned)g.BH);
+    const size_t smem = 2 * T * g.D * sizeof(float);
+    AttnGeom gs = g;
+    gs.stripe_stride = 0;
+    gs.lse_stripe_stride = 0;
+    simt_round_kernel<<<grid, kThreads, smem, stream>>>(q_d, k_e, v_e, o_acc, lse_acc, o_out, d, e,
+                                                        first, gs, tile_stats);
+    return cuda_status(cudaGetLastError());
+}
+
+int launch_simt_bwd(const float *q, const float *k, const float *v, const float *o,
+                    const float *lse, const float *dO, float *dq, float *dk, float *dv,
+                    float *delta_ws, const AttnGeom &g, int64_t *tile_stats, cudaStream_t stream) {
+    // full [BH][S][D] tensors: rows of all heads are contiguous
+    const int64_t rows = g.BH * g.N * g.L;
+    simt_delta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(o, dO, delta_ws, rows, g.D);
+    int st = cuda_status(cudaGetLastError());
+    if (st != STRIPED_OK) return st;
+    const int nq = (int)((g.L + T - 1) / T);
+    dim3 grid((unsigned)(nq * g.N), (unsigned)g.BH);
+    const size_t smem = 2 * T * g.D * sizeof(float);
+    simt_dq_kernel<<<grid, kThreads, smem, stream>>>(q, k, v, lse, dO, delta_ws, dq, g, tile_stats);
+    st = cuda_status(cudaGetLastError());
+    if (st != STRIPED_OK) return st;
+    simt_dkdv_kernel<<<grid, kThreads, smem + 2 * T * sizeof(float), stream>>>(q, k, v, lse, dO,
+                                                                               delta_ws, dk, dv, g);
+    return cuda_status(cudaGetLastError());
+}
+
+}  // namespace striped

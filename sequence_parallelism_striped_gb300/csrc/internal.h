@@ -1,0 +1,68 @@
+// internal.h -- declarations shared between the host entry points (api.cu)
+// and the kernel launchers.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "striped.h"
+
+namespace striped {
+
+// Records a failed CUDA call so striped_last_cuda_error() can report it and
+// maps it to a status code.
+int cuda_status(cudaError_t err);
+
+// Device address of the library's error word on the current device (where
+// bounded waits record STRIPED_ERR_TIMEOUT), or nullptr on failure.
+int *device_error_word();
+
+// Geometry of one attention launch.  Every tensor is addressed as
+// [BH][N stripes][L rows][D] with stripe e of head bh starting at element
+// bh*stride_bh + e*stripe_stride (stripe_stride = L*D for full tensors,
+// 0 when the pointers are already the stripe slices of one round).
+struct AttnGeom {
+    int64_t BH, L, D;
+    int N;
+    int layout;
+    int64_t stride_bh;          // elements between heads (q/k/v/o)
+    int64_t stripe_stride;      // elements between stripes
+    int64_t lse_stride_bh;      // elements between heads of lse
+    int64_t lse_stripe_stride;  // elements between stripes of lse
+    float scale;
+};
+
+// ---- permute.cu
+int launch_stripe_permute(const void *x, void *y, int64_t BH, int64_t S, int64_t row_bytes, int N,
+                          bool gather, cudaStream_t stream);
+
+// ---- attn_simt.cu (fp32 CUDA-core path, tile edge kSimtTile)
+constexpr int kSimtTile = 16;
+int launch_simt_fwd(const float *q, const float *k, const float *v, float *o, float *lse,
+                    const AttnGeom &g, int64_t *tile_stats, cudaStream_t stream);
+int launch_simt_round(const float *q_d, const float *k_e, const float *v_e, float *o_acc,
+                      float *lse_acc, float *o_out, int d, int e, int first, const AttnGeom &g,
+                      int64_t *tile_stats, cudaStream_t stream);
+int launch_simt_bwd(const float *q, const float *k, const float *v, const float *o,
+                    const float *lse, const float *dO, float *dq, float *dk, float *dv,
+                    float *delta_ws, const AttnGeom &g, int64_t *tile_stats, cudaStream_t stream);
+
+// ---- attn_fwd_tc.cu / attn_bwd_tc.cu (bf16 tensor-core path, tile 128)
+constexpr int kTcTile = 128;
+int launch_tc_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                  const AttnGeom &g, int64_t *tile_stats, cudaStream_t stream);
+int launch_tc_round(const void *q_d, const void *k_e, const void *v_e, float *o_acc, float *lse_acc,
+                    void *o_out, int d, int e, int first, const AttnGeom &g, int64_t *tile_stats,
+                    cudaStream_t stream);
+int launch_tc_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                  const void *dO, void *dq, void *dk, void *dv, float *dq_acc, float *delta,
+                  const AttnGeom &g, int64_t *tile_stats, cudaStream_t stream);
+
+// bf16 tensor viewed as [BH][N][L][D] -> 4-D tensor map with boxes of
+// 64 elements x box_rows rows, 128-byte swizzle, zero fill out of range.
+// Returns a status code.
+int make_bf16_map(CUtensorMap *map, const void *base, int64_t D, int64_t L, int64_t N, int64_t BH,
+                  int64_t stripe_stride, int64_t stride_bh, int box_rows);
+
+}  // namespace striped

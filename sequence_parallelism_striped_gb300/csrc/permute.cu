@@ -1,0 +1,78 @@
+// permute.cu -- stripe permutation of [B, H, S, D] tensors (HBM-bound copy).
+//
+// Striped Attention gives virtual device d every N-th token: positions
+// p = i*N + d, i < L = S/N ("every N-th token", research.elamur.ai summary
+// page, §Summary), applied once before the model (§Key points "Striped
+// layout").  Stripe-major row d*L + i therefore holds position i*N + d.
+//
+//   permute   (gather):  y[d*L + i] = x[i*N + d]
+//   unpermute (scatter): y[i*N + d] = x[d*L + i]
+//
+// One block moves a run of consecutive stripe rows of one (b, h) head; the
+// stripe index d is uniform per block (no per-element division).  Each row
+// is D*esize bytes moved as 16-byte vectors; a thread issues all its loads
+// before its stores so that every thread keeps several requests in flight.
+#include "common.cuh"
+#include "internal.h"
+
+namespace striped {
+
+constexpr int kPermThreads = 256;
+constexpr int kPermVecPerThread = 8;  // 16-byte vectors per thread per block
+
+template <bool kGather>
+__global__ void __launch_bounds__(kPermThreads) stripe_permute_kernel(
+    const uint4 *__restrict__ x, uint4 *__restrict__ y, int64_t S, int64_t L, int N, int vec_per_row_log2,
+    int rows_per_block, int blocks_per_stripe) {
+    const int64_t bh = blockIdx.y;
+    const int d = blockIdx.x / blocks_per_stripe;
+    const int64_t i0 = (int64_t)(blockIdx.x % blocks_per_stripe) * rows_per_block;
+    const int vpr = 1 << vec_per_row_log2;
+    const int64_t head = bh * S;  // row offset of this head
+    const int nvec = rows_per_block << vec_per_row_log2;
+
+    uint4 buf[kPermVecPerThread];
+    int64_t dst_idx[kPermVecPerThread];
+#pragma unroll
+    for (int u = 0; u < kPermVecPerThread; ++u) {
+        const int v = threadIdx.x + u * kPermThreads;
+        dst_idx[u] = -1;
+        if (v < nvec) {
+            const int64_t i = i0 + (v >> vec_per_row_log2);
+            const int c = v & (vpr - 1);
+            if (i < L) {
+                const int64_t striped_row = head + (int64_t)d * L + i;
+                const int64_t pos_row = head + i * N + d;
+                const int64_t src = (kGather ? pos_row : striped_row) * vpr + c;
+                dst_idx[u] = (kGather ? striped_row : pos_row) * vpr + c;
+                buf[u] = __ldg(x + src);
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kPermVecPerThread; ++u)
+        if (dst_idx[u] >= 0) y[dst_idx[u]] = buf[u];
+}
+
+int launch_stripe_permute(const void *x, void *y, int64_t BH, int64_t S, int64_t row_bytes, int N,
+                          bool gather, cudaStream_t stream) {
+    const int64_t L = S / N;
+    const int64_t vpr = row_bytes / 16;
+    int vlog = 0;
+    while ((1ll << vlog) < vpr) ++vlog;
+    if (vpr < 1 || (1ll << vlog) != vpr || vlog > 11) return STRIPED_ERR_UNSUPPORTED;
+    // rows per block such that the block moves kPermThreads*kPermVecPerThread vectors
+    const int rows_per_block = (kPermThreads * kPermVecPerThread) >> vlog;
+    const int64_t bps = (L + rows_per_block - 1) / rows_per_block;
+    if (bps * N > 0x7fffffffll || BH > 65535) return STRIPED_ERR_UNSUPPORTED;
+    dim3 grid((unsigned)(bps * N), (unsigned)BH);
+    if (gather)
+        stripe_permute_kernel<true><<<grid, kPermThreads, 0, stream>>>(
+            (const uint4 *)x, (uint4 *)y, S, L, N, vlog, rows_per_block, (int)bps);
+    else
+        stripe_permute_kernel<false><<<grid, kPermThreads, 0, stream>>>(
+            (const uint4 *)x, (uint4 *)y, S, L, N, vlog, rows_per_block, (int)bps);
+    return cuda_status(cudaGetLastError());
+}
+
+}  // namespace striped

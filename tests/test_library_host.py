@@ -1,0 +1,108 @@
+"""Host-side checks of libstriped (no GPU needed): the library builds,
+loads and exports every entry point of include/striped.h; the exact
+per-round tile table and critical path agree with the oracle's brute force
+and with the golden tables; argument validation rejects bad input before
+touching the device."""
+import ctypes
+import json
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import sequence_parallelism_striped_gb300 as sp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return sp.load()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "striped.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert "striped_attn_fwd" in names and "ring_round_fwd" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+@pytest.mark.parametrize("layout", [sp.STRIPED, sp.CONTIGUOUS])
+@pytest.mark.parametrize("S,N,Tq,Tk", [(256, 4, 16, 16), (1200, 4, 128, 128), (1028, 4, 128, 128),
+                                       (96, 8, 3, 3), (90, 3, 4, 7), (40, 8, 1, 1), (8192, 8, 128, 128),
+                                       (64, 1, 16, 16), (4, 4, 128, 128)])
+def test_tile_counts_match_oracle_bruteforce(lib, S, N, Tq, Tk, layout):
+    full, part = sp.tile_counts(S, N, Tq, Tk, layout)
+    bf, bp = oracle.tile_counts_bruteforce(S, N, Tq, Tk, layout)
+    assert np.array_equal(full, bf) and np.array_equal(part, bp)
+    assert sp.critical_path(S, N, Tq, Tk, layout) == oracle.critical_path(bf, bp)
+
+
+def test_golden_tables(lib):
+    gold = json.load(open(os.path.join(ROOT, "tests", "golden", "tile_counts.json")))
+    for w in gold["workloads"]:
+        S, N, T = w["S"], w["N"], w["T"]
+        for name, layout in (("striped", sp.STRIPED), ("contiguous", sp.CONTIGUOUS)):
+            full, part = sp.tile_counts(S, N, T, T, layout)
+            assert full.tolist() == w[name]["full"], (w["name"], name)
+            assert part.tolist() == w[name]["partial"], (w["name"], name)
+            assert sp.critical_path(S, N, T, T, layout) == w[name]["critical_path"]
+
+
+def test_kernel_tiles(lib):
+    import torch
+
+    assert sp.kernel_tile(torch.bfloat16, 128) == 128
+    assert sp.kernel_tile(torch.float32, 64) == 16
+    with pytest.raises(sp.StripedError):
+        sp.kernel_tile(torch.bfloat16, 96)
+
+
+def test_invalid_arguments_rejected_on_host(lib):
+    P = ctypes.c_void_p
+    fake = P(1 << 20)  # never dereferenced: validation fails first
+    # NULL pointers
+    assert lib.striped_attn_fwd(None, fake, fake, fake, fake, 1, 1, 64, 128, 4, 0, 0, 1.0, None, None) == -1
+    # S % N != 0
+    assert lib.striped_attn_fwd(fake, fake, fake, fake, fake, 1, 1, 66, 128, 4, 0, 0, 1.0, None, None) == -1
+    # unsupported head dim for bf16
+    assert lib.striped_attn_fwd(fake, fake, fake, fake, fake, 1, 1, 64, 96, 4, 0, 0, 1.0, None, None) == -2
+    # bad layout / dtype
+    assert lib.striped_attn_fwd(fake, fake, fake, fake, fake, 1, 1, 64, 128, 4, 7, 0, 1.0, None, None) == -1
+    assert lib.striped_attn_fwd(fake, fake, fake, fake, fake, 1, 1, 64, 128, 4, 0, 9, 1.0, None, None) == -1
+    # misaligned pointer
+    assert lib.striped_attn_fwd(P((1 << 20) + 2), fake, fake, fake, fake, 1, 1, 64, 128, 4, 0, 0, 1.0, None,
+                                None) == -3
+    # permute: overlapping buffers, bad sizes
+    assert lib.striped_permute(fake, fake, 1, 1, 64, 128, 4, 0, None) == -1
+    assert lib.striped_permute(fake, P((1 << 24)), 1, 1, 64, 128, 0, 0, None) == -1
+    # workspace too small
+    assert lib.striped_attn_bwd(fake, fake, fake, fake, fake, fake, fake, fake, fake, fake, 16, 1, 1, 64, 128,
+                                4, 0, 0, 1.0, None, None) == -6
+    # ring round: bad device index
+    assert lib.ring_round_fwd(fake, fake, fake, fake, fake, None, 5, 0, 1, 1, 16, 128, 4, 16 * 128, 16, 0, 0,
+                              1.0, 1, None, None) == -1
+    assert lib.striped_tile_counts(65, 4, 16, 16, 0, None, None) == -1
+    assert lib.striped_critical_path(64, 0, 16, 16, 0) < 0
+
+
+def test_workspace_size(lib):
+    import torch
+
+    B, H, S, D = 2, 3, 512, 128
+    n = sp.workspace_size(B, H, S, D, torch.bfloat16)
+    assert n >= B * H * S * D * 4 + B * H * S * 4 and n % 256 == 0
+    assert sp.workspace_size(1, 1, 256, 64, torch.float32) >= 256 * 4
+
+
+def test_status_strings(lib):
+    assert sp.status_string(0) == "ok"
+    assert "timed out" in sp.status_string(-5)
