@@ -21,9 +21,15 @@ namespace striped {
 // bounded waits; a timeout is recorded in the library's device error word
 // (owned by api.cu, passed to every kernel as a pointer)
 // --------------------------------------------------------------------------
-// Number of polls before a wait gives up.  Every legitimate wait in these
-// kernels is microseconds; this bound is seconds.
-constexpr uint32_t kSpinLimit = 1u << 26;
+// A wait gives up after this many nanoseconds of wall-clock time (read from
+// %globaltimer).  Every legitimate wait in these kernels is microseconds.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 
 __device__ __forceinline__ void record_timeout(int *err) {
     if (err) atomicExch(err, STRIPED_ERR_TIMEOUT);
@@ -154,8 +160,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Wait for the phase of parity `parity` to complete; false (and the device
 // error word set) if the bound ran out.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *err) {
-    for (uint32_t it = 0; it < kSpinLimit; ++it)
+    for (int it = 0; it < 64; ++it)
         if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 255u && global_timer_ns() - t0 > kWaitLimitNs) break;
+    }
     record_timeout(err);
     return false;
 }

@@ -1,0 +1,94 @@
+"""Forward parity on the GPU against the fp64 CPU oracle (on the unpermuted
+sequence), plus the per-round tile counters against the oracle's brute
+force.  Striped results are mapped back to position order on the host."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sequence_parallelism_striped_gb300 as sp
+from tests._util import TOL, head64, inputs, maxerr, to_layout, to_positions
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda")
+
+
+def _run_fwd(B, H, S, D, N, layout, dtype, seed=0):
+    x = inputs(B, H, S, D, dtype, seed=seed, with_do=False)
+    q, k, v = (to_layout(x[n], N, layout, DEV) for n in ("q", "k", "v"))
+    stats = sp.new_tile_stats(N, DEV)
+    o, lse = sp.striped_attn_fwd(q, k, v, N, layout, tile_stats=stats)
+    torch.cuda.synchronize()
+    assert sp.check_error() == 0
+    return x, o, lse, stats
+
+
+def _check_fwd(x, o, lse, stats, B, H, S, D, N, layout, dtype, heads=None):
+    scale = 1.0 / D ** 0.5
+    o_pos = to_positions(o, N, layout)
+    lse_pos = to_positions(lse[..., None], N, layout)[..., 0]
+    tol = TOL[dtype]
+    worst_o = worst_l = 0.0
+    for b in range(B):
+        for h in (range(H) if heads is None else heads):
+            o_ref, lse_ref = oracle.attn_fwd(head64(x["q"], b, h), head64(x["k"], b, h),
+                                             head64(x["v"], b, h), scale)
+            worst_o = max(worst_o, maxerr(o_pos[b, h], o_ref))
+            worst_l = max(worst_l, maxerr(lse_pos[b, h], lse_ref))
+    assert worst_o <= tol["o"], worst_o
+    assert worst_l <= tol["lse"], worst_l
+    T = sp.kernel_tile(dtype, D)
+    full, part = oracle.tile_counts_bruteforce(S, N, T, T, layout)
+    st = stats.cpu().numpy()
+    assert np.array_equal(st[0], B * H * full) and np.array_equal(st[1], B * H * part)
+    return worst_o, worst_l
+
+
+@pytest.mark.parametrize("layout", [sp.STRIPED, sp.CONTIGUOUS])
+@pytest.mark.parametrize("B,H,S,D,N", [(1, 1, 256, 64, 4), (1, 2, 4 * 37, 32, 4), (2, 1, 96, 128, 8),
+                                       (1, 1, 64, 64, 1), (1, 1, 16, 64, 16)])
+def test_fwd_fp32(B, H, S, D, N, layout):
+    x, o, lse, stats = _run_fwd(B, H, S, D, N, layout, torch.float32)
+    _check_fwd(x, o, lse, stats, B, H, S, D, N, layout, torch.float32)
+
+
+@pytest.mark.parametrize("layout", [sp.STRIPED, sp.CONTIGUOUS])
+@pytest.mark.parametrize("B,H,S,D,N", [(1, 2, 1200, 128, 4),   # L=300: 128+128+44 rows
+                                       (1, 1, 1028, 128, 4),   # L=257: last tile has one row
+                                       (2, 1, 512, 128, 4),    # L=128: one full tile
+                                       (1, 1, 256, 128, 4),    # L=64 < tile
+                                       (1, 1, 384, 128, 1),    # N=1: plain causal attention
+                                       (1, 1, 48, 128, 16)])   # L=3
+def test_fwd_bf16_small(B, H, S, D, N, layout):
+    x, o, lse, stats = _run_fwd(B, H, S, D, N, layout, torch.bfloat16, seed=1)
+    _check_fwd(x, o, lse, stats, B, H, S, D, N, layout, torch.bfloat16)
+
+
+@pytest.mark.parametrize("layout", [sp.STRIPED, sp.CONTIGUOUS])
+def test_fwd_bf16_short_sequence_full(layout):
+    """Short-sequence workload B=1, H=8, S=8192, D=128, N=8: every row."""
+    B, H, S, D, N = 1, 8, 8192, 128, 8
+    x, o, lse, stats = _run_fwd(B, H, S, D, N, layout, torch.bfloat16)
+    _check_fwd(x, o, lse, stats, B, H, S, D, N, layout, torch.bfloat16)
+
+
+def test_striped_equals_contiguous_after_unpermute():
+    """Permutation equivariance on the GPU path itself: striped output mapped
+    back to positions equals the contiguous-layout output."""
+    B, H, S, D, N = 1, 2, 2048, 128, 8
+    x = inputs(B, H, S, D, torch.bfloat16, seed=3, with_do=False)
+    q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
+    o_c, lse_c = sp.striped_attn_fwd(q, k, v, N, sp.CONTIGUOUS)
+    qs, ks, vs = (sp.striped_permute(t, N) for t in (q, k, v))
+    o_s, lse_s = sp.striped_attn_fwd(qs, ks, vs, N, sp.STRIPED)
+    o_back = sp.striped_unpermute(o_s, N)
+    assert maxerr(o_back.float().cpu(), o_c.float().cpu()) <= 2e-2
+    lse_back = to_positions(lse_s[..., None], N, sp.STRIPED)[..., 0]
+    assert maxerr(lse_back, lse_c.cpu().numpy()) <= 1e-3
+
+
+def test_first_position_attends_itself():
+    """Position 0 keeps one key: O_0 = v_0 (to bf16 rounding)."""
+    B, H, S, D, N = 1, 1, 1024, 128, 8
+    x, o, lse, stats = _run_fwd(B, H, S, D, N, sp.STRIPED, torch.bfloat16, seed=4)
+    assert maxerr(o[0, 0, 0].float().cpu(), x["v"][0, 0, 0].float()) <= 1e-2

@@ -1,0 +1,43 @@
+"""Stripe permutation on the GPU: bit-exact against the placement the oracle
+builds by enumeration ("every N-th token"), and round trip."""
+import pytest
+import torch
+
+import sequence_parallelism_striped_gb300 as sp
+from tests._util import positions
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("B,H,S,D,N", [(1, 1, 256, 64, 4), (2, 3, 1200, 128, 4), (1, 8, 8192, 128, 8),
+                                       (1, 2, 4096, 64, 16), (1, 1, 40, 128, 8), (1, 2, 384, 128, 1),
+                                       (1, 1, 48, 32, 48)])
+def test_permute_bit_exact(B, H, S, D, N, dtype):
+    dev = torch.device("cuda")
+    g = torch.Generator(device="cpu").manual_seed(123)
+    x = torch.randn(B, H, S, D, generator=g).to(dtype)
+    pos = torch.as_tensor(positions(S, N, sp.STRIPED))
+    ref = x[:, :, pos]  # row r holds position pos[r]
+    y = sp.striped_permute(x.to(dev), N)
+    assert torch.equal(y.cpu(), ref)
+    z = sp.striped_unpermute(y, N)
+    assert torch.equal(z.cpu(), x)
+
+
+def test_permute_full_size_long_context():
+    """Largest tensor of the benchmark workloads (B=1, H=32, S=262144,
+    D=128, bf16, N=8): sampled rows bit-exact, round trip exact."""
+    dev = torch.device("cuda")
+    B, H, S, D, N = 1, 32, 262144, 128, 8
+    g = torch.Generator(device=dev).manual_seed(5)
+    x = torch.randn(B, H, S, D, generator=g, device=dev).to(torch.bfloat16)
+    y = sp.striped_permute(x, N)
+    L = S // N
+    rows = torch.randint(0, S, (4096,), generator=torch.Generator().manual_seed(9))
+    heads = torch.randint(0, H, (4096,), generator=torch.Generator().manual_seed(10))
+    d, i = rows // L, rows % L
+    got = y[0, heads.to(dev), rows.to(dev)]
+    want = x[0, heads.to(dev), (i * N + d).to(dev)]
+    assert torch.equal(got, want)
+    assert torch.equal(sp.striped_unpermute(y, N), x)
