@@ -1,0 +1,345 @@
+"""Benchmark: striped causal attention fwd+bwd on GB300, one JSON line.
+
+A step is one pass of the whole hot path over one batch of synthetic input
+(long-context workload B=1, H=32, S=262144, D=128, N=8 stripes, bf16):
+permute Q, K, V, dO into the striped layout -> forward over all N ring
+rounds (with per-round tile counters) -> backward -> unpermute O, dQ, dK,
+dV.  The metric counts only unmasked FLOPs: 14 * D * B * H * S(S+1)/2 per
+step (4D per kept pair forward, 10D backward).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the fp64 CPU oracle (the only reference this method
+has) on a bounded causal-prefix sample of the same workload.
+Multi-GPU (torchrun): every rank runs an independent replica (the method's
+ring is emulated on one GPU; there is no data-path collective); value is the
+total over ranks / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal attn fwd+bwd TFLOP/s (unmasked FLOPs) and % of GB300 BF16 tensor peak"
+WORKLOAD = {"workload": "long-context striped causal attention fwd+bwd", "B": 1, "H": 32, "S": 262144,
+            "D": 128, "N": 8, "layout": "striped", "dtype": "bf16", "scale": "1/sqrt(D)",
+            "inputs": "Q,K,V,dO ~ N(0,1) seeded, generated on device",
+            "l2": "inputs larger than L2 (each tensor 2.1 GB > 129 MB)"}
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return {"bf16_tflops": float(m["bf16_tflops"]),
+                "bf16_tflops_sustained": float(m.get("bf16_tflops_sustained", m["bf16_tflops"])),
+                "hbm_gbs": float(m["hbm_gbs"]), "source": "measured"}
+    except Exception:
+        return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def _flops(B, H, S, D, per_pair):
+    return per_pair * D * B * H * S * (S + 1) / 2
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[3:7]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_oracle_sample(S_sample: int, D: int, seed: int = 0):
+    """Time the fp64 CPU oracle on a causal prefix of one head of the same
+    workload: forward + full backward over the first S_sample positions."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    g = torch.Generator().manual_seed(seed)
+    x = [torch.randn(S_sample, D, generator=g).to(torch.bfloat16).double().numpy() for _ in range(4)]
+    oracle.build()
+    threads = oracle.default_threads()
+    scale = 1.0 / D ** 0.5
+    t0 = time.perf_counter()
+    oracle.attn_fwd(x[0], x[1], x[2], scale, nthreads=threads)
+    oracle.attn_bwd(x[0], x[1], x[2], x[3], scale, nthreads=threads)
+    dt = time.perf_counter() - t0
+    fl = _flops(1, 1, S_sample, D, 14)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"fwd+bwd of one head over the causal prefix of the first {S_sample} positions "
+                      f"(D={D}, fp64), {fl:.3e} unmasked FLOP in {dt:.2f} s"}, dt
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle as it stands, on the host cores."""
+    if rank != 0:
+        return
+    samples = []
+    cb = None
+    for _ in range(max(args.warmup, 0)):
+        cpu_oracle_sample(4096, 128)
+    for _ in range(args.steps):
+        cb, dt = cpu_oracle_sample(args.cpu_sample, 128)
+        samples.append(dt)
+    ms = 1000.0 * statistics.mean(samples)
+    line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": dict(WORKLOAD),
+            "cpu_baseline": cb, "e2e": {"value": cb["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                                        "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+
+    import sequence_parallelism_striped_gb300 as sp
+    from seeded_inputs import device_inputs
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    sp.load(build_if_missing=True)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist  # noqa: F811
+
+        dist.init_process_group("nccl", device_id=dev)
+
+    B, H, S, D, N = (WORKLOAD[k] for k in ("B", "H", "S", "D", "N"))
+    x = device_inputs(B, H, S, D, torch.bfloat16, seed=rank, device=dev)
+    stream = torch.cuda.current_stream()
+    # preallocated buffers: the step allocates nothing
+    qs, ks, vs, dos = (torch.empty_like(x["q"]) for _ in range(4))
+    o = torch.empty_like(x["q"])
+    lse = torch.empty(B, H, S, dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(x["q"]) for _ in range(3))
+    outs = [torch.empty_like(x["q"]) for _ in range(4)]
+    ws = sp.new_workspace(B, H, S, D, torch.bfloat16, dev)
+    stats = sp.new_tile_stats(N, dev)
+    ev = {k: [] for k in ("fwd", "bwd", "perm")}
+
+    def step(record=False, layout=sp.STRIPED, src=None):
+        src = src if src is not None else x
+        if layout == sp.STRIPED:
+            e_p0 = torch.cuda.Event(enable_timing=True) if record else None
+            if record:
+                e_p0.record()
+            for name, dst in (("q", qs), ("k", ks), ("v", vs), ("do", dos)):
+                sp.striped_permute(src[name], N, out=dst)
+            q_, k_, v_, do_ = qs, ks, vs, dos
+        else:
+            q_, k_, v_, do_ = src["q"], src["k"], src["v"], src["do"]
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e2 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        sp.striped_attn_fwd(q_, k_, v_, N, layout, tile_stats=stats, out=o, lse_out=lse)
+        e1.record()
+        sp.striped_attn_bwd(q_, k_, v_, o, lse, do_, N, layout, workspace=ws, dq=dq, dk=dk, dv=dv)
+        e2.record()
+        if layout == sp.STRIPED:
+            for t, dst in zip((o, dq, dk, dv), outs):
+                sp.striped_unpermute(t, N, out=dst)
+        if record:
+            e3 = torch.cuda.Event(enable_timing=True)
+            e3.record()
+            ev["fwd"].append((e0, e1))
+            ev["bwd"].append((e1, e2))
+            if layout == sp.STRIPED:
+                ev["perm"].append((e_p0, e0, e2, e3))
+
+    for _ in range(args.warmup):
+        stats.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert sp.check_error() == 0
+    stats.zero_()
+
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                      else local_rank) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record()
+        for _ in range(args.steps):
+            step(record=True)
+        t_end.record()
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    ms_total = t_start.elapsed_time(t_end)
+    err = sp.check_error()
+    ms = torch.tensor([ms_total], device=dev, dtype=torch.float64)
+    if dist is not None:
+        dist.all_reduce(ms, op=dist.ReduceOp.MAX)
+    ms_step = float(ms.item()) / args.steps
+
+    fl_step = _flops(B, H, S, D, 14)
+    value = world * fl_step / (ms_step / 1000.0) / 1e12
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["fwd"])
+    bwd_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["bwd"])
+    perm_ms = statistics.mean(a.elapsed_time(b) + c.elapsed_time(d) for a, b, c, d in ev["perm"])
+    stats_np = stats.cpu().numpy() // args.steps  # counters of one step, all heads
+    T = sp.kernel_tile(torch.bfloat16, D)
+
+    # contiguous layout (Ring Attention placement) for comparison, 1-2 steps
+    contig = None
+    if args.compare:
+        step(layout=sp.CONTIGUOUS)
+        torch.cuda.synchronize()
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record()
+        nc = 2
+        for _ in range(nc):
+            step(layout=sp.CONTIGUOUS)
+        c1.record()
+        torch.cuda.synchronize()
+        cms = c0.elapsed_time(c1) / nc
+        contig = {"ms_per_step": cms, "tflops": fl_step / (cms / 1000.0) / 1e12}
+
+    # end to end through the C ABI with host buffers (pinned), copies timed
+    e2e = None
+    if args.e2e_steps > 0:
+        host_in = {k: torch.empty(x[k].shape, dtype=x[k].dtype, pin_memory=True) for k in ("q", "k", "v", "do")}
+        for k_ in host_in:
+            host_in[k_].copy_(x[k_])
+        host_out = [torch.empty(x["q"].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(4)]
+        dev_in = {k: torch.empty_like(x[k]) for k in host_in}
+        torch.cuda.synchronize()
+        h0 = torch.cuda.Event(enable_timing=True)
+        h1 = torch.cuda.Event(enable_timing=True)
+        h0.record()
+        for _ in range(args.e2e_steps):
+            for k_ in host_in:
+                dev_in[k_].copy_(host_in[k_], non_blocking=True)
+            step(src=dev_in)
+            for t, h in zip(outs, host_out):
+                h.copy_(t, non_blocking=True)
+        h1.record()
+        torch.cuda.synchronize()
+        e_ms = h0.elapsed_time(h1) / args.e2e_steps
+        bi = sum(t.numel() * t.element_size() for t in host_in.values())
+        bo = sum(t.numel() * t.element_size() for t in host_out)
+        e2e = {"value": world * fl_step / (e_ms / 1000.0) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
+               "d2h_bytes_per_step": bo, "ms_per_step": e_ms}
+        del host_in, host_out, dev_in
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    peaks = _peaks()
+    bwd_fl = _flops(B, H, S, D, 10)
+    bwd_achieved = bwd_fl / (bwd_ms / 1000.0) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(WORKLOAD, parallelism="replicas" if world > 1 else "single-gpu"),
+        "pct_of_peak": {"burst": value / world / peaks["bf16_tflops"],
+                        "sustained": value / world / peaks["bf16_tflops_sustained"],
+                        "peak_source": peaks["source"]},
+        "breakdown_ms": {"fwd": fwd_ms, "bwd": bwd_ms, "permute+unpermute": perm_ms,
+                         "fwd_tflops": _flops(B, H, S, D, 4) / (fwd_ms / 1000) / 1e12,
+                         "bwd_tflops": bwd_achieved},
+        "roofline": {"kernel": "striped_attn_bwd (tcgen05 main loop + Delta/dQ passes)", "bound": "tensor",
+                     "achieved": bwd_achieved, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                     "peak_kind": f"sustained bf16 ({peaks['source']})",
+                     "frac": bwd_achieved / peaks["bf16_tflops_sustained"], "traffic": None},
+        "tile_counts": {"T": T, "per_step_all_heads_full": int(stats_np[0].sum()),
+                        "per_step_all_heads_partial": int(stats_np[1].sum()),
+                        "critical_path_striped": sp.critical_path(S, N, T, T, sp.STRIPED),
+                        "critical_path_contiguous": sp.critical_path(S, N, T, T, sp.CONTIGUOUS)},
+        "gpu_launches": 12 * args.steps,
+        "device_error": err,
+    }
+    if contig is not None:
+        line["contiguous_layout"] = contig
+    if e2e is not None:
+        line["e2e"] = e2e
+    line["clocks"] = clk.summary()
+    if world == 1 and args.cpu_sample > 0:
+        cb, _ = cpu_oracle_sample(args.cpu_sample, D)
+        line["cpu_baseline"] = cb
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-sample", type=int, default=24576,
+                    help="causal-prefix length of the timed CPU-oracle sample (0 disables)")
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--no-compare", dest="compare", action="store_false")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.impl == "reference" else 1)))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_gpu(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,12 +1,496 @@
 // attn_bwd_tc.cu -- bf16 striped causal attention backward on tcgen05.
+//
+// The pages use the method to train causal models (research.elamur.ai
+// summary page, §Summary) but give no backward formulas; this is the
+// derivative of the exact causal attention the forward computes.  With
+// P = exp(scale q k^T - LSE) on kept pairs and Delta_p = <dO_p, O_p>:
+//   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - Delta),
+//   dK = scale * dS^T Q,  dQ = scale * dS K.
+// The same ring schedule and tile skipping as the forward: the key tile of
+// stripe e is visited, in ring rounds r = 0..N-1, by the query stripe of
+// device d = (e + r) mod N (the device that holds stripe e in round r).
+//
+// Three kernels:
+//   bwd_pre    Delta_p = <dO_p, O_p> (fp32) and zero the fp32 dQ accumulator
+//   bwd_main   one CTA per 128-key tile; loops over the query tiles that see
+//              it.  warp 0 = TMA producer (K, V once; Q_i, dO_i 2-stage
+//              ring), warp 1 = TMEM allocator + MMA issuer, warps 2..5 =
+//              compute (thread t owns key row t of S^T/dP^T and query row t
+//              of dQ).  TMEM: S^T [0,128) (P^T bf16 over it, then dQ_i),
+//              dP^T [128,256) (dS^T bf16 over it), dV [256,384), dK [384,512).
+//                S^T  = K Q_i^T      SS, both K-major
+//                dP^T = V dO_i^T     SS, both K-major
+//                dV  += P^T dO_i     TS, A = P^T in TMEM, B = dO_i MN-major
+//                dK  += dS^T Q_i     TS, A = dS^T in TMEM, B = Q_i MN-major
+//                dQ_i = dS K         SS, A = dS in smem MN-major, B = K MN-major
+//              dQ_i is added to the fp32 accumulator with vector reductions.
+//   bwd_post   dQ = bf16(scale * accumulator)
+#include <math.h>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace striped {
 
-int launch_tc_bwd(const void *, const void *, const void *, const void *, const float *, const void *, void *,
-                  void *, void *, float *, float *, const AttnGeom &, int64_t *, cudaStream_t) {
-    return STRIPED_ERR_UNSUPPORTED;
+namespace {
+
+constexpr int BT = 128, HD = 128;
+constexpr int QS = 2;  // Q/dO stages
+constexpr uint32_t kBox = 128 * 128;
+constexpr uint32_t kTile = 2 * kBox;
+constexpr uint32_t kKOff = 0;
+constexpr uint32_t kVOff = kTile;
+constexpr uint32_t kQOff = 2 * kTile;                 // stage s: Q at kQOff + s*2*kTile, dO after
+constexpr uint32_t kDSOff = kQOff + QS * 2 * kTile;   // dS (MN-major A operand)
+constexpr uint32_t kStatOff = kDSOff + kTile;         // [lse2 128 | delta 128] floats
+constexpr uint32_t kBarOff = kStatOff + 2 * 128 * 4;
+constexpr size_t kSmemBytes = 1024 + kBarOff + 256;
+static_assert(kSmemBytes <= 232448, "shared memory over the per-block limit");
+constexpr int kThreads = 192;
+
+struct BwdParams {
+    AttnGeom g;
+    const float *lse;    // [BH][S] natural log
+    const float *delta;  // [BH][S]
+    float *dq_acc;       // [BH][S][D] fp32
+    __nv_bfloat16 *dk, *dv;
+    int64_t *tile_stats;
+    int *err;
+};
+
+struct Bars {
+    uint64_t kv_full;
+    uint64_t q_full[QS];
+    uint64_t q_empty[QS];
+    uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, dq_free;
+    uint32_t tmem_slot;
+};
+
+__device__ __forceinline__ int tile_rows(int64_t L, int t) {
+    const int64_t r = L - (int64_t)t * BT;
+    return r >= BT ? BT : (int)r;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                  const BwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    Bars *bars = reinterpret_cast<Bars *>(smem + kBarOff);
+    float *sStat = reinterpret_cast<float *>(smem + kStatOff);
+    const uint32_t sbase = smem_u32(smem);
+    const AttnGeom &g = p.g;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int N = g.N;
+    const int nq = (int)((g.L + BT - 1) / BT);
+
+    // heaviest key tiles first: small b (and, contiguous, small e)
+    const int64_t id = blockIdx.x;
+    const int b = (int)(id / ((int64_t)N * g.BH));
+    const int e = (int)((id / g.BH) % N);
+    const int64_t bh = id % g.BH;
+    const int rows_b = tile_rows(g.L, b);
+
+    int nt = 0;
+    for (int r = 0; r < N; ++r) {
+        const QuerySpan sp = query_span(g.layout, (e + r) % N, e, b, nq, rows_b);
+        nt += nq - sp.a_lo;
+    }
+
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bars->kv_full), 1);
+        for (int s = 0; s < QS; ++s) {
+            mbar_init(smem_u32(&bars->q_full[s]), 1);
+            mbar_init(smem_u32(&bars->q_empty[s]), 1);
+        }
+        mbar_init(smem_u32(&bars->s_full), 1);
+        mbar_init(smem_u32(&bars->dp_full), 1);
+        mbar_init(smem_u32(&bars->p_ready), 4);
+        mbar_init(smem_u32(&bars->ds_ready), 4);
+        mbar_init(smem_u32(&bars->dq_full), 1);
+        mbar_init(smem_u32(&bars->dq_free), 4);
+        fence_barrier_init();
+        if (p.tile_stats) {
+            for (int r = 0; r < N; ++r) {
+                const int d = (e + r) % N;
+                const QuerySpan sp = query_span(g.layout, d, e, b, nq, rows_b);
+                const int cnt = nq - sp.a_lo;
+                if (cnt == 0) continue;
+                const int rr = ring_round_of(d, e, N);
+                atomicAdd((unsigned long long *)&p.tile_stats[rr * N + d],
+                          (unsigned long long)(cnt - sp.has_diag));
+                atomicAdd((unsigned long long *)&p.tile_stats[N * N + rr * N + d],
+                          (unsigned long long)sp.has_diag);
+            }
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&bars->tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_slot;
+    const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
+
+    if (warp == 0 && lane == 0 && nt > 0) {
+        // ---------------- TMA producer
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmdO);
+        const uint32_t kb = smem_u32(&bars->kv_full);
+        mbar_arrive_expect_tx(kb, 2 * kTile);
+        tma_load_4d(sbase + kKOff, &tmK, kb, 0, b * BT, e, (int)bh);
+        tma_load_4d(sbase + kKOff + kBox, &tmK, kb, 64, b * BT, e, (int)bh);
+        tma_load_4d(sbase + kVOff, &tmV, kb, 0, b * BT, e, (int)bh);
+        tma_load_4d(sbase + kVOff + kBox, &tmV, kb, 64, b * BT, e, (int)bh);
+        int i = 0;
+        bool ok = true;
+        for (int r = 0; r < N && ok; ++r) {
+            const int d = (e + r) % N;
+            const QuerySpan sp = query_span(g.layout, d, e, b, nq, rows_b);
+            for (int a = sp.a_lo; a < nq; ++a, ++i) {
+                const int s = i % QS;
+                if (i >= QS && !mbar_wait(smem_u32(&bars->q_empty[s]), ((i / QS) + 1) & 1, p.err)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = smem_u32(&bars->q_full[s]);
+                const uint32_t qdst = sbase + kQOff + s * 2 * kTile;
+                const uint32_t odst = qdst + kTile;
+                mbar_arrive_expect_tx(fb, 2 * kTile);
+                tma_load_4d(qdst, &tmQ, fb, 0, a * BT, d, (int)bh);
+                tma_load_4d(qdst + kBox, &tmQ, fb, 64, a * BT, d, (int)bh);
+                tma_load_4d(odst, &tmdO, fb, 0, a * BT, d, (int)bh);
+                tma_load_4d(odst + kBox, &tmdO, fb, 64, a * BT, d, (int)bh);
+            }
+        }
+    } else if (warp == 1 && lane == 0 && nt > 0) {
+        // ---------------- MMA issuer
+        constexpr uint32_t id_kk = idesc_bf16_f32(BT, BT, false, false);
+        constexpr uint32_t id_tmn = idesc_bf16_f32(BT, HD, false, true);
+        constexpr uint32_t id_mnmn = idesc_bf16_f32(BT, HD, true, true);
+        bool ok = mbar_wait(smem_u32(&bars->kv_full), 0, p.err);
+        for (int i = 0; i < nt && ok; ++i) {
+            const int s = i % QS;
+            if (!mbar_wait(smem_u32(&bars->q_full[s]), (i / QS) & 1, p.err)) break;
+            if (i > 0 && !mbar_wait(smem_u32(&bars->dq_free), (i - 1) & 1, p.err)) break;
+            tc_fence_after();
+            const uint32_t qaddr = sbase + kQOff + s * 2 * kTile;
+            const uint32_t oaddr = qaddr + kTile;
+            // S^T = K Q^T ; dP^T = V dO^T
+#pragma unroll
+            for (int kk = 0; kk < HD / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+                mma_ss(tS, sdesc_sw128(sbase + kKOff + off, 16, 1024), sdesc_sw128(qaddr + off, 16, 1024),
+                       id_kk, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(smem_u32(&bars->s_full));
+#pragma unroll
+            for (int kk = 0; kk < HD / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+                mma_ss(tdP, sdesc_sw128(sbase + kVOff + off, 16, 1024), sdesc_sw128(oaddr + off, 16, 1024),
+                       id_kk, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(smem_u32(&bars->dp_full));
+            // dV += P^T dO
+            if (!mbar_wait(smem_u32(&bars->p_ready), i & 1, p.err)) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < BT / 16; ++kk)
+                mma_ts(tdV, tS + kk * 8, sdesc_sw128(oaddr + kk * 2048, kBox, 1024), id_tmn,
+                       (i > 0 || kk > 0) ? 1u : 0u);
+            // dK += dS^T Q ; dQ = dS K
+            if (!mbar_wait(smem_u32(&bars->ds_ready), i & 1, p.err)) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < BT / 16; ++kk)
+                mma_ts(tdK, tdP + kk * 8, sdesc_sw128(qaddr + kk * 2048, kBox, 1024), id_tmn,
+                       (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < BT / 16; ++kk)
+                mma_ss(tS, sdesc_sw128(sbase + kDSOff + kk * 2048, kBox, 1024),
+                       sdesc_sw128(sbase + kKOff + kk * 2048, kBox, 1024), id_mnmn, kk > 0 ? 1u : 0u);
+            mma_commit(smem_u32(&bars->dq_full));
+            if (i + QS < nt) mma_commit(smem_u32(&bars->q_empty[s]));
+        }
+    } else if (warp >= 2) {
+        // ---------------- compute warpgroup
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;  // key row of S^T/dP^T; query row of dQ
+        const int ct = threadIdx.x - 64;      // 0..127
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const float cl2 = g.scale * 1.4426950408889634f;
+        const bool key_valid = row < rows_b;
+        int i = 0;
+        bool ok = true;
+        for (int r = 0; r < N && ok; ++r) {
+            const int d = (e + r) % N;
+            const QuerySpan sp = query_span(g.layout, d, e, b, nq, rows_b);
+            const int64_t srow0 = bh * g.lse_stride_bh + (int64_t)d * g.lse_stripe_stride;
+            for (int a = sp.a_lo; a < nq; ++a, ++i) {
+                // per-query statistics of this tile -> smem; the first barrier
+                // keeps the previous tile's readers ahead of the overwrite
+                float *sL = sStat, *sD = sStat + 128;
+                named_bar_sync(1, 128);
+                {
+                    const int64_t qi = (int64_t)a * BT + ct;
+                    const bool qv = qi < g.L;
+                    // an out-of-range query gets LSE = +inf, hence P = 0
+                    sL[ct] = qv ? p.lse[srow0 + qi] * 1.4426950408889634f : INFINITY;
+                    sD[ct] = qv ? p.delta[srow0 + qi] : 0.f;
+                }
+                named_bar_sync(1, 128);
+                const bool diag = sp.has_diag && a == sp.a_lo;
+                // keep pair (query col c, key row) iff row <= c + diag_off
+                const int cmin = diag ? row - sp.diag_off : 0;
+                // ---- P^T
+                if (!mbar_wait(smem_u32(&bars->s_full), i & 1, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float P[BT];
+#pragma unroll
+                for (int c = 0; c < BT / 32; ++c) {
+                    uint32_t rr[32];
+                    tmem_ld32(tS + lane_off + c * 32, rr);
+                    tmem_ld_wait(rr);
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) {
+                        const int col = c * 32 + u;
+                        const float pv = ex2(fmaf(__uint_as_float(rr[u]), cl2, -sL[col]));
+                        P[col] = (key_valid && col >= cmin) ? pv : 0.f;
+                    }
+                }
+                {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) pk[u] = pack_bf16x2(P[2 * u], P[2 * u + 1]);
+                    tmem_st32(tS + lane_off, pk);
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) pk[u] = pack_bf16x2(P[64 + 2 * u], P[64 + 2 * u + 1]);
+                    tmem_st32(tS + lane_off + 32, pk);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars->p_ready));
+                // ---- dS^T = P^T * (dP^T - Delta)
+                if (!mbar_wait(smem_u32(&bars->dp_full), i & 1, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint8_t *sDS = smem + kDSOff;
+#pragma unroll
+                for (int c = 0; c < BT / 32; ++c) {
+                    uint32_t rr[32];
+                    tmem_ld32(tdP + lane_off + c * 32, rr);
+                    tmem_ld_wait(rr);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        const int c0 = c * 32 + 2 * u;
+                        const float ds0 = P[c0] * (__uint_as_float(rr[2 * u]) - sD[c0]);
+                        const float ds1 = P[c0 + 1] * (__uint_as_float(rr[2 * u + 1]) - sD[c0 + 1]);
+                        pk[u] = pack_bf16x2(ds0, ds1);
+                    }
+                    // dS^T (bf16) over the dP^T columns already read: columns
+                    // c*16 .. c*16+15 hold query columns c*32 .. c*32+31
+                    asm volatile(
+                        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+                            tdP + lane_off + c * 16),
+                        "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]), "r"(pk[6]),
+                        "r"(pk[7]), "r"(pk[8]), "r"(pk[9]), "r"(pk[10]), "r"(pk[11]), "r"(pk[12]),
+                        "r"(pk[13]), "r"(pk[14]), "r"(pk[15])
+                        : "memory");
+                    // dS into smem as the MN-major A operand of dQ = dS K:
+                    // key row `row`, query columns c*32 .. c*32+31 = 4 chunks
+                    // of 8 in box (c >> 1), chunk index ((c & 1) * 4 + v)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const int chunk = (c & 1) * 4 + v;
+                        const uint32_t off = (uint32_t)(c >> 1) * kBox + (uint32_t)row * 128u +
+                                             (uint32_t)((chunk ^ (row & 7)) * 16);
+                        *reinterpret_cast<uint4 *>(sDS + off) =
+                            make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    }
+                }
+                tmem_st_wait();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready));
+                // ---- dQ_i readout -> fp32 accumulator
+                if (!mbar_wait(smem_u32(&bars->dq_full), i & 1, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float dqv[HD];
+#pragma unroll
+                for (int c = 0; c < HD / 32; ++c) {
+                    uint32_t rr[32];
+                    tmem_ld32(tS + lane_off + c * 32, rr);
+                    tmem_ld_wait(rr);
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) dqv[c * 32 + u] = __uint_as_float(rr[u]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
+                const int64_t qi = (int64_t)a * BT + row;
+                if (qi < g.L) {
+                    float *dst = p.dq_acc + (bh * g.stride_bh + (int64_t)d * g.stripe_stride + qi * HD);
+#pragma unroll
+                    for (int v = 0; v < HD / 4; ++v)
+                        red_add_v4(dst + 4 * v, dqv[4 * v], dqv[4 * v + 1], dqv[4 * v + 2], dqv[4 * v + 3]);
+                }
+            }
+        }
+        // ---------------- epilogue: dK, dV of this key tile
+        const int64_t kj = (int64_t)b * BT + row;
+        const int64_t krow = bh * g.stride_bh + (int64_t)e * g.stripe_stride + kj * HD;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+            const uint32_t tacc = which ? tdK : tdV;
+            __nv_bfloat16 *outp = which ? p.dk : p.dv;
+            const float mul = which ? g.scale : 1.f;
+#pragma unroll
+            for (int c = 0; c < HD / 32; ++c) {
+                uint32_t rr[32];
+                if (nt > 0 && ok) {
+                    tmem_ld32(tacc + lane_off + c * 32, rr);
+                    tmem_ld_wait(rr);
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) rr[u] = 0u;
+                }
+                if (kj < g.L) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(outp + krow + c * 32);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(rr[8 * v + 0]) * mul, __uint_as_float(rr[8 * v + 1]) * mul);
+                        w.y = pack_bf16x2(__uint_as_float(rr[8 * v + 2]) * mul, __uint_as_float(rr[8 * v + 3]) * mul);
+                        w.z = pack_bf16x2(__uint_as_float(rr[8 * v + 4]) * mul, __uint_as_float(rr[8 * v + 5]) * mul);
+                        w.w = pack_bf16x2(__uint_as_float(rr[8 * v + 6]) * mul, __uint_as_float(rr[8 * v + 7]) * mul);
+                        dst[v] = w;
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// Delta_p = <dO_p, O_p> (fp32) and a zeroed dQ accumulator row; one warp
+// per row of D = 128 (each lane: 4 elements of dO/O, 4 floats of dQ).
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o,
+                                                      const __nv_bfloat16 *__restrict__ dO,
+                                                      float *__restrict__ delta, float *__restrict__ dq_acc,
+                                                      int64_t rows) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t rw = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); rw < rows; rw += nwarps) {
+        const uint2 ov = *reinterpret_cast<const uint2 *>(o + rw * HD + lane * 4);
+        const uint2 gv = *reinterpret_cast<const uint2 *>(dO + rw * HD + lane * 4);
+        const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&ov);
+        const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&gv);
+        float2 a0 = __bfloat1622float2(o2[0]), a1 = __bfloat1622float2(o2[1]);
+        float2 b0 = __bfloat1622float2(g2[0]), b1 = __bfloat1622float2(g2[1]);
+        float s = a0.x * b0.x + a0.y * b0.y + a1.x * b1.x + a1.y * b1.y;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        if (lane == 0) delta[rw] = s;
+        *reinterpret_cast<float4 *>(dq_acc + rw * HD + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+// dQ = bf16(scale * accumulator), 8 elements per thread per step.
+__global__ void __launch_bounds__(256) bwd_post_kernel(const float *__restrict__ dq_acc,
+                                                       __nv_bfloat16 *__restrict__ dq, int64_t n8, float scale) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n8; t += stride) {
+        const float4 x = reinterpret_cast<const float4 *>(dq_acc)[2 * t];
+        const float4 y = reinterpret_cast<const float4 *>(dq_acc)[2 * t + 1];
+        uint4 w;
+        w.x = pack_bf16x2(x.x * scale, x.y * scale);
+        w.y = pack_bf16x2(x.z * scale, x.w * scale);
+        w.z = pack_bf16x2(y.x * scale, y.y * scale);
+        w.w = pack_bf16x2(y.z * scale, y.w * scale);
+        reinterpret_cast<uint4 *>(dq)[t] = w;
+    }
+}
+
+int num_sms() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 152;
+    }
+    return n;
+}
+
+}  // namespace
+
+int launch_tc_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                  const void *dO, void *dq, void *dk, void *dv, float *dq_acc, float *delta,
+                  const AttnGeom &g, int64_t *tile_stats, cudaStream_t stream) {
+    static int attr = 1;
+    if (attr == 1) {
+        cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytes);
+        attr = cuda_status(e);
+    }
+    if (attr != STRIPED_OK) return attr;
+    const int64_t rows = g.BH * g.N * g.L;
+    const int sms = num_sms();
+    bwd_pre_kernel<<<sms * 8, 256, 0, stream>>>((const __nv_bfloat16 *)o, (const __nv_bfloat16 *)dO, delta,
+                                                dq_acc, rows);
+    int st = cuda_status(cudaGetLastError());
+    if (st != STRIPED_OK) return st;
+    CUtensorMap mq, mk, mv, mdo;
+    if ((st = make_bf16_map(&mq, q, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 128)) ||
+        (st = make_bf16_map(&mk, k, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 128)) ||
+        (st = make_bf16_map(&mv, v, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 128)) ||
+        (st = make_bf16_map(&mdo, dO, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 128)))
+        return st;
+    BwdParams p{};
+    p.g = g;
+    p.lse = lse;
+    p.delta = delta;
+    p.dq_acc = dq_acc;
+    p.dk = (__nv_bfloat16 *)dk;
+    p.dv = (__nv_bfloat16 *)dv;
+    p.tile_stats = tile_stats;
+    p.err = device_error_word();
+    const int64_t nk = (g.L + BT - 1) / BT;
+    const int64_t nblocks = nk * g.N * g.BH;
+    if (nblocks > 0x7fffffffll) return STRIPED_ERR_UNSUPPORTED;
+    tc_bwd_kernel<<<(unsigned)nblocks, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
+    st = cuda_status(cudaGetLastError());
+    if (st != STRIPED_OK) return st;
+    bwd_post_kernel<<<sms * 8, 256, 0, stream>>>(dq_acc, (__nv_bfloat16 *)dq, rows * HD / 8, g.scale);
+    return cuda_status(cudaGetLastError());
 }
 
 }  // namespace striped

@@ -38,6 +38,7 @@ constexpr uint32_t kKVOff = kTileBytes;
 constexpr uint32_t kStageBytes = 2 * kTileBytes;  // K + V
 constexpr uint32_t kBarOff = kKVOff + NS * kStageBytes;
 constexpr size_t kSmemBytes = 1024 + kBarOff + 256;
+static_assert(kSmemBytes <= 232448, "shared memory over the per-block limit");
 constexpr int kThreads = 192;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
