@@ -156,6 +156,11 @@ def run_gpu(args, rank, world, local_rank):
 
         dist.init_process_group("nccl", device_id=dev)
 
+    for key in ("B", "H", "S", "N"):
+        if getattr(args, key) is not None:
+            WORKLOAD[key] = getattr(args, key)
+    if any(getattr(args, key) is not None for key in ("B", "H", "S", "N")):
+        WORKLOAD["workload"] = "striped causal attention fwd+bwd (reduced profiling case)"
     B, H, S, D, N = (WORKLOAD[k] for k in ("B", "H", "S", "D", "N"))
     x = device_inputs(B, H, S, D, torch.bfloat16, seed=rank, device=dev)
     stream = torch.cuda.current_stream()
@@ -331,6 +336,8 @@ def main():
                     help="causal-prefix length of the timed CPU-oracle sample (0 disables)")
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-compare", dest="compare", action="store_false")
+    for key in ("B", "H", "S", "N"):
+        ap.add_argument(f"--{key}", type=int, default=None, help="override the workload (profiling cases)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.impl == "reference" else 1)))
