@@ -122,6 +122,27 @@ int striped_attn_bwd(const void *q, const void *k, const void *v, const void *o,
                      int layout, int dtype, float scale, int64_t *tile_stats, void *stream);
 
 /*
+ * striped_attn_bwd for callers that cannot allocate device memory (the paper
+ * has no counterpart; this is a library convenience).  Same arguments,
+ * results and tile counters as striped_attn_bwd, minus the workspace: the
+ * scratch lives in a fixed 48 MiB device array inside the library, present
+ * on every GPU that loads it until the process exits.  For callers whose
+ * device memory is owned by an allocator or budget they cannot extend, or
+ * who must keep cudaMalloc off their hot path.
+ *  - Returns STRIPED_ERR_WORKSPACE when striped_workspace_size(B,H,S,D,dtype)
+ *    exceeds 48 MiB (bf16, D = 128: B*H*S up to about 97,000 rows).
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - All calls on one device share the array: calls that overlap on the GPU
+ *    race and give wrong results.  Nothing needs clearing by the caller.
+ */
+int striped_attn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                             const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                             int64_t B, int64_t H, int64_t S, int64_t D, int N, int layout,
+                             int dtype, float scale, int64_t *tile_stats, void *stream);
+
+/*
  * One ring round of one virtual device (§Summary: per round, a device's
  * query block attends to the key/value block it currently holds; the
  * partial results are merged into running output statistics).
