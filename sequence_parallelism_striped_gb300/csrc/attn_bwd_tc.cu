@@ -14,10 +14,12 @@
 //   bwd_pre    Delta_p = <dO_p, O_p> (fp32) and zero the fp32 dQ accumulator
 //   bwd_main   one CTA per 128-key tile; loops over the query tiles that see
 //              it.  warp 0 = TMA producer (K, V once; Q_i, dO_i 2-stage
-//              ring), warp 1 = TMEM allocator + MMA issuer, warps 2..5 =
-//              compute (thread t owns key row t of S^T/dP^T and query row t
-//              of dQ).  TMEM: S^T [0,128) (P^T bf16 over it, then dQ_i),
-//              dP^T [128,256) (dS^T bf16 over it), dV [256,384), dK [384,512).
+//              ring), warp 1 = TMEM allocator + MMA issuer, warps 4..11 =
+//              two compute warpgroups; thread t of a warpgroup owns key row
+//              t of S^T/dP^T (query row t of dQ), warpgroup 0 columns
+//              0..63 and warpgroup 1 columns 64..127.  TMEM: S^T [0,128)
+//              (P^T bf16 pairs over it, then dQ_i), dP^T [128,256) (dS^T
+//              bf16 pairs over it), dV [256,384), dK [384,512).
 //                S^T  = K Q_i^T      SS, both K-major
 //                dP^T = V dO_i^T     SS, both K-major
 //                dV  += P^T dO_i     TS, A = P^T in TMEM, B = dO_i MN-major
@@ -42,11 +44,11 @@ constexpr uint32_t kKOff = 0;
 constexpr uint32_t kVOff = kTile;
 constexpr uint32_t kQOff = 2 * kTile;                 // stage s: Q at kQOff + s*2*kTile, dO after
 constexpr uint32_t kDSOff = kQOff + QS * 2 * kTile;   // dS (MN-major A operand)
-constexpr uint32_t kStatOff = kDSOff + kTile;         // [lse2 128 | delta 128] floats
+constexpr uint32_t kStatOff = kDSOff + kTile;         // per warpgroup: [lse2 64 | delta 64] floats
 constexpr uint32_t kBarOff = kStatOff + 2 * 128 * 4;
 constexpr size_t kSmemBytes = 1024 + kBarOff + 256;
 static_assert(kSmemBytes <= 232448, "shared memory over the per-block limit");
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 4..11 compute
 
 struct BwdParams {
     AttnGeom g;
@@ -90,18 +92,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int N = g.N;
     const int nq = (int)((g.L + BT - 1) / BT);
 
-    // heaviest key tiles first: small b (and, contiguous, small e)
+    // Head-major order: resident CTAs belong to one head and sweep its query
+    // tiles in the same order, sharing Q/dO tiles and dQ accumulator lines
+    // in L2.  Within a head the heaviest key tiles (small b) go first.
     const int64_t id = blockIdx.x;
-    const int b = (int)(id / ((int64_t)N * g.BH));
-    const int e = (int)((id / g.BH) % N);
-    const int64_t bh = id % g.BH;
+    const int64_t per_head = (int64_t)nq * N;
+    const int64_t bh = id / per_head;
+    const int rem = (int)(id % per_head);
+    const int b = rem / N;
+    const int e = rem % N;
     const int rows_b = tile_rows(g.L, b);
 
     int nt = 0;
-    for (int r = 0; r < N; ++r) {
-        const QuerySpan sp = query_span(g.layout, (e + r) % N, e, b, nq, rows_b);
-        nt += nq - sp.a_lo;
-    }
+    for (int d = 0; d < N; ++d) nt += nq - query_span(g.layout, d, e, b, nq, rows_b).a_lo;
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bars->kv_full), 1);
@@ -111,14 +114,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(smem_u32(&bars->s_full), 1);
         mbar_init(smem_u32(&bars->dp_full), 1);
-        mbar_init(smem_u32(&bars->p_ready), 4);
-        mbar_init(smem_u32(&bars->ds_ready), 4);
+        mbar_init(smem_u32(&bars->p_ready), 8);
+        mbar_init(smem_u32(&bars->ds_ready), 8);
         mbar_init(smem_u32(&bars->dq_full), 1);
-        mbar_init(smem_u32(&bars->dq_free), 4);
+        mbar_init(smem_u32(&bars->dq_free), 8);
         fence_barrier_init();
         if (p.tile_stats) {
-            for (int r = 0; r < N; ++r) {
-                const int d = (e + r) % N;
+            for (int d = 0; d < N; ++d) {
                 const QuerySpan sp = query_span(g.layout, d, e, b, nq, rows_b);
                 const int cnt = nq - sp.a_lo;
                 if (cnt == 0) continue;
@@ -154,10 +156,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(sbase + kVOff + kBox, &tmV, kb, 64, b * BT, e, (int)bh);
         int i = 0;
         bool ok = true;
-        for (int r = 0; r < N && ok; ++r) {
-            const int d = (e + r) % N;
+        for (int d = 0; d < N && ok; ++d) {
             const QuerySpan sp = query_span(g.layout, d, e, b, nq, rows_b);
-            for (int a = sp.a_lo; a < nq; ++a, ++i) {
+            for (int a = nq - 1; a >= sp.a_lo; --a, ++i) {
                 const int s = i % QS;
                 if (i >= QS && !mbar_wait(smem_u32(&bars->q_empty[s]), ((i / QS) + 1) & 1, p.err)) {
                     ok = false;
@@ -201,20 +202,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                        id_kk, kk > 0 ? 1u : 0u);
             }
             mma_commit(smem_u32(&bars->dp_full));
-            // dV += P^T dO
+            // dV += P^T dO: P^T (bf16 pairs) sits in TMEM columns [0,32) for
+            // queries 0..63 and [64,96) for queries 64..127
             if (!mbar_wait(smem_u32(&bars->p_ready), i & 1, p.err)) break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < BT / 16; ++kk)
-                mma_ts(tdV, tS + kk * 8, sdesc_sw128(oaddr + kk * 2048, kBox, 1024), id_tmn,
-                       (i > 0 || kk > 0) ? 1u : 0u);
+                mma_ts(tdV, tS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+                       sdesc_sw128(oaddr + kk * 2048, kBox, 1024), id_tmn, (i > 0 || kk > 0) ? 1u : 0u);
             // dK += dS^T Q ; dQ = dS K
             if (!mbar_wait(smem_u32(&bars->ds_ready), i & 1, p.err)) break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < BT / 16; ++kk)
-                mma_ts(tdK, tdP + kk * 8, sdesc_sw128(qaddr + kk * 2048, kBox, 1024), id_tmn,
-                       (i > 0 || kk > 0) ? 1u : 0u);
+                mma_ts(tdK, tdP + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+                       sdesc_sw128(qaddr + kk * 2048, kBox, 1024), id_tmn, (i > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
             for (int kk = 0; kk < BT / 16; ++kk)
                 mma_ss(tS, sdesc_sw128(sbase + kDSOff + kk * 2048, kBox, 1024),
@@ -222,107 +224,97 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(smem_u32(&bars->dq_full));
             if (i + QS < nt) mma_commit(smem_u32(&bars->q_empty[s]));
         }
-    } else if (warp >= 2) {
-        // ---------------- compute warpgroup
+    } else if (warp >= 4) {
+        // ---------------- compute: two warpgroups split the 128 columns
+        const int wg = (warp - 4) >> 2;       // 0: columns 0..63, 1: columns 64..127
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;  // key row of S^T/dP^T; query row of dQ
-        const int ct = threadIdx.x - 64;      // 0..127
+        const int wt = threadIdx.x - 128 - wg * 128;
+        const int cbase = wg * 64;            // first column of this warpgroup
+        const uint32_t pbase = wg * 64;       // packed bf16 columns of P^T / dS^T
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const float cl2 = g.scale * 1.4426950408889634f;
         const bool key_valid = row < rows_b;
+        float *sL = sStat + wg * 128, *sD = sL + 64;
         int i = 0;
         bool ok = true;
-        for (int r = 0; r < N && ok; ++r) {
-            const int d = (e + r) % N;
+        for (int d = 0; d < N && ok; ++d) {
             const QuerySpan sp = query_span(g.layout, d, e, b, nq, rows_b);
             const int64_t srow0 = bh * g.lse_stride_bh + (int64_t)d * g.lse_stripe_stride;
-            for (int a = sp.a_lo; a < nq; ++a, ++i) {
-                // per-query statistics of this tile -> smem; the first barrier
-                // keeps the previous tile's readers ahead of the overwrite
-                float *sL = sStat, *sD = sStat + 128;
-                named_bar_sync(1, 128);
+            for (int a = nq - 1; a >= sp.a_lo; --a, ++i) {
+                // this warpgroup's 64 query statistics -> smem; the first
+                // barrier keeps the previous tile's readers ahead
+                named_bar_sync(1 + wg, 128);
                 {
-                    const int64_t qi = (int64_t)a * BT + ct;
+                    const int c = wt & 63;
+                    const int64_t qi = (int64_t)a * BT + cbase + c;
                     const bool qv = qi < g.L;
                     // an out-of-range query gets LSE = +inf, hence P = 0
-                    sL[ct] = qv ? p.lse[srow0 + qi] * 1.4426950408889634f : INFINITY;
-                    sD[ct] = qv ? p.delta[srow0 + qi] : 0.f;
+                    if (wt < 64) sL[c] = qv ? p.lse[srow0 + qi] * 1.4426950408889634f : INFINITY;
+                    else sD[c] = qv ? p.delta[srow0 + qi] : 0.f;
                 }
-                named_bar_sync(1, 128);
+                named_bar_sync(1 + wg, 128);
                 const bool diag = sp.has_diag && a == sp.a_lo;
-                // keep pair (query col c, key row) iff row <= c + diag_off
+                // keep pair (query col, key row) iff row <= col + diag_off
                 const int cmin = diag ? row - sp.diag_off : 0;
-                // ---- P^T
+                // ---- P^T -> TMEM (bf16 pairs)
                 if (!mbar_wait(smem_u32(&bars->s_full), i & 1, p.err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                float P[BT];
 #pragma unroll
-                for (int c = 0; c < BT / 32; ++c) {
+                for (int c = 0; c < 2; ++c) {
                     uint32_t rr[32];
-                    tmem_ld32(tS + lane_off + c * 32, rr);
-                    tmem_ld_wait(rr);
-#pragma unroll
-                    for (int u = 0; u < 32; ++u) {
-                        const int col = c * 32 + u;
-                        const float pv = ex2(fmaf(__uint_as_float(rr[u]), cl2, -sL[col]));
-                        P[col] = (key_valid && col >= cmin) ? pv : 0.f;
-                    }
-                }
-                {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int u = 0; u < 32; ++u) pk[u] = pack_bf16x2(P[2 * u], P[2 * u + 1]);
-                    tmem_st32(tS + lane_off, pk);
-#pragma unroll
-                    for (int u = 0; u < 32; ++u) pk[u] = pack_bf16x2(P[64 + 2 * u], P[64 + 2 * u + 1]);
-                    tmem_st32(tS + lane_off + 32, pk);
-                }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&bars->p_ready));
-                // ---- dS^T = P^T * (dP^T - Delta)
-                if (!mbar_wait(smem_u32(&bars->dp_full), i & 1, p.err)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                uint8_t *sDS = smem + kDSOff;
-#pragma unroll
-                for (int c = 0; c < BT / 32; ++c) {
-                    uint32_t rr[32];
-                    tmem_ld32(tdP + lane_off + c * 32, rr);
+                    tmem_ld32(tS + lane_off + cbase + c * 32, rr);
                     tmem_ld_wait(rr);
                     uint32_t pk[16];
 #pragma unroll
                     for (int u = 0; u < 16; ++u) {
                         const int c0 = c * 32 + 2 * u;
-                        const float ds0 = P[c0] * (__uint_as_float(rr[2 * u]) - sD[c0]);
-                        const float ds1 = P[c0 + 1] * (__uint_as_float(rr[2 * u + 1]) - sD[c0 + 1]);
+                        const float p0 = ex2(fmaf(__uint_as_float(rr[2 * u]), cl2, -sL[c0]));
+                        const float p1 = ex2(fmaf(__uint_as_float(rr[2 * u + 1]), cl2, -sL[c0 + 1]));
+                        const bool k0 = key_valid && (cbase + c0 >= cmin);
+                        const bool k1 = key_valid && (cbase + c0 + 1 >= cmin);
+                        pk[u] = pack_bf16x2(k0 ? p0 : 0.f, k1 ? p1 : 0.f);
+                    }
+                    tmem_st16(tS + lane_off + pbase + c * 16, pk);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars->p_ready));
+                // ---- dS^T = P^T * (dP^T - Delta): TMEM (for dK) and smem (for dQ)
+                if (!mbar_wait(smem_u32(&bars->dp_full), i & 1, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint8_t *sDS = smem + kDSOff + wg * kBox + row * 128;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t rr[32], pp[16];
+                    tmem_ld32(tdP + lane_off + cbase + c * 32, rr);
+                    tmem_ld16(tS + lane_off + pbase + c * 16, pp);
+                    tmem_ld_wait2(rr, pp);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        const int c0 = c * 32 + 2 * u;
+                        __nv_bfloat162 pv = *reinterpret_cast<__nv_bfloat162 *>(&pp[u]);
+                        const float2 pf = __bfloat1622float2(pv);
+                        const float ds0 = pf.x * (__uint_as_float(rr[2 * u]) - sD[c0]);
+                        const float ds1 = pf.y * (__uint_as_float(rr[2 * u + 1]) - sD[c0 + 1]);
                         pk[u] = pack_bf16x2(ds0, ds1);
                     }
-                    // dS^T (bf16) over the dP^T columns already read: columns
-                    // c*16 .. c*16+15 hold query columns c*32 .. c*32+31
-                    asm volatile(
-                        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-                        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-                            tdP + lane_off + c * 16),
-                        "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]), "r"(pk[6]),
-                        "r"(pk[7]), "r"(pk[8]), "r"(pk[9]), "r"(pk[10]), "r"(pk[11]), "r"(pk[12]),
-                        "r"(pk[13]), "r"(pk[14]), "r"(pk[15])
-                        : "memory");
-                    // dS into smem as the MN-major A operand of dQ = dS K:
-                    // key row `row`, query columns c*32 .. c*32+31 = 4 chunks
-                    // of 8 in box (c >> 1), chunk index ((c & 1) * 4 + v)
+                    // written over dP^T columns this thread has already read
+                    tmem_st16(tdP + lane_off + pbase + c * 16, pk);
+                    // MN-major A operand of dQ = dS K: key row `row`, query
+                    // chunks of 8 in this warpgroup's 64-column box
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
-                        const int chunk = (c & 1) * 4 + v;
-                        const uint32_t off = (uint32_t)(c >> 1) * kBox + (uint32_t)row * 128u +
-                                             (uint32_t)((chunk ^ (row & 7)) * 16);
-                        *reinterpret_cast<uint4 *>(sDS + off) =
+                        const int chunk = c * 4 + v;
+                        *reinterpret_cast<uint4 *>(sDS + ((chunk ^ (row & 7)) * 16)) =
                             make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
                     }
                 }
@@ -337,40 +329,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                float dqv[HD];
-#pragma unroll
-                for (int c = 0; c < HD / 32; ++c) {
-                    uint32_t rr[32];
-                    tmem_ld32(tS + lane_off + c * 32, rr);
-                    tmem_ld_wait(rr);
-#pragma unroll
-                    for (int u = 0; u < 32; ++u) dqv[c * 32 + u] = __uint_as_float(rr[u]);
-                }
+                uint32_t q0[32], q1[32];
+                tmem_ld32(tS + lane_off + cbase, q0);
+                tmem_ld32(tS + lane_off + cbase + 32, q1);
+                tmem_ld_wait(q0);
+                tmem_ld_wait(q1);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
                 const int64_t qi = (int64_t)a * BT + row;
                 if (qi < g.L) {
-                    float *dst = p.dq_acc + (bh * g.stride_bh + (int64_t)d * g.stripe_stride + qi * HD);
+                    float *dst = p.dq_acc + (bh * g.stride_bh + (int64_t)d * g.stripe_stride + qi * HD + cbase);
 #pragma unroll
-                    for (int v = 0; v < HD / 4; ++v)
-                        red_add_v4(dst + 4 * v, dqv[4 * v], dqv[4 * v + 1], dqv[4 * v + 2], dqv[4 * v + 3]);
+                    for (int v = 0; v < 8; ++v)
+                        red_add_v4(dst + 4 * v, __uint_as_float(q0[4 * v]), __uint_as_float(q0[4 * v + 1]),
+                                   __uint_as_float(q0[4 * v + 2]), __uint_as_float(q0[4 * v + 3]));
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        red_add_v4(dst + 32 + 4 * v, __uint_as_float(q1[4 * v]), __uint_as_float(q1[4 * v + 1]),
+                                   __uint_as_float(q1[4 * v + 2]), __uint_as_float(q1[4 * v + 3]));
                 }
             }
         }
-        // ---------------- epilogue: dK, dV of this key tile
+        // ---------------- epilogue: this warpgroup's columns of dK, dV
         const int64_t kj = (int64_t)b * BT + row;
-        const int64_t krow = bh * g.stride_bh + (int64_t)e * g.stripe_stride + kj * HD;
+        const int64_t krow = bh * g.stride_bh + (int64_t)e * g.stripe_stride + kj * HD + cbase;
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
             const uint32_t tacc = which ? tdK : tdV;
             __nv_bfloat16 *outp = which ? p.dk : p.dv;
             const float mul = which ? g.scale : 1.f;
 #pragma unroll
-            for (int c = 0; c < HD / 32; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint32_t rr[32];
                 if (nt > 0 && ok) {
-                    tmem_ld32(tacc + lane_off + c * 32, rr);
+                    tmem_ld32(tacc + lane_off + cbase + c * 32, rr);
                     tmem_ld_wait(rr);
                 } else {
 #pragma unroll

@@ -88,17 +88,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         d = p.d_fixed;
         bh = blockIdx.y;
     } else {
-        // heaviest query tiles first (largest a; for contiguous also largest d)
+        // Head-major order: the CTAs resident at one time belong to one head
+        // and share its K/V tiles in L2.  Within a head the heaviest query
+        // tiles go first (largest a; for contiguous also largest d).
         const int64_t id = blockIdx.x;
-        a = nq - 1 - (int)(id / ((int64_t)g.N * g.BH));
-        const int dd = (int)((id / g.BH) % g.N);
+        const int64_t per_head = (int64_t)nq * g.N;
+        bh = id / per_head;
+        const int rem = (int)(id % per_head);
+        a = nq - 1 - rem / g.N;
+        const int dd = rem % g.N;
         d = (g.layout == STRIPED_LAYOUT_CONTIGUOUS) ? g.N - 1 - dd : dd;
-        bh = id % g.BH;
     }
     const int rows_a = tile_rows(g.L, a);
     const int nrounds = kRound ? 1 : g.N;
-    const int e_fixed = p.e_fixed, Nst = g.N;
-    auto stripe_of = [=](int r) { return kRound ? e_fixed : (d - r + Nst) % Nst; };
+    const int e_fixed = p.e_fixed;
+    // Key stripes are visited in the same global order e = 0..N-1 by every
+    // query tile (so resident CTAs read the same key tiles at the same
+    // time); tile counts are still attributed to ring round (d - e) mod N.
+    // The first tile (e = 0, b = 0) always holds a kept key for every row.
+    auto stripe_of = [=](int r) { return kRound ? e_fixed : r; };
 
     // number of key tiles this query tile visits
     int nt = 0;
