@@ -17,15 +17,20 @@
 //              ring), warp 1 = TMEM allocator + MMA issuer, warps 4..11 =
 //              two compute warpgroups; thread t of a warpgroup owns key row
 //              t of S^T/dP^T (query row t of dQ), warpgroup 0 columns
-//              0..63 and warpgroup 1 columns 64..127.  TMEM: S^T [0,128)
-//              (P^T bf16 pairs over it, then dQ_i), dP^T [128,256) (dS^T
-//              bf16 pairs over it), dV [256,384), dK [384,512).
+//              0..63 and warpgroup 1 columns 64..127.
+//              TMEM: S^T [0,128) (P^T bf16 pairs over it), dP^T [128,256)
+//              (dQ_i over it once dS_i is formed), dV [256,384), dK [384,512).
 //                S^T  = K Q_i^T      SS, both K-major
 //                dP^T = V dO_i^T     SS, both K-major
 //                dV  += P^T dO_i     TS, A = P^T in TMEM, B = dO_i MN-major
-//                dK  += dS^T Q_i     TS, A = dS^T in TMEM, B = Q_i MN-major
-//                dQ_i = dS K         SS, A = dS in smem MN-major, B = K MN-major
-//              dQ_i is added to the fp32 accumulator with vector reductions.
+//                dQ_i = dS K         SS, A = dS smem tile read MN-major
+//                dK  += dS^T Q_i     SS, A = the same smem tile read K-major
+//              The dS tile ([key][query], 128-byte swizzle) is a valid
+//              operand both ways, so dS^T never goes through TMEM.  Issue
+//              order dV_i, S_{i+1}, dQ_i, dK_i, dP_{i+1} keeps the tensor core
+//              busy while the compute warps form dS_i, P_{i+1} and read dQ_i
+//              out; dQ_i is added to the fp32 accumulator with vector
+//              reductions.
 //   bwd_post   dQ = bf16(scale * accumulator)
 #include <math.h>
 
@@ -64,13 +69,42 @@ struct Bars {
     uint64_t kv_full;
     uint64_t q_full[QS];
     uint64_t q_empty[QS];
-    uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, dq_free;
+    uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, dq_free, acc_done;
     uint32_t tmem_slot;
 };
 
 __device__ __forceinline__ int tile_rows(int64_t L, int t) {
     const int64_t r = L - (int64_t)t * BT;
     return r >= BT ? BT : (int)r;
+}
+
+// Order in which a key tile visits its query tiles: stripes d = 0..N-1,
+// and within a stripe a = nq-1 down to the first tile that sees the key
+// tile (the diagonal, if any, last).
+struct QTileIter {
+    int d, a, a_lo, has_diag, diag_off;
+};
+
+__device__ __forceinline__ void qiter_seek(QTileIter &it, int layout, int N, int e, int b, int nq, int rows_b) {
+    while (it.d < N) {
+        const QuerySpan sp = query_span(layout, it.d, e, b, nq, rows_b);
+        if (sp.a_lo < nq) {
+            it.a_lo = sp.a_lo;
+            it.has_diag = sp.has_diag;
+            it.diag_off = sp.diag_off;
+            return;
+        }
+        ++it.d;
+        it.a = nq - 1;
+    }
+}
+
+__device__ __forceinline__ void qiter_next(QTileIter &it, int layout, int N, int e, int b, int nq, int rows_b) {
+    if (--it.a < it.a_lo) {
+        ++it.d;
+        it.a = nq - 1;
+        qiter_seek(it, layout, N, e, b, nq, rows_b);
+    }
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
@@ -118,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&bars->ds_ready), 8);
         mbar_init(smem_u32(&bars->dq_full), 1);
         mbar_init(smem_u32(&bars->dq_free), 8);
+        mbar_init(smem_u32(&bars->acc_done), 1);
         fence_barrier_init();
         if (p.tile_stats) {
             for (int d = 0; d < N; ++d) {
@@ -176,18 +211,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1 && lane == 0 && nt > 0) {
         // ---------------- MMA issuer
+        // Per query tile i (TMEM: S = S^T then P^T; DP = dP^T then dQ_i):
+        //   dV += P^T dO | S(i+1) | dQ_i = dS K | dK += dS^T Q | dP(i+1)
+        // so S(i+1) runs while the compute warps form dS_i, dK_i runs while
+        // they read dQ_i out, and dP(i+1) follows as soon as dQ_i is out.
         constexpr uint32_t id_kk = idesc_bf16_f32(BT, BT, false, false);
-        constexpr uint32_t id_tmn = idesc_bf16_f32(BT, HD, false, true);
+        constexpr uint32_t id_kmn = idesc_bf16_f32(BT, HD, false, true);
         constexpr uint32_t id_mnmn = idesc_bf16_f32(BT, HD, true, true);
-        bool ok = mbar_wait(smem_u32(&bars->kv_full), 0, p.err);
-        for (int i = 0; i < nt && ok; ++i) {
-            const int s = i % QS;
-            if (!mbar_wait(smem_u32(&bars->q_full[s]), (i / QS) & 1, p.err)) break;
-            if (i > 0 && !mbar_wait(smem_u32(&bars->dq_free), (i - 1) & 1, p.err)) break;
+        auto issue_s = [&](int t) -> bool {
+            const int s = t % QS;
+            if (!mbar_wait(smem_u32(&bars->q_full[s]), (t / QS) & 1, p.err)) return false;
             tc_fence_after();
             const uint32_t qaddr = sbase + kQOff + s * 2 * kTile;
-            const uint32_t oaddr = qaddr + kTile;
-            // S^T = K Q^T ; dP^T = V dO^T
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk) {
                 const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
@@ -195,6 +230,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                        id_kk, kk > 0 ? 1u : 0u);
             }
             mma_commit(smem_u32(&bars->s_full));
+            return true;
+        };
+        auto issue_dp = [&](int t) {
+            const uint32_t oaddr = sbase + kQOff + (t % QS) * 2 * kTile + kTile;
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk) {
                 const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
@@ -202,28 +241,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                        id_kk, kk > 0 ? 1u : 0u);
             }
             mma_commit(smem_u32(&bars->dp_full));
-            // dV += P^T dO: P^T (bf16 pairs) sits in TMEM columns [0,32) for
+        };
+        bool ok = mbar_wait(smem_u32(&bars->kv_full), 0, p.err) && issue_s(0);
+        if (ok) issue_dp(0);
+        for (int i = 0; i < nt && ok; ++i) {
+            const int s = i % QS;
+            const uint32_t qaddr = sbase + kQOff + s * 2 * kTile;
+            const uint32_t oaddr = qaddr + kTile;
+            // dV += P^T dO: P^T (bf16 pairs) in TMEM columns [0,32) for
             // queries 0..63 and [64,96) for queries 64..127
             if (!mbar_wait(smem_u32(&bars->p_ready), i & 1, p.err)) break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < BT / 16; ++kk)
                 mma_ts(tdV, tS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
-                       sdesc_sw128(oaddr + kk * 2048, kBox, 1024), id_tmn, (i > 0 || kk > 0) ? 1u : 0u);
-            // dK += dS^T Q ; dQ = dS K
+                       sdesc_sw128(oaddr + kk * 2048, kBox, 1024), id_kmn, (i > 0 || kk > 0) ? 1u : 0u);
+            if (i + 1 < nt && !issue_s(i + 1)) break;
+            // dQ_i = dS K (A = dS, MN-major view of the smem tile) -> DP columns
             if (!mbar_wait(smem_u32(&bars->ds_ready), i & 1, p.err)) break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < BT / 16; ++kk)
-                mma_ts(tdK, tdP + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
-                       sdesc_sw128(qaddr + kk * 2048, kBox, 1024), id_tmn, (i > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-            for (int kk = 0; kk < BT / 16; ++kk)
-                mma_ss(tS, sdesc_sw128(sbase + kDSOff + kk * 2048, kBox, 1024),
+                mma_ss(tdP, sdesc_sw128(sbase + kDSOff + kk * 2048, kBox, 1024),
                        sdesc_sw128(sbase + kKOff + kk * 2048, kBox, 1024), id_mnmn, kk > 0 ? 1u : 0u);
             mma_commit(smem_u32(&bars->dq_full));
+            // dK += dS^T Q (A = dS^T, K-major view of the same smem tile)
+#pragma unroll
+            for (int kk = 0; kk < BT / 16; ++kk)
+                mma_ss(tdK, sdesc_sw128(sbase + kDSOff + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024),
+                       sdesc_sw128(qaddr + kk * 2048, kBox, 1024), id_kmn, (i > 0 || kk > 0) ? 1u : 0u);
             if (i + QS < nt) mma_commit(smem_u32(&bars->q_empty[s]));
+            if (i + 1 < nt) {
+                if (!mbar_wait(smem_u32(&bars->dq_free), i & 1, p.err)) break;
+                tc_fence_after();
+                issue_dp(i + 1);
+            }
         }
+        if (ok) mma_commit(smem_u32(&bars->acc_done));
     } else if (warp >= 4) {
         // ---------------- compute: two warpgroups split the 128 columns
         const int wg = (warp - 4) >> 2;       // 0: columns 0..63, 1: columns 64..127
@@ -231,125 +285,140 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = quarter * 32 + lane;  // key row of S^T/dP^T; query row of dQ
         const int wt = threadIdx.x - 128 - wg * 128;
         const int cbase = wg * 64;            // first column of this warpgroup
-        const uint32_t pbase = wg * 64;       // packed bf16 columns of P^T / dS^T
+        const uint32_t pbase = wg * 64;       // TMEM columns of this warpgroup's P^T pairs
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const float cl2 = g.scale * 1.4426950408889634f;
         const bool key_valid = row < rows_b;
         float *sL = sStat + wg * 128, *sD = sL + 64;
-        int i = 0;
-        bool ok = true;
-        for (int d = 0; d < N && ok; ++d) {
-            const QuerySpan sp = query_span(g.layout, d, e, b, nq, rows_b);
-            const int64_t srow0 = bh * g.lse_stride_bh + (int64_t)d * g.lse_stripe_stride;
-            for (int a = nq - 1; a >= sp.a_lo; --a, ++i) {
-                // this warpgroup's 64 query statistics -> smem; the first
-                // barrier keeps the previous tile's readers ahead
-                named_bar_sync(1 + wg, 128);
-                {
-                    const int c = wt & 63;
-                    const int64_t qi = (int64_t)a * BT + cbase + c;
-                    const bool qv = qi < g.L;
-                    // an out-of-range query gets LSE = +inf, hence P = 0
-                    if (wt < 64) sL[c] = qv ? p.lse[srow0 + qi] * 1.4426950408889634f : INFINITY;
-                    else sD[c] = qv ? p.delta[srow0 + qi] : 0.f;
-                }
-                named_bar_sync(1 + wg, 128);
-                const bool diag = sp.has_diag && a == sp.a_lo;
-                // keep pair (query col, key row) iff row <= col + diag_off
-                const int cmin = diag ? row - sp.diag_off : 0;
-                // ---- P^T -> TMEM (bf16 pairs)
-                if (!mbar_wait(smem_u32(&bars->s_full), i & 1, p.err)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
+        uint8_t *sDS = smem + kDSOff + wg * kBox + row * 128;
+        bool ok = nt > 0;
+
+        // per-query statistics of a tile -> smem (callers fence with barriers)
+        auto load_stats = [&](const QTileIter &t) {
+            const int c = wt & 63;
+            const int64_t qi = (int64_t)t.a * BT + cbase + c;
+            const int64_t srow = bh * g.lse_stride_bh + (int64_t)t.d * g.lse_stripe_stride + qi;
+            const bool qv = qi < g.L;
+            // an out-of-range query gets LSE = +inf, hence P = 0
+            if (wt < 64) sL[c] = qv ? p.lse[srow] * 1.4426950408889634f : INFINITY;
+            else sD[c] = qv ? p.delta[srow] : 0.f;
+        };
+        // P^T of tile t (index i): kept in registers (bf16 pairs) for dS and
+        // written to TMEM as the A operand of dV += P^T dO
+        uint32_t pkP[32];
+        auto compute_p = [&](const QTileIter &t, int i) -> bool {
+            if (!mbar_wait(smem_u32(&bars->s_full), i & 1, p.err)) return false;
+            tc_fence_after();
+            const bool diag = t.has_diag && t.a == t.a_lo;
+            // keep pair (query col, key row) iff row <= col + diag_off
+            const int cmin = diag ? row - t.diag_off : 0;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t rr[32];
-                    tmem_ld32(tS + lane_off + cbase + c * 32, rr);
-                    tmem_ld_wait(rr);
-                    uint32_t pk[16];
+            for (int c = 0; c < 2; ++c) {
+                uint32_t rr[32];
+                tmem_ld32(tS + lane_off + cbase + c * 32, rr);
+                tmem_ld_wait(rr);
+                uint32_t pk[16];
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) {
+                for (int u = 0; u < 16; ++u) {
+                    const int c0 = c * 32 + 2 * u;
+                    const float p0 = ex2(fmaf(__uint_as_float(rr[2 * u]), cl2, -sL[c0]));
+                    const float p1 = ex2(fmaf(__uint_as_float(rr[2 * u + 1]), cl2, -sL[c0 + 1]));
+                    const bool k0 = key_valid && (cbase + c0 >= cmin);
+                    const bool k1 = key_valid && (cbase + c0 + 1 >= cmin);
+                    pk[u] = pack_bf16x2(k0 ? p0 : 0.f, k1 ? p1 : 0.f);
+                    pkP[c * 16 + u] = pk[u];
+                }
+                tmem_st16(tS + lane_off + pbase + c * 16, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->p_ready));
+            return true;
+        };
+
+        QTileIter cur{0, nq - 1, 0, 0, 0};
+        qiter_seek(cur, g.layout, N, e, b, nq, rows_b);
+        if (ok) {
+            load_stats(cur);
+            named_bar_sync(1 + wg, 128);
+            ok = compute_p(cur, 0);
+        }
+        for (int i = 0; i < nt && ok; ++i) {
+            // ---- dS = P * (dP - Delta) -> smem (A operand of dQ and dK)
+            if (!mbar_wait(smem_u32(&bars->dp_full), i & 1, p.err)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t rr[32];
+                tmem_ld32(tdP + lane_off + cbase + c * 32, rr);
+                tmem_ld_wait(rr);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const int u = v * 4 + h;  // pair index within the chunk
                         const int c0 = c * 32 + 2 * u;
-                        const float p0 = ex2(fmaf(__uint_as_float(rr[2 * u]), cl2, -sL[c0]));
-                        const float p1 = ex2(fmaf(__uint_as_float(rr[2 * u + 1]), cl2, -sL[c0 + 1]));
-                        const bool k0 = key_valid && (cbase + c0 >= cmin);
-                        const bool k1 = key_valid && (cbase + c0 + 1 >= cmin);
-                        pk[u] = pack_bf16x2(k0 ? p0 : 0.f, k1 ? p1 : 0.f);
-                    }
-                    tmem_st16(tS + lane_off + pbase + c * 16, pk);
-                }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&bars->p_ready));
-                // ---- dS^T = P^T * (dP^T - Delta): TMEM (for dK) and smem (for dQ)
-                if (!mbar_wait(smem_u32(&bars->dp_full), i & 1, p.err)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                uint8_t *sDS = smem + kDSOff + wg * kBox + row * 128;
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t rr[32], pp[16];
-                    tmem_ld32(tdP + lane_off + cbase + c * 32, rr);
-                    tmem_ld16(tS + lane_off + pbase + c * 16, pp);
-                    tmem_ld_wait2(rr, pp);
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        const int c0 = c * 32 + 2 * u;
-                        __nv_bfloat162 pv = *reinterpret_cast<__nv_bfloat162 *>(&pp[u]);
+                        __nv_bfloat162 pv = *reinterpret_cast<__nv_bfloat162 *>(&pkP[c * 16 + u]);
                         const float2 pf = __bfloat1622float2(pv);
-                        const float ds0 = pf.x * (__uint_as_float(rr[2 * u]) - sD[c0]);
-                        const float ds1 = pf.y * (__uint_as_float(rr[2 * u + 1]) - sD[c0 + 1]);
-                        pk[u] = pack_bf16x2(ds0, ds1);
+                        w[h] = pack_bf16x2(pf.x * (__uint_as_float(rr[2 * u]) - sD[c0]),
+                                           pf.y * (__uint_as_float(rr[2 * u + 1]) - sD[c0 + 1]));
                     }
-                    // written over dP^T columns this thread has already read
-                    tmem_st16(tdP + lane_off + pbase + c * 16, pk);
-                    // MN-major A operand of dQ = dS K: key row `row`, query
-                    // chunks of 8 in this warpgroup's 64-column box
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const int chunk = c * 4 + v;
-                        *reinterpret_cast<uint4 *>(sDS + ((chunk ^ (row & 7)) * 16)) =
-                            make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-                    }
-                }
-                tmem_st_wait();
-                fence_proxy_async_smem();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready));
-                // ---- dQ_i readout -> fp32 accumulator
-                if (!mbar_wait(smem_u32(&bars->dq_full), i & 1, p.err)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                uint32_t q0[32], q1[32];
-                tmem_ld32(tS + lane_off + cbase, q0);
-                tmem_ld32(tS + lane_off + cbase + 32, q1);
-                tmem_ld_wait(q0);
-                tmem_ld_wait(q1);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
-                const int64_t qi = (int64_t)a * BT + row;
-                if (qi < g.L) {
-                    float *dst = p.dq_acc + (bh * g.stride_bh + (int64_t)d * g.stripe_stride + qi * HD + cbase);
-#pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        red_add_v4(dst + 4 * v, __uint_as_float(q0[4 * v]), __uint_as_float(q0[4 * v + 1]),
-                                   __uint_as_float(q0[4 * v + 2]), __uint_as_float(q0[4 * v + 3]));
-#pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        red_add_v4(dst + 32 + 4 * v, __uint_as_float(q1[4 * v]), __uint_as_float(q1[4 * v + 1]),
-                                   __uint_as_float(q1[4 * v + 2]), __uint_as_float(q1[4 * v + 3]));
+                    const int chunk = c * 4 + v;
+                    *reinterpret_cast<uint4 *>(sDS + ((chunk ^ (row & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready));
+            // ---- P of the next tile while the tensor core runs dQ_i / dK_i
+            const QTileIter done = cur;
+            if (i + 1 < nt) {
+                qiter_next(cur, g.layout, N, e, b, nq, rows_b);
+                named_bar_sync(1 + wg, 128);  // everyone is past dS_i (last use of sL/sD)
+                load_stats(cur);
+                named_bar_sync(1 + wg, 128);
+                if (!compute_p(cur, i + 1)) {
+                    ok = false;
+                    break;
+                }
+            }
+            // ---- dQ_i readout -> fp32 accumulator
+            if (!mbar_wait(smem_u32(&bars->dq_full), i & 1, p.err)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t q0[32], q1[32];
+            tmem_ld32(tdP + lane_off + cbase, q0);
+            tmem_ld32(tdP + lane_off + cbase + 32, q1);
+            tmem_ld_wait(q0);
+            tmem_ld_wait(q1);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
+            const int64_t qi = (int64_t)done.a * BT + row;
+            if (qi < g.L) {
+                float *dst =
+                    p.dq_acc + (bh * g.stride_bh + (int64_t)done.d * g.stripe_stride + qi * HD + cbase);
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    red_add_v4(dst + 4 * v, __uint_as_float(q0[4 * v]), __uint_as_float(q0[4 * v + 1]),
+                               __uint_as_float(q0[4 * v + 2]), __uint_as_float(q0[4 * v + 3]));
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    red_add_v4(dst + 32 + 4 * v, __uint_as_float(q1[4 * v]), __uint_as_float(q1[4 * v + 1]),
+                               __uint_as_float(q1[4 * v + 2]), __uint_as_float(q1[4 * v + 3]));
+            }
+        }
+        if (ok) {
+            ok = mbar_wait(smem_u32(&bars->acc_done), 0, p.err);
+            tc_fence_after();
         }
         // ---------------- epilogue: this warpgroup's columns of dK, dV
         const int64_t kj = (int64_t)b * BT + row;
@@ -362,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 uint32_t rr[32];
-                if (nt > 0 && ok) {
+                if (ok) {
                     tmem_ld32(tacc + lane_off + cbase + c * 32, rr);
                     tmem_ld_wait(rr);
                 } else {
