@@ -27,10 +27,10 @@
 //                dK  += dS^T Q_i     SS, A = the same smem tile read K-major
 //              The dS tile ([key][query], 128-byte swizzle) is a valid
 //              operand both ways, so dS^T never goes through TMEM.  Issue
-//              order dV_i, S_{i+1}, dQ_i, dK_i, dP_{i+1} keeps the tensor core
-//              busy while the compute warps form dS_i, P_{i+1} and read dQ_i
-//              out; dQ_i is added to the fp32 accumulator with vector
-//              reductions.
+//              order dV_i, S_{i+1}, dQ_i, dK_i, dP_{i+1}; the compute warps
+//              form dS_i, then P_{i+1} while dQ_i and dK_i run, then read
+//              dQ_i out (freeing the columns for dP_{i+1}) and add it to the
+//              fp32 accumulator with vector reductions.
 //   bwd_post   dQ = bf16(scale * accumulator)
 #include <math.h>
 
@@ -293,15 +293,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t *sDS = smem + kDSOff + wg * kBox + row * 128;
         bool ok = nt > 0;
 
-        // per-query statistics of a tile -> smem (callers fence with barriers)
-        auto load_stats = [&](const QTileIter &t) {
+        // This thread's share of a tile's per-query statistics (threads 0..63
+        // of the warpgroup fetch LSE in log2 units, 64..127 fetch Delta); an
+        // out-of-range query gets LSE = +inf, hence P = 0.
+        auto fetch_stat = [&](const QTileIter &t) -> float {
             const int c = wt & 63;
             const int64_t qi = (int64_t)t.a * BT + cbase + c;
             const int64_t srow = bh * g.lse_stride_bh + (int64_t)t.d * g.lse_stripe_stride + qi;
-            const bool qv = qi < g.L;
-            // an out-of-range query gets LSE = +inf, hence P = 0
-            if (wt < 64) sL[c] = qv ? p.lse[srow] * 1.4426950408889634f : INFINITY;
-            else sD[c] = qv ? p.delta[srow] : 0.f;
+            if (qi >= g.L) return wt < 64 ? INFINITY : 0.f;
+            return wt < 64 ? p.lse[srow] * 1.4426950408889634f : p.delta[srow];
+        };
+        auto store_stat = [&](float v) {
+            if (wt < 64) sL[wt] = v;
+            else sD[wt - 64] = v;
         };
         // P^T of tile t (index i): kept in registers (bf16 pairs) for dS and
         // written to TMEM as the A operand of dV += P^T dO
@@ -319,14 +323,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_wait(rr);
                 uint32_t pk[16];
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const int c0 = c * 32 + 2 * u;
-                    const float p0 = ex2(fmaf(__uint_as_float(rr[2 * u]), cl2, -sL[c0]));
-                    const float p1 = ex2(fmaf(__uint_as_float(rr[2 * u + 1]), cl2, -sL[c0 + 1]));
-                    const bool k0 = key_valid && (cbase + c0 >= cmin);
-                    const bool k1 = key_valid && (cbase + c0 + 1 >= cmin);
-                    pk[u] = pack_bf16x2(k0 ? p0 : 0.f, k1 ? p1 : 0.f);
-                    pkP[c * 16 + u] = pk[u];
+                for (int u4 = 0; u4 < 8; ++u4) {
+                    const float4 l4 = *reinterpret_cast<const float4 *>(sL + c * 32 + 4 * u4);
+                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int u = 2 * u4 + h;
+                        const int c0 = c * 32 + 2 * u;
+                        const float p0 = ex2(fmaf(__uint_as_float(rr[2 * u]), cl2, -lv[2 * h]));
+                        const float p1 = ex2(fmaf(__uint_as_float(rr[2 * u + 1]), cl2, -lv[2 * h + 1]));
+                        const bool k0 = key_valid && (cbase + c0 >= cmin);
+                        const bool k1 = key_valid && (cbase + c0 + 1 >= cmin);
+                        pk[u] = pack_bf16x2(k0 ? p0 : 0.f, k1 ? p1 : 0.f);
+                        pkP[c * 16 + u] = pk[u];
+                    }
                 }
                 tmem_st16(tS + lane_off + pbase + c * 16, pk);
             }
@@ -339,12 +349,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         QTileIter cur{0, nq - 1, 0, 0, 0};
         qiter_seek(cur, g.layout, N, e, b, nq, rows_b);
+        QTileIter nxt = cur;
+        if (nt > 1) qiter_next(nxt, g.layout, N, e, b, nq, rows_b);
         if (ok) {
-            load_stats(cur);
+            store_stat(fetch_stat(cur));
             named_bar_sync(1 + wg, 128);
             ok = compute_p(cur, 0);
         }
         for (int i = 0; i < nt && ok; ++i) {
+            // statistics of the next tile: issue the global loads now, use
+            // them after dS_i and the dQ_i readout
+            const float pre = (i + 1 < nt) ? fetch_stat(nxt) : 0.f;
             // ---- dS = P * (dP - Delta) -> smem (A operand of dQ and dK)
             if (!mbar_wait(smem_u32(&bars->dp_full), i & 1, p.err)) {
                 ok = false;
@@ -358,15 +373,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_wait(rr);
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
+                    const float4 d0 = *reinterpret_cast<const float4 *>(sD + c * 32 + 8 * v);
+                    const float4 d1 = *reinterpret_cast<const float4 *>(sD + c * 32 + 8 * v + 4);
+                    const float dv8[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
                     uint32_t w[4];
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
                         const int u = v * 4 + h;  // pair index within the chunk
-                        const int c0 = c * 32 + 2 * u;
                         __nv_bfloat162 pv = *reinterpret_cast<__nv_bfloat162 *>(&pkP[c * 16 + u]);
                         const float2 pf = __bfloat1622float2(pv);
-                        w[h] = pack_bf16x2(pf.x * (__uint_as_float(rr[2 * u]) - sD[c0]),
-                                           pf.y * (__uint_as_float(rr[2 * u + 1]) - sD[c0 + 1]));
+                        w[h] = pack_bf16x2(pf.x * (__uint_as_float(rr[2 * u]) - dv8[2 * h]),
+                                           pf.y * (__uint_as_float(rr[2 * u + 1]) - dv8[2 * h + 1]));
                     }
                     const int chunk = c * 4 + v;
                     *reinterpret_cast<uint4 *>(sDS + ((chunk ^ (row & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -376,19 +393,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready));
-            // ---- P of the next tile while the tensor core runs dQ_i / dK_i
-            const QTileIter done = cur;
+            // ---- P of the next tile while the tensor core runs dQ_i and dK_i
             if (i + 1 < nt) {
-                qiter_next(cur, g.layout, N, e, b, nq, rows_b);
                 named_bar_sync(1 + wg, 128);  // everyone is past dS_i (last use of sL/sD)
-                load_stats(cur);
+                store_stat(pre);
                 named_bar_sync(1 + wg, 128);
-                if (!compute_p(cur, i + 1)) {
+                if (!compute_p(nxt, i + 1)) {
                     ok = false;
                     break;
                 }
             }
-            // ---- dQ_i readout -> fp32 accumulator
+            // ---- dQ_i out of TMEM (frees the columns for dP_{i+1})
             if (!mbar_wait(smem_u32(&bars->dq_full), i & 1, p.err)) {
                 ok = false;
                 break;
@@ -402,10 +417,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
-            const int64_t qi = (int64_t)done.a * BT + row;
+            // ---- dQ_i -> fp32 accumulator
+            const int64_t qi = (int64_t)cur.a * BT + row;
             if (qi < g.L) {
                 float *dst =
-                    p.dq_acc + (bh * g.stride_bh + (int64_t)done.d * g.stripe_stride + qi * HD + cbase);
+                    p.dq_acc + (bh * g.stride_bh + (int64_t)cur.d * g.stripe_stride + qi * HD + cbase);
 #pragma unroll
                 for (int v = 0; v < 8; ++v)
                     red_add_v4(dst + 4 * v, __uint_as_float(q0[4 * v]), __uint_as_float(q0[4 * v + 1]),
@@ -415,6 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     red_add_v4(dst + 32 + 4 * v, __uint_as_float(q1[4 * v]), __uint_as_float(q1[4 * v + 1]),
                                __uint_as_float(q1[4 * v + 2]), __uint_as_float(q1[4 * v + 3]));
             }
+            cur = nxt;
+            if (i + 2 < nt) qiter_next(nxt, g.layout, N, e, b, nq, rows_b);
         }
         if (ok) {
             ok = mbar_wait(smem_u32(&bars->acc_done), 0, p.err);
