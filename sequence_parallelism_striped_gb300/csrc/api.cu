@@ -37,8 +37,11 @@ typedef CUresult (*EncodeTiledFnT)(CUtensorMap *, CUtensorMapDataType, cuuint32_
                                    const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-int make_bf16_map(CUtensorMap *map, const void *base, int64_t D, int64_t L, int64_t N, int64_t BH,
-                  int64_t stripe_stride, int64_t stride_bh, int box_rows) {
+// [BH][N][L][D] tensor of `esize`-byte elements -> 4-D tiled tensor map,
+// boxes of box_x elements x box_rows rows, 128-byte swizzle, zero fill.
+static int make_map(CUtensorMap *map, CUtensorMapDataType dt, int64_t esize, const void *base, int64_t D,
+                    int64_t L, int64_t N, int64_t BH, int64_t stripe_stride, int64_t stride_bh, int box_x,
+                    int box_rows) {
     static EncodeTiledFnT fn = nullptr;
     static int resolved = 0;
     if (!resolved) {
@@ -52,18 +55,30 @@ int make_bf16_map(CUtensorMap *map, const void *base, int64_t D, int64_t L, int6
         resolved = 1;
     }
     cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)N, (cuuint64_t)BH};
-    cuuint64_t strides[3] = {(cuuint64_t)(D * 2), (cuuint64_t)(stripe_stride * 2),
-                             (cuuint64_t)(stride_bh * 2)};
-    cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
+    cuuint64_t strides[3] = {(cuuint64_t)(D * esize), (cuuint64_t)(stripe_stride * esize),
+                             (cuuint64_t)(stride_bh * esize)};
+    cuuint32_t box[4] = {(cuuint32_t)box_x, (cuuint32_t)box_rows, 1, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box,
-                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    CUresult r = fn(map, dt, 4, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         t_last_cuda_error = (int)r;
         return STRIPED_ERR_CUDA;
     }
     return STRIPED_OK;
+}
+
+int make_bf16_map(CUtensorMap *map, const void *base, int64_t D, int64_t L, int64_t N, int64_t BH,
+                  int64_t stripe_stride, int64_t stride_bh, int box_rows) {
+    return make_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, D, L, N, BH, stripe_stride, stride_bh, 64,
+                    box_rows);
+}
+
+int make_f32_map(CUtensorMap *map, const void *base, int64_t D, int64_t L, int64_t N, int64_t BH,
+                 int64_t stripe_stride, int64_t stride_bh, int box_rows) {
+    return make_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, D, L, N, BH, stripe_stride, stride_bh, 32,
+                    box_rows);
 }
 
 // ---------------------------------------------------------------- validation

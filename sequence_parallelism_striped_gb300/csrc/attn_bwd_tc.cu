@@ -27,10 +27,13 @@
 //                dK  += dS^T Q_i     SS, A = the same smem tile read K-major
 //              The dS tile ([key][query], 128-byte swizzle) is a valid
 //              operand both ways, so dS^T never goes through TMEM.  Issue
-//              order dV_i, S_{i+1}, dQ_i, dK_i, dP_{i+1}; the compute warps
-//              form dS_i, then P_{i+1} while dQ_i and dK_i run, then read
-//              dQ_i out (freeing the columns for dP_{i+1}) and add it to the
-//              fp32 accumulator with vector reductions.
+//              order dV_i, S_{i+1}, dQ_i, dK_i, dP_{i+1} keeps the tensor core
+//              busy while the compute warps form dS_i, P_{i+1} and read dQ_i
+//              out.  dQ_i is added to the fp32 accumulator by TMA bulk
+//              reduce-add from shared memory, staged in the tile buffers that
+//              are dead by then (dO_i after dV_i, Q_i after dK_i), so the
+//              reduction travels as whole swizzled boxes, not as per-thread
+//              16-byte atomics.
 //   bwd_post   dQ = bf16(scale * accumulator)
 #include <math.h>
 
@@ -69,7 +72,7 @@ struct Bars {
     uint64_t kv_full;
     uint64_t q_full[QS];
     uint64_t q_empty[QS];
-    uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, dq_free, acc_done;
+    uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, dq_free, dk_done, acc_done;
     uint32_t tmem_slot;
 };
 
@@ -114,7 +117,7 @@ __device__ __forceinline__ void named_bar_sync(int id, int n) {
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                  const BwdParams p) {
+                  const __grid_constant__ CUtensorMap tmdQ, const BwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
@@ -144,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&bars->kv_full), 1);
         for (int s = 0; s < QS; ++s) {
             mbar_init(smem_u32(&bars->q_full[s]), 1);
-            mbar_init(smem_u32(&bars->q_empty[s]), 1);
+            mbar_init(smem_u32(&bars->q_empty[s]), 2);  // one arrival per compute warpgroup
         }
         mbar_init(smem_u32(&bars->s_full), 1);
         mbar_init(smem_u32(&bars->dp_full), 1);
@@ -152,6 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&bars->ds_ready), 8);
         mbar_init(smem_u32(&bars->dq_full), 1);
         mbar_init(smem_u32(&bars->dq_free), 8);
+        mbar_init(smem_u32(&bars->dk_done), 1);
         mbar_init(smem_u32(&bars->acc_done), 1);
         fence_barrier_init();
         if (p.tile_stats) {
@@ -270,7 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < BT / 16; ++kk)
                 mma_ss(tdK, sdesc_sw128(sbase + kDSOff + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024),
                        sdesc_sw128(qaddr + kk * 2048, kBox, 1024), id_kmn, (i > 0 || kk > 0) ? 1u : 0u);
-            if (i + QS < nt) mma_commit(smem_u32(&bars->q_empty[s]));
+            // the Q_i buffer is free once dK_i completes (it becomes dQ_i staging)
+            mma_commit(smem_u32(&bars->dk_done));
             if (i + 1 < nt) {
                 if (!mbar_wait(smem_u32(&bars->dq_free), i & 1, p.err)) break;
                 tc_fence_after();
@@ -293,19 +298,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t *sDS = smem + kDSOff + wg * kBox + row * 128;
         bool ok = nt > 0;
 
-        // This thread's share of a tile's per-query statistics (threads 0..63
-        // of the warpgroup fetch LSE in log2 units, 64..127 fetch Delta); an
-        // out-of-range query gets LSE = +inf, hence P = 0.
-        auto fetch_stat = [&](const QTileIter &t) -> float {
+        // per-query statistics of a tile -> smem (callers fence with barriers)
+        auto load_stats = [&](const QTileIter &t) {
             const int c = wt & 63;
             const int64_t qi = (int64_t)t.a * BT + cbase + c;
             const int64_t srow = bh * g.lse_stride_bh + (int64_t)t.d * g.lse_stripe_stride + qi;
-            if (qi >= g.L) return wt < 64 ? INFINITY : 0.f;
-            return wt < 64 ? p.lse[srow] * 1.4426950408889634f : p.delta[srow];
-        };
-        auto store_stat = [&](float v) {
-            if (wt < 64) sL[wt] = v;
-            else sD[wt - 64] = v;
+            const bool qv = qi < g.L;
+            // an out-of-range query gets LSE = +inf, hence P = 0
+            if (wt < 64) sL[c] = qv ? p.lse[srow] * 1.4426950408889634f : INFINITY;
+            else sD[c] = qv ? p.delta[srow] : 0.f;
         };
         // P^T of tile t (index i): kept in registers (bf16 pairs) for dS and
         // written to TMEM as the A operand of dV += P^T dO
@@ -323,20 +324,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_wait(rr);
                 uint32_t pk[16];
 #pragma unroll
-                for (int u4 = 0; u4 < 8; ++u4) {
-                    const float4 l4 = *reinterpret_cast<const float4 *>(sL + c * 32 + 4 * u4);
-                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int u = 2 * u4 + h;
-                        const int c0 = c * 32 + 2 * u;
-                        const float p0 = ex2(fmaf(__uint_as_float(rr[2 * u]), cl2, -lv[2 * h]));
-                        const float p1 = ex2(fmaf(__uint_as_float(rr[2 * u + 1]), cl2, -lv[2 * h + 1]));
-                        const bool k0 = key_valid && (cbase + c0 >= cmin);
-                        const bool k1 = key_valid && (cbase + c0 + 1 >= cmin);
-                        pk[u] = pack_bf16x2(k0 ? p0 : 0.f, k1 ? p1 : 0.f);
-                        pkP[c * 16 + u] = pk[u];
-                    }
+                for (int u = 0; u < 16; ++u) {
+                    const int c0 = c * 32 + 2 * u;
+                    const float p0 = ex2(fmaf(__uint_as_float(rr[2 * u]), cl2, -sL[c0]));
+                    const float p1 = ex2(fmaf(__uint_as_float(rr[2 * u + 1]), cl2, -sL[c0 + 1]));
+                    const bool k0 = key_valid && (cbase + c0 >= cmin);
+                    const bool k1 = key_valid && (cbase + c0 + 1 >= cmin);
+                    pk[u] = pack_bf16x2(k0 ? p0 : 0.f, k1 ? p1 : 0.f);
+                    pkP[c * 16 + u] = pk[u];
                 }
                 tmem_st16(tS + lane_off + pbase + c * 16, pk);
             }
@@ -349,17 +344,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         QTileIter cur{0, nq - 1, 0, 0, 0};
         qiter_seek(cur, g.layout, N, e, b, nq, rows_b);
-        QTileIter nxt = cur;
-        if (nt > 1) qiter_next(nxt, g.layout, N, e, b, nq, rows_b);
         if (ok) {
-            store_stat(fetch_stat(cur));
+            load_stats(cur);
             named_bar_sync(1 + wg, 128);
             ok = compute_p(cur, 0);
         }
         for (int i = 0; i < nt && ok; ++i) {
-            // statistics of the next tile: issue the global loads now, use
-            // them after dS_i and the dQ_i readout
-            const float pre = (i + 1 < nt) ? fetch_stat(nxt) : 0.f;
             // ---- dS = P * (dP - Delta) -> smem (A operand of dQ and dK)
             if (!mbar_wait(smem_u32(&bars->dp_full), i & 1, p.err)) {
                 ok = false;
@@ -373,17 +363,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_wait(rr);
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
-                    const float4 d0 = *reinterpret_cast<const float4 *>(sD + c * 32 + 8 * v);
-                    const float4 d1 = *reinterpret_cast<const float4 *>(sD + c * 32 + 8 * v + 4);
-                    const float dv8[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
                     uint32_t w[4];
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
                         const int u = v * 4 + h;  // pair index within the chunk
+                        const int c0 = c * 32 + 2 * u;
                         __nv_bfloat162 pv = *reinterpret_cast<__nv_bfloat162 *>(&pkP[c * 16 + u]);
                         const float2 pf = __bfloat1622float2(pv);
-                        w[h] = pack_bf16x2(pf.x * (__uint_as_float(rr[2 * u]) - dv8[2 * h]),
-                                           pf.y * (__uint_as_float(rr[2 * u + 1]) - dv8[2 * h + 1]));
+                        w[h] = pack_bf16x2(pf.x * (__uint_as_float(rr[2 * u]) - sD[c0]),
+                                           pf.y * (__uint_as_float(rr[2 * u + 1]) - sD[c0 + 1]));
                     }
                     const int chunk = c * 4 + v;
                     *reinterpret_cast<uint4 *>(sDS + ((chunk ^ (row & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -393,17 +381,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready));
-            // ---- P of the next tile while the tensor core runs dQ_i and dK_i
+            // ---- P of the next tile while the tensor core runs dQ_i / dK_i
+            const QTileIter done = cur;
             if (i + 1 < nt) {
+                qiter_next(cur, g.layout, N, e, b, nq, rows_b);
                 named_bar_sync(1 + wg, 128);  // everyone is past dS_i (last use of sL/sD)
-                store_stat(pre);
+                load_stats(cur);
                 named_bar_sync(1 + wg, 128);
-                if (!compute_p(nxt, i + 1)) {
+                if (!compute_p(cur, i + 1)) {
                     ok = false;
                     break;
                 }
             }
-            // ---- dQ_i out of TMEM (frees the columns for dP_{i+1})
+            // ---- dQ_i readout -> fp32 accumulator
             if (!mbar_wait(smem_u32(&bars->dq_full), i & 1, p.err)) {
                 ok = false;
                 break;
@@ -417,23 +407,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
-            // ---- dQ_i -> fp32 accumulator
-            const int64_t qi = (int64_t)cur.a * BT + row;
-            if (qi < g.L) {
-                float *dst =
-                    p.dq_acc + (bh * g.stride_bh + (int64_t)cur.d * g.stripe_stride + qi * HD + cbase);
-#pragma unroll
-                for (int v = 0; v < 8; ++v)
-                    red_add_v4(dst + 4 * v, __uint_as_float(q0[4 * v]), __uint_as_float(q0[4 * v + 1]),
-                               __uint_as_float(q0[4 * v + 2]), __uint_as_float(q0[4 * v + 3]));
-#pragma unroll
-                for (int v = 0; v < 8; ++v)
-                    red_add_v4(dst + 32 + 4 * v, __uint_as_float(q1[4 * v]), __uint_as_float(q1[4 * v + 1]),
-                               __uint_as_float(q1[4 * v + 2]), __uint_as_float(q1[4 * v + 3]));
+            // dQ_i -> fp32 accumulator by TMA reduce-add.  Staging: warpgroup 0
+            // uses the dO_i tile buffer (dead once dV_i, covered by dq_full, is
+            // done), warpgroup 1 the Q_i buffer (dead once dK_i is done).  Two
+            // 32-column boxes of 128 rows, 128-byte swizzled.
+            const int s = i % QS;
+            uint32_t stage = sbase + kQOff + s * 2 * kTile + (wg == 0 ? kTile : 0);
+            if (wg == 1 && !mbar_wait(smem_u32(&bars->dk_done), i & 1, p.err)) {
+                ok = false;
+                break;
             }
-            cur = nxt;
-            if (i + 2 < nt) qiter_next(nxt, g.layout, N, e, b, nq, rows_b);
+#pragma unroll
+            for (int box = 0; box < 2; ++box) {
+                const uint32_t(&src)[32] = box ? q1 : q0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t addr = stage + box * kBox + row * 128 + ((j ^ (row & 7)) * 16);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(src[4 * j]),
+                                 "r"(src[4 * j + 1]), "r"(src[4 * j + 2]), "r"(src[4 * j + 3])
+                                 : "memory");
+                }
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1 + wg, 128);
+            if (wt == 0) {
+                tma_reduce_add_4d(&tmdQ, stage, cbase, done.a * BT, done.d, (int)bh);
+                tma_reduce_add_4d(&tmdQ, stage + kBox, cbase + 32, done.a * BT, done.d, (int)bh);
+                bulk_commit_group();
+                bulk_wait_group_read0();
+                mbar_arrive(smem_u32(&bars->q_empty[s]));
+            }
         }
+        if (wt == 0) bulk_wait_group0();
         if (ok) {
             ok = mbar_wait(smem_u32(&bars->acc_done), 0, p.err);
             tc_fence_after();
@@ -554,6 +559,8 @@ int launch_tc_bwd(const void *q, const void *k, const void *v, const void *o, co
         (st = make_bf16_map(&mv, v, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 128)) ||
         (st = make_bf16_map(&mdo, dO, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 128)))
         return st;
+    CUtensorMap mdq;
+    if ((st = make_f32_map(&mdq, dq_acc, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 128))) return st;
     BwdParams p{};
     p.g = g;
     p.lse = lse;
@@ -566,7 +573,7 @@ int launch_tc_bwd(const void *q, const void *k, const void *v, const void *o, co
     const int64_t nk = (g.L + BT - 1) / BT;
     const int64_t nblocks = nk * g.N * g.BH;
     if (nblocks > 0x7fffffffll) return STRIPED_ERR_UNSUPPORTED;
-    tc_bwd_kernel<<<(unsigned)nblocks, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
+    tc_bwd_kernel<<<(unsigned)nblocks, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, p);
     st = cuda_status(cudaGetLastError());
     if (st != STRIPED_OK) return st;
     bwd_post_kernel<<<sms * 8, 256, 0, stream>>>(dq_acc, (__nv_bfloat16 *)dq, rows * HD / 8, g.scale);

@@ -64,5 +64,8 @@ int launch_tc_bwd(const void *q, const void *k, const void *v, const void *o, co
 // Returns a status code.
 int make_bf16_map(CUtensorMap *map, const void *base, int64_t D, int64_t L, int64_t N, int64_t BH,
                   int64_t stripe_stride, int64_t stride_bh, int box_rows);
+// Same for fp32 tensors: boxes of 32 elements (128 bytes) x box_rows rows.
+int make_f32_map(CUtensorMap *map, const void *base, int64_t D, int64_t L, int64_t N, int64_t BH,
+                 int64_t stripe_stride, int64_t stride_bh, int box_rows);
 
 }  // namespace striped
