@@ -170,7 +170,7 @@ def run_gpu(args, rank, world, local_rank):
     lse = torch.empty(B, H, S, dtype=torch.float32, device=dev)
     dq, dk, dv = (torch.empty_like(x["q"]) for _ in range(3))
     outs = [torch.empty_like(x["q"]) for _ in range(4)]
-    ws = sp.new_workspace(B, H, S, D, torch.bfloat16, dev)
+    ws = sp.new_workspace(B, H, S, D, N, torch.bfloat16, dev)
     stats = sp.new_tile_stats(N, dev)
     ev = {k: [] for k in ("fwd", "bwd", "perm")}
 

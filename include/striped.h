@@ -101,9 +101,10 @@ int striped_attn_fwd(const void *q, const void *k, const void *v, void *o, float
                      int64_t H, int64_t S, int64_t D, int N, int layout, int dtype, float scale,
                      int64_t *tile_stats, void *stream);
 
-/* Bytes of device workspace striped_attn_bwd needs (fp32 dQ accumulator and
- * per-row softmax statistics), or 0 for invalid sizes. */
-size_t striped_workspace_size(int64_t B, int64_t H, int64_t S, int64_t D, int dtype);
+/* Bytes of device workspace striped_attn_bwd needs for these sizes (fp32 dQ
+ * accumulator and per-row softmax statistics padded to whole tiles), or 0
+ * for invalid sizes. */
+size_t striped_workspace_size(int64_t B, int64_t H, int64_t S, int64_t D, int N, int dtype);
 
 /*
  * Backward of striped_attn_fwd (training use, §Summary).  Given the forward
@@ -129,8 +130,8 @@ int striped_attn_bwd(const void *q, const void *k, const void *v, const void *o,
  * on every GPU that loads it until the process exits.  For callers whose
  * device memory is owned by an allocator or budget they cannot extend, or
  * who must keep cudaMalloc off their hot path.
- *  - Returns STRIPED_ERR_WORKSPACE when striped_workspace_size(B,H,S,D,dtype)
- *    exceeds 48 MiB (bf16, D = 128: B*H*S up to about 97,000 rows).
+ *  - Returns STRIPED_ERR_WORKSPACE when striped_workspace_size(B,H,S,D,N,dtype)
+ *    exceeds 48 MiB (bf16, D = 128: B*H*S up to about 96,000 rows).
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
  *    before any stream capture.

@@ -61,7 +61,7 @@ def load(build_if_missing: bool = True):
         lib.striped_permute.argtypes = [P, P, I64, I64, I64, I64, I, I, P]
         lib.striped_unpermute.argtypes = [P, P, I64, I64, I64, I64, I, I, P]
         lib.striped_attn_fwd.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I, I, I, F, P, P]
-        lib.striped_workspace_size.argtypes = [I64, I64, I64, I64, I]
+        lib.striped_workspace_size.argtypes = [I64, I64, I64, I64, I, I]
         lib.striped_workspace_size.restype = SZ
         lib.striped_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, I64, I64, I64, I64, I, I, I, F,
                                          P, P]
@@ -156,13 +156,13 @@ def striped_attn_fwd(q, k, v, N: int, layout: int = STRIPED, scale: float | None
     return o, lse
 
 
-def workspace_size(B: int, H: int, S: int, D: int, dtype: torch.dtype) -> int:
+def workspace_size(B: int, H: int, S: int, D: int, N: int, dtype: torch.dtype) -> int:
     code = BF16 if dtype == torch.bfloat16 else FP32
-    return int(load().striped_workspace_size(B, H, S, D, code))
+    return int(load().striped_workspace_size(B, H, S, D, N, code))
 
 
-def new_workspace(B, H, S, D, dtype, device) -> torch.Tensor:
-    n = workspace_size(B, H, S, D, dtype)
+def new_workspace(B, H, S, D, N, dtype, device) -> torch.Tensor:
+    n = workspace_size(B, H, S, D, N, dtype)
     return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
 
 
@@ -176,7 +176,7 @@ def striped_attn_bwd(q, k, v, o, lse, dO, N: int, layout: int = STRIPED, scale: 
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    ws = new_workspace(B, H, S, D, q.dtype, q.device) if workspace is None else workspace
+    ws = new_workspace(B, H, S, D, N, q.dtype, q.device) if workspace is None else workspace
     _check(load().striped_attn_bwd(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(o, "o"), _dev(lse, "lse"),
                                    _dev(dO, "dO"), _dev(dq, "dq"), _dev(dk, "dk"), _dev(dv, "dv"),
                                    _dev(ws, "workspace"), ws.numel() * ws.element_size(), B, H, S, D, N,

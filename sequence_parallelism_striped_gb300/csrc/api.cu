@@ -232,11 +232,20 @@ int striped_attn_fwd(const void *q, const void *k, const void *v, void *o, float
     return launch_tc_fwd(q, k, v, o, lse, g, tile_stats, s);
 }
 
-size_t striped_workspace_size(int64_t B, int64_t H, int64_t S, int64_t D, int dtype) {
-    if (B < 1 || H < 1 || S < 1 || D < 1) return 0;
+// bf16 workspace: fp32 dQ accumulator [B*H*S][D], then per (b, h, stripe)
+// and 128-row tile a statistics block [LSE*log2e 128 | Delta 128] (fp32).
+static size_t bf16_stats_offset(int64_t B, int64_t H, int64_t S, int64_t D) {
+    return align256((size_t)(B * H * S) * (size_t)D * sizeof(float));
+}
+
+size_t striped_workspace_size(int64_t B, int64_t H, int64_t S, int64_t D, int N, int dtype) {
+    if (B < 1 || H < 1 || S < 1 || D < 1 || N < 1 || S % N != 0) return 0;
     const size_t rows = (size_t)(B * H * S);
     if (dtype == STRIPED_FP32) return align256(rows * sizeof(float));
-    if (dtype == STRIPED_BF16) return align256(rows * (size_t)D * sizeof(float)) + align256(rows * sizeof(float));
+    if (dtype == STRIPED_BF16) {
+        const size_t nq = (size_t)((S / N + kTcTile - 1) / kTcTile);
+        return bf16_stats_offset(B, H, S, D) + align256((size_t)(B * H * N) * nq * 2 * kTcTile * sizeof(float));
+    }
     return 0;
 }
 
@@ -250,7 +259,7 @@ int striped_attn_bwd(const void *q, const void *k, const void *v, const void *o,
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
         !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
         return STRIPED_ERR_ALIGN;
-    const size_t need = striped_workspace_size(B, H, S, D, dtype);
+    const size_t need = striped_workspace_size(B, H, S, D, N, dtype);
     if (!workspace || ws_bytes < need) return STRIPED_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return STRIPED_ERR_ALIGN;
     const AttnGeom g = full_geom(B, H, S, D, N, layout, scale);
@@ -260,8 +269,8 @@ int striped_attn_bwd(const void *q, const void *k, const void *v, const void *o,
                                (const float *)dO, (float *)dq, (float *)dk, (float *)dv,
                                (float *)workspace, g, tile_stats, s);
     float *dq_acc = (float *)workspace;
-    float *delta = (float *)((char *)workspace + align256((size_t)(B * H * S * D) * sizeof(float)));
-    return launch_tc_bwd(q, k, v, o, lse, dO, dq, dk, dv, dq_acc, delta, g, tile_stats, s);
+    float *stats = (float *)((char *)workspace + bf16_stats_offset(B, H, S, D));
+    return launch_tc_bwd(q, k, v, o, lse, dO, dq, dk, dv, dq_acc, stats, g, tile_stats, s);
 }
 
 int ring_round_fwd(const void *q_d, const void *k_e, const void *v_e, float *o_acc, float *lse_acc,

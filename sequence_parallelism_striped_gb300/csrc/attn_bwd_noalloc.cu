@@ -14,15 +14,15 @@
 // share it, so calls that overlap on that GPU (different streams, or host
 // threads racing on one device) corrupt each other's results.  It keeps
 // whatever the previous call left; the backward's first kernel rewrites
-// every word it later reads (Delta) and zeroes the dQ accumulator itself.
+// every statistic it later reads and zeroes the dQ accumulator itself.
 #include <mutex>
 
 #include "internal.h"
 
 namespace striped {
 
-// 48 MiB: enough for B*H*S rows with D = 128 up to 97,000 rows (e.g. the
-// short-sequence workload B=1, H=8, S=8192), and for fp32 heads of any D.
+// 48 MiB: enough for B*H*S rows with D = 128 up to about 96,000 rows (e.g.
+// the short-sequence workload B=1, H=8, S=8192), and for fp32 heads of any D.
 constexpr size_t kNoAllocScratchBytes = size_t(48) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -55,7 +55,7 @@ extern "C" int striped_attn_bwd_noalloc(const void *q, const void *k, const void
                                         int64_t B, int64_t H, int64_t S, int64_t D, int N, int layout,
                                         int dtype, float scale, int64_t *tile_stats, void *stream) {
     using namespace striped;
-    const size_t need = striped_workspace_size(B, H, S, D, dtype);
+    const size_t need = striped_workspace_size(B, H, S, D, N, dtype);
     if (need > kNoAllocScratchBytes) return STRIPED_ERR_WORKSPACE;  // problem too large for the array
     void *scratch = nullptr;
     const int st = noalloc_scratch(&scratch);

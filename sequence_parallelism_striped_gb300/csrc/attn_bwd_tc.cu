@@ -52,16 +52,16 @@ constexpr uint32_t kKOff = 0;
 constexpr uint32_t kVOff = kTile;
 constexpr uint32_t kQOff = 2 * kTile;                 // stage s: Q at kQOff + s*2*kTile, dO after
 constexpr uint32_t kDSOff = kQOff + QS * 2 * kTile;   // dS (MN-major A operand)
-constexpr uint32_t kStatOff = kDSOff + kTile;         // per warpgroup: [lse2 64 | delta 64] floats
-constexpr uint32_t kBarOff = kStatOff + 2 * 128 * 4;
-constexpr size_t kSmemBytes = 1024 + kBarOff + 256;
+constexpr uint32_t kStatOff = kDSOff + kTile;         // per stage: [LSE*log2e 128 | Delta 128] floats
+constexpr uint32_t kStatBytes = 2 * 128 * 4;
+constexpr uint32_t kBarOff = kStatOff + QS * kStatBytes;
+constexpr size_t kSmemBytes = kBarOff + 256;            // the dynamic smem base is 1024-aligned
 static_assert(kSmemBytes <= 232448, "shared memory over the per-block limit");
 constexpr int kThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 4..11 compute
 
 struct BwdParams {
     AttnGeom g;
-    const float *lse;    // [BH][S] natural log
-    const float *delta;  // [BH][S]
+    const float *stats;  // [BH][N][nq][LSE*log2e 128 | Delta 128], padded per 128-row tile
     float *dq_acc;       // [BH][S][D] fp32
     __nv_bfloat16 *dk, *dv;
     int64_t *tile_stats;
@@ -81,48 +81,60 @@ __device__ __forceinline__ int tile_rows(int64_t L, int t) {
     return r >= BT ? BT : (int)r;
 }
 
-// Order in which a key tile visits its query tiles: stripes d = 0..N-1,
-// and within a stripe a = nq-1 down to the first tile that sees the key
-// tile (the diagonal, if any, last).
+#ifndef BWD_RING_ORDER
+#define BWD_RING_ORDER 0
+#endif
+#ifndef BWD_ASCENDING
+#define BWD_ASCENDING 0
+#endif
+// Order in which a key tile visits its query tiles: stripes d = d0, d0+1,
+// ... (mod N), and within a stripe the tiles that see the key tile, in
+// ascending or descending order.
 struct QTileIter {
-    int d, a, a_lo, has_diag, diag_off;
+    int k, d, a, a_lo, has_diag, diag_off;
 };
 
 __device__ __forceinline__ void qiter_seek(QTileIter &it, int layout, int N, int e, int b, int nq, int rows_b) {
-    while (it.d < N) {
+    while (it.k < N) {
+        it.d = BWD_RING_ORDER ? (e + it.k) % N : it.k;
         const QuerySpan sp = query_span(layout, it.d, e, b, nq, rows_b);
         if (sp.a_lo < nq) {
             it.a_lo = sp.a_lo;
             it.has_diag = sp.has_diag;
             it.diag_off = sp.diag_off;
+            it.a = BWD_ASCENDING ? sp.a_lo : nq - 1;
             return;
         }
-        ++it.d;
-        it.a = nq - 1;
+        ++it.k;
     }
 }
 
+__device__ __forceinline__ QTileIter qiter_begin(int layout, int N, int e, int b, int nq, int rows_b) {
+    QTileIter it{0, 0, 0, 0, 0, 0};
+    qiter_seek(it, layout, N, e, b, nq, rows_b);
+    return it;
+}
+
 __device__ __forceinline__ void qiter_next(QTileIter &it, int layout, int N, int e, int b, int nq, int rows_b) {
-    if (--it.a < it.a_lo) {
-        ++it.d;
-        it.a = nq - 1;
+    const bool end = BWD_ASCENDING ? (++it.a >= nq) : (--it.a < it.a_lo);
+    if (end) {
+        ++it.k;
         qiter_seek(it, layout, N, e, b, nq, rows_b);
     }
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                   const __grid_constant__ CUtensorMap tmdQ, const BwdParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw;
+    if ((smem_u32(smem) & 1023u) != 0) {  // operand tiles need 1024-byte alignment
+        if (threadIdx.x == 0 && p.err) atomicExch(p.err, STRIPED_ERR_ALIGN);
+        return;
+    }
     Bars *bars = reinterpret_cast<Bars *>(smem + kBarOff);
-    float *sStat = reinterpret_cast<float *>(smem + kStatOff);
     const uint32_t sbase = smem_u32(smem);
     const AttnGeom &g = p.g;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -147,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&bars->kv_full), 1);
         for (int s = 0; s < QS; ++s) {
             mbar_init(smem_u32(&bars->q_full[s]), 1);
-            mbar_init(smem_u32(&bars->q_empty[s]), 2);  // one arrival per compute warpgroup
+            mbar_init(smem_u32(&bars->q_empty[s]), 8);  // one arrival per compute warp
         }
         mbar_init(smem_u32(&bars->s_full), 1);
         mbar_init(smem_u32(&bars->dp_full), 1);
@@ -193,25 +205,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(sbase + kKOff + kBox, &tmK, kb, 64, b * BT, e, (int)bh);
         tma_load_4d(sbase + kVOff, &tmV, kb, 0, b * BT, e, (int)bh);
         tma_load_4d(sbase + kVOff + kBox, &tmV, kb, 64, b * BT, e, (int)bh);
-        int i = 0;
-        bool ok = true;
-        for (int d = 0; d < N && ok; ++d) {
-            const QuerySpan sp = query_span(g.layout, d, e, b, nq, rows_b);
-            for (int a = nq - 1; a >= sp.a_lo; --a, ++i) {
-                const int s = i % QS;
-                if (i >= QS && !mbar_wait(smem_u32(&bars->q_empty[s]), ((i / QS) + 1) & 1, p.err)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t fb = smem_u32(&bars->q_full[s]);
-                const uint32_t qdst = sbase + kQOff + s * 2 * kTile;
-                const uint32_t odst = qdst + kTile;
-                mbar_arrive_expect_tx(fb, 2 * kTile);
-                tma_load_4d(qdst, &tmQ, fb, 0, a * BT, d, (int)bh);
-                tma_load_4d(qdst + kBox, &tmQ, fb, 64, a * BT, d, (int)bh);
-                tma_load_4d(odst, &tmdO, fb, 0, a * BT, d, (int)bh);
-                tma_load_4d(odst + kBox, &tmdO, fb, 64, a * BT, d, (int)bh);
-            }
+        QTileIter it = qiter_begin(g.layout, N, e, b, nq, rows_b);
+        for (int i = 0; i < nt; ++i, qiter_next(it, g.layout, N, e, b, nq, rows_b)) {
+            const int s = i % QS;
+            if (i >= QS && !mbar_wait(smem_u32(&bars->q_empty[s]), ((i / QS) + 1) & 1, p.err)) break;
+            const uint32_t fb = smem_u32(&bars->q_full[s]);
+            const uint32_t qdst = sbase + kQOff + s * 2 * kTile;
+            const uint32_t odst = qdst + kTile;
+            mbar_arrive_expect_tx(fb, 2 * kTile + kStatBytes);
+            bulk_load(sbase + kStatOff + s * kStatBytes,
+                      p.stats + (((bh * N + it.d) * (int64_t)nq + it.a) << 8), kStatBytes, fb);
+            tma_load_4d(qdst, &tmQ, fb, 0, it.a * BT, it.d, (int)bh);
+            tma_load_4d(qdst + kBox, &tmQ, fb, 64, it.a * BT, it.d, (int)bh);
+            tma_load_4d(odst, &tmdO, fb, 0, it.a * BT, it.d, (int)bh);
+            tma_load_4d(odst + kBox, &tmdO, fb, 64, it.a * BT, it.d, (int)bh);
         }
     } else if (warp == 1 && lane == 0 && nt > 0) {
         // ---------------- MMA issuer
@@ -288,32 +295,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int wg = (warp - 4) >> 2;       // 0: columns 0..63, 1: columns 64..127
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;  // key row of S^T/dP^T; query row of dQ
-        const int wt = threadIdx.x - 128 - wg * 128;
         const int cbase = wg * 64;            // first column of this warpgroup
         const uint32_t pbase = wg * 64;       // TMEM columns of this warpgroup's P^T pairs
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const float cl2 = g.scale * 1.4426950408889634f;
         const bool key_valid = row < rows_b;
-        float *sL = sStat + wg * 128, *sD = sL + 64;
         uint8_t *sDS = smem + kDSOff + wg * kBox + row * 128;
         bool ok = nt > 0;
 
-        // per-query statistics of a tile -> smem (callers fence with barriers)
-        auto load_stats = [&](const QTileIter &t) {
-            const int c = wt & 63;
-            const int64_t qi = (int64_t)t.a * BT + cbase + c;
-            const int64_t srow = bh * g.lse_stride_bh + (int64_t)t.d * g.lse_stripe_stride + qi;
-            const bool qv = qi < g.L;
-            // an out-of-range query gets LSE = +inf, hence P = 0
-            if (wt < 64) sL[c] = qv ? p.lse[srow] * 1.4426950408889634f : INFINITY;
-            else sD[c] = qv ? p.delta[srow] : 0.f;
+        // per-query statistics of tile i (bulk-copied with Q_i/dO_i):
+        // LSE*log2e (+inf past the stripe end, so P = 0 there) and Delta
+        auto stat_ptr = [&](int i) -> const float * {
+            return reinterpret_cast<const float *>(smem + kStatOff + (i % QS) * kStatBytes) + cbase;
         };
         // P^T of tile t (index i): kept in registers (bf16 pairs) for dS and
         // written to TMEM as the A operand of dV += P^T dO
         uint32_t pkP[32];
         auto compute_p = [&](const QTileIter &t, int i) -> bool {
+            if (!mbar_wait(smem_u32(&bars->q_full[i % QS]), (i / QS) & 1, p.err)) return false;
             if (!mbar_wait(smem_u32(&bars->s_full), i & 1, p.err)) return false;
             tc_fence_after();
+            const float *sL = stat_ptr(i);
             const bool diag = t.has_diag && t.a == t.a_lo;
             // keep pair (query col, key row) iff row <= col + diag_off
             const int cmin = diag ? row - t.diag_off : 0;
@@ -342,13 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             return true;
         };
 
-        QTileIter cur{0, nq - 1, 0, 0, 0};
-        qiter_seek(cur, g.layout, N, e, b, nq, rows_b);
-        if (ok) {
-            load_stats(cur);
-            named_bar_sync(1 + wg, 128);
-            ok = compute_p(cur, 0);
-        }
+        QTileIter cur = qiter_begin(g.layout, N, e, b, nq, rows_b);
+        if (ok) ok = compute_p(cur, 0);
         for (int i = 0; i < nt && ok; ++i) {
             // ---- dS = P * (dP - Delta) -> smem (A operand of dQ and dK)
             if (!mbar_wait(smem_u32(&bars->dp_full), i & 1, p.err)) {
@@ -356,6 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
+            const float *sD = stat_ptr(i) + 128;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 uint32_t rr[32];
@@ -385,9 +383,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const QTileIter done = cur;
             if (i + 1 < nt) {
                 qiter_next(cur, g.layout, N, e, b, nq, rows_b);
-                named_bar_sync(1 + wg, 128);  // everyone is past dS_i (last use of sL/sD)
-                load_stats(cur);
-                named_bar_sync(1 + wg, 128);
                 if (!compute_p(cur, i + 1)) {
                     ok = false;
                     break;
@@ -409,8 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
             // dQ_i -> fp32 accumulator by TMA reduce-add.  Staging: warpgroup 0
             // uses the dO_i tile buffer (dead once dV_i, covered by dq_full, is
-            // done), warpgroup 1 the Q_i buffer (dead once dK_i is done).  Two
-            // 32-column boxes of 128 rows, 128-byte swizzled.
+            // done), warpgroup 1 the Q_i buffer (dead once dK_i is done); two
+            // 128-byte-swizzled 32-column boxes.  Each warp reduces its own 32
+            // rows, so no warpgroup barrier is needed.
             const int s = i % QS;
             uint32_t stage = sbase + kQOff + s * 2 * kTile + (wg == 0 ? kTile : 0);
             if (wg == 1 && !mbar_wait(smem_u32(&bars->dk_done), i & 1, p.err)) {
@@ -429,16 +425,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             fence_proxy_async_smem();
-            named_bar_sync(1 + wg, 128);
-            if (wt == 0) {
-                tma_reduce_add_4d(&tmdQ, stage, cbase, done.a * BT, done.d, (int)bh);
-                tma_reduce_add_4d(&tmdQ, stage + kBox, cbase + 32, done.a * BT, done.d, (int)bh);
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t wofs = (uint32_t)quarter * 32 * 128;
+                const int r0 = done.a * BT + quarter * 32;
+                tma_reduce_add_4d(&tmdQ, stage + wofs, cbase, r0, done.d, (int)bh);
+                tma_reduce_add_4d(&tmdQ, stage + kBox + wofs, cbase + 32, r0, done.d, (int)bh);
                 bulk_commit_group();
                 bulk_wait_group_read0();
                 mbar_arrive(smem_u32(&bars->q_empty[s]));
             }
         }
-        if (wt == 0) bulk_wait_group0();
+        if (lane == 0) bulk_wait_group0();
         if (ok) {
             ok = mbar_wait(smem_u32(&bars->acc_done), 0, p.err);
             tc_fence_after();
@@ -485,25 +483,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// Delta_p = <dO_p, O_p> (fp32) and a zeroed dQ accumulator row; one warp
-// per row of D = 128 (each lane: 4 elements of dO/O, 4 floats of dQ).
+// Per row of every stripe, padded to whole 128-row tiles: the tile-major
+// statistics block [LSE*log2e 128 | Delta 128] with Delta_p = <dO_p, O_p>
+// (fp32); padding rows get LSE = +inf and Delta = 0.  Real rows also get
+// their dQ accumulator row zeroed.  One warp per padded row, D = 128.
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o,
                                                       const __nv_bfloat16 *__restrict__ dO,
-                                                      float *__restrict__ delta, float *__restrict__ dq_acc,
-                                                      int64_t rows) {
+                                                      const float *__restrict__ lse, float *__restrict__ stats,
+                                                      float *__restrict__ dq_acc, int64_t L, int nq,
+                                                      int64_t padded_rows) {
     const int lane = threadIdx.x & 31;
+    const int64_t per_stripe = (int64_t)nq * BT;
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    for (int64_t rw = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); rw < rows; rw += nwarps) {
+    for (int64_t pr = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); pr < padded_rows;
+         pr += nwarps) {
+        const int64_t stripe = pr / per_stripe;  // bh * N + d
+        const int64_t ii = pr - stripe * per_stripe;
+        float *blk = stats + ((stripe * nq + (ii >> 7)) << 8) + (ii & 127);
+        if (ii >= L) {
+            if (lane == 0) {
+                blk[0] = INFINITY;
+                blk[128] = 0.f;
+            }
+            continue;
+        }
+        const int64_t rw = stripe * L + ii;  // row of the [BH][S] tensors
         const uint2 ov = *reinterpret_cast<const uint2 *>(o + rw * HD + lane * 4);
         const uint2 gv = *reinterpret_cast<const uint2 *>(dO + rw * HD + lane * 4);
         const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&ov);
         const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&gv);
         float2 a0 = __bfloat1622float2(o2[0]), a1 = __bfloat1622float2(o2[1]);
         float2 b0 = __bfloat1622float2(g2[0]), b1 = __bfloat1622float2(g2[1]);
-        float s = a0.x * b0.x + a0.y * b0.y + a1.x * b1.x + a1.y * b1.y;
+        float sum = a0.x * b0.x + a0.y * b0.y + a1.x * b1.x + a1.y * b1.y;
 #pragma unroll
-        for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        if (lane == 0) delta[rw] = s;
+        for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        if (lane == 0) {
+            blk[0] = lse[rw] * 1.4426950408889634f;
+            blk[128] = sum;
+        }
         *reinterpret_cast<float4 *>(dq_acc + rw * HD + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 }
@@ -538,7 +555,7 @@ int num_sms() {
 }  // namespace
 
 int launch_tc_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
-                  const void *dO, void *dq, void *dk, void *dv, float *dq_acc, float *delta,
+                  const void *dO, void *dq, void *dk, void *dv, float *dq_acc, float *stats,
                   const AttnGeom &g, int64_t *tile_stats, cudaStream_t stream) {
     static int attr = 1;
     if (attr == 1) {
@@ -549,8 +566,9 @@ int launch_tc_bwd(const void *q, const void *k, const void *v, const void *o, co
     if (attr != STRIPED_OK) return attr;
     const int64_t rows = g.BH * g.N * g.L;
     const int sms = num_sms();
-    bwd_pre_kernel<<<sms * 8, 256, 0, stream>>>((const __nv_bfloat16 *)o, (const __nv_bfloat16 *)dO, delta,
-                                                dq_acc, rows);
+    const int nq = (int)((g.L + BT - 1) / BT);
+    bwd_pre_kernel<<<sms * 8, 256, 0, stream>>>((const __nv_bfloat16 *)o, (const __nv_bfloat16 *)dO, lse, stats,
+                                                dq_acc, g.L, nq, g.BH * g.N * (int64_t)nq * BT);
     int st = cuda_status(cudaGetLastError());
     if (st != STRIPED_OK) return st;
     CUtensorMap mq, mk, mv, mdo;
@@ -560,11 +578,10 @@ int launch_tc_bwd(const void *q, const void *k, const void *v, const void *o, co
         (st = make_bf16_map(&mdo, dO, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 128)))
         return st;
     CUtensorMap mdq;
-    if ((st = make_f32_map(&mdq, dq_acc, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 128))) return st;
+    if ((st = make_f32_map(&mdq, dq_acc, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 32))) return st;
     BwdParams p{};
     p.g = g;
-    p.lse = lse;
-    p.delta = delta;
+    p.stats = stats;
     p.dq_acc = dq_acc;
     p.dk = (__nv_bfloat16 *)dk;
     p.dv = (__nv_bfloat16 *)dv;

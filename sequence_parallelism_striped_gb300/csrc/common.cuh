@@ -187,6 +187,15 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *m, 
         : "memory");
 }
 
+// Plain bulk copy global -> shared of `bytes` (multiple of 16, both
+// addresses 16-byte aligned), completing on an mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 // Element-wise add of a shared-memory box into global memory through the
 // tensor map (out-of-range rows are skipped), tracked by the bulk group of
 // the issuing thread.

@@ -56,7 +56,7 @@ int launch_tc_round(const void *q_d, const void *k_e, const void *v_e, float *o_
                     void *o_out, int d, int e, int first, const AttnGeom &g, int64_t *tile_stats,
                     cudaStream_t stream);
 int launch_tc_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
-                  const void *dO, void *dq, void *dk, void *dv, float *dq_acc, float *delta,
+                  const void *dO, void *dq, void *dk, void *dv, float *dq_acc, float *stats,
                   const AttnGeom &g, int64_t *tile_stats, cudaStream_t stream);
 
 // bf16 tensor viewed as [BH][N][L][D] -> 4-D tensor map with boxes of

@@ -91,7 +91,7 @@ def test_bwd_workspace_contents_ignored():
     x = inputs(B, H, S, D, torch.bfloat16, seed=8)
     q, k, v, do = (to_layout(x[n], N, sp.STRIPED, DEV) for n in ("q", "k", "v", "do"))
     o, lse = sp.striped_attn_fwd(q, k, v, N)
-    ws = sp.new_workspace(B, H, S, D, torch.bfloat16, DEV)
+    ws = sp.new_workspace(B, H, S, D, N, torch.bfloat16, DEV)
     ws.fill_(0x7f)
     g1 = sp.striped_attn_bwd(q, k, v, o, lse, do, N, workspace=ws)
     ws.fill_(0x11)

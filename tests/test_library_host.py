@@ -97,10 +97,13 @@ def test_invalid_arguments_rejected_on_host(lib):
 def test_workspace_size(lib):
     import torch
 
-    B, H, S, D = 2, 3, 512, 128
-    n = sp.workspace_size(B, H, S, D, torch.bfloat16)
-    assert n >= B * H * S * D * 4 + B * H * S * 4 and n % 256 == 0
-    assert sp.workspace_size(1, 1, 256, 64, torch.float32) >= 256 * 4
+    B, H, S, D, N = 2, 3, 512, 128, 4
+    n = sp.workspace_size(B, H, S, D, N, torch.bfloat16)
+    assert n >= B * H * S * D * 4 + 2 * B * H * S * 4 and n % 256 == 0
+    # statistics are padded to whole 128-row tiles per stripe: L = 129 -> 2 tiles
+    assert sp.workspace_size(1, 1, 4 * 129, D, 4, torch.bfloat16) >= 4 * 129 * D * 4 + 4 * 2 * 256 * 4
+    assert sp.workspace_size(1, 1, 256, 64, 4, torch.float32) >= 256 * 4
+    assert sp.workspace_size(1, 1, 257, 64, 4, torch.float32) == 0
 
 
 def test_status_strings(lib):
