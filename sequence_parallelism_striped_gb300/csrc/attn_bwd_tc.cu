@@ -13,10 +13,11 @@
 // Three kernels:
 //   bwd_pre    Delta_p = <dO_p, O_p> (fp32) and zero the fp32 dQ accumulator
 //   bwd_main   one CTA per 128-key tile; loops over the query tiles that see
-//              it.  warp 0 = TMA producer (K, V once; Q_i, dO_i 2-stage
-//              ring), warp 1 = TMEM allocator + MMA issuer, warps 4..11 =
-//              two compute warpgroups; thread t of a warpgroup owns key row
-//              t of S^T/dP^T (query row t of dQ), warpgroup 0 columns
+//              it.  warp 0 = TMA producer (K, V once; then Q_i with its
+//              statistics, 2 stages), warp 2 = TMA producer of dO_i (own
+//              2-stage stream), warp 1 = TMEM allocator + MMA issuer, warps
+//              4..11 = two compute warpgroups; thread t of a warpgroup owns
+//              key row t of S^T/dP^T (query row t of dQ), warpgroup 0 columns
 //              0..63 and warpgroup 1 columns 64..127.
 //              TMEM: S^T [0,128) (P^T bf16 pairs over it), dP^T [128,256)
 //              (dQ_i over it once dS_i is formed), dV [256,384), dK [384,512).
@@ -29,11 +30,10 @@
 //              operand both ways, so dS^T never goes through TMEM.  Issue
 //              order dV_i, S_{i+1}, dQ_i, dK_i, dP_{i+1} keeps the tensor core
 //              busy while the compute warps form dS_i, P_{i+1} and read dQ_i
-//              out.  dQ_i is added to the fp32 accumulator by TMA bulk
-//              reduce-add from shared memory, staged in the tile buffers that
-//              are dead by then (dO_i after dV_i, Q_i after dK_i), so the
-//              reduction travels as whole swizzled boxes, not as per-thread
-//              16-byte atomics.
+//              out.  dQ_i goes to the fp32 accumulator half by vector
+//              reductions (warpgroup 0) and half by TMA bulk reduce-add from
+//              the dO_i buffer, dead by then (warpgroup 1); Q_i is released
+//              as soon as dK_i completes so the next Q tile loads early.
 //   bwd_post   dQ = bf16(scale * accumulator)
 #include <math.h>
 
@@ -70,9 +70,9 @@ struct BwdParams {
 
 struct Bars {
     uint64_t kv_full;
-    uint64_t q_full[QS];
-    uint64_t q_empty[QS];
-    uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, dq_free, dk_done, acc_done;
+    uint64_t q_full[QS], q_empty[QS];    // Q_i + statistics of tile i
+    uint64_t do_full[QS], do_empty[QS];  // dO_i (its buffer also stages half of dQ_i)
+    uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, dq_free, acc_done;
     uint32_t tmem_slot;
 };
 
@@ -159,7 +159,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&bars->kv_full), 1);
         for (int s = 0; s < QS; ++s) {
             mbar_init(smem_u32(&bars->q_full[s]), 1);
-            mbar_init(smem_u32(&bars->q_empty[s]), 8);  // one arrival per compute warp
+            mbar_init(smem_u32(&bars->q_empty[s]), 1);   // released by dK_i's commit
+            mbar_init(smem_u32(&bars->do_full[s]), 1);
+            mbar_init(smem_u32(&bars->do_empty[s]), 4);  // one arrival per warpgroup-1 warp
         }
         mbar_init(smem_u32(&bars->s_full), 1);
         mbar_init(smem_u32(&bars->dp_full), 1);
@@ -167,7 +169,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&bars->ds_ready), 8);
         mbar_init(smem_u32(&bars->dq_full), 1);
         mbar_init(smem_u32(&bars->dq_free), 8);
-        mbar_init(smem_u32(&bars->dk_done), 1);
         mbar_init(smem_u32(&bars->acc_done), 1);
         fence_barrier_init();
         if (p.tile_stats) {
@@ -194,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
 
     if (warp == 0 && lane == 0 && nt > 0) {
-        // ---------------- TMA producer
+        // ---------------- TMA producer: K, V once, then Q_i + statistics
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
@@ -211,12 +212,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (i >= QS && !mbar_wait(smem_u32(&bars->q_empty[s]), ((i / QS) + 1) & 1, p.err)) break;
             const uint32_t fb = smem_u32(&bars->q_full[s]);
             const uint32_t qdst = sbase + kQOff + s * 2 * kTile;
-            const uint32_t odst = qdst + kTile;
-            mbar_arrive_expect_tx(fb, 2 * kTile + kStatBytes);
+            mbar_arrive_expect_tx(fb, kTile + kStatBytes);
             bulk_load(sbase + kStatOff + s * kStatBytes,
                       p.stats + (((bh * N + it.d) * (int64_t)nq + it.a) << 8), kStatBytes, fb);
             tma_load_4d(qdst, &tmQ, fb, 0, it.a * BT, it.d, (int)bh);
             tma_load_4d(qdst + kBox, &tmQ, fb, 64, it.a * BT, it.d, (int)bh);
+        }
+    } else if (warp == 2 && lane == 0 && nt > 0) {
+        // ---------------- TMA producer: dO_i (its own stream: the buffer is
+        // released later than Q_i's, after the dQ_i half staged in it is read)
+        tma_prefetch_desc(&tmdO);
+        QTileIter it = qiter_begin(g.layout, N, e, b, nq, rows_b);
+        for (int i = 0; i < nt; ++i, qiter_next(it, g.layout, N, e, b, nq, rows_b)) {
+            const int s = i % QS;
+            if (i >= QS && !mbar_wait(smem_u32(&bars->do_empty[s]), ((i / QS) + 1) & 1, p.err)) break;
+            const uint32_t fb = smem_u32(&bars->do_full[s]);
+            const uint32_t odst = sbase + kQOff + s * 2 * kTile + kTile;
+            mbar_arrive_expect_tx(fb, kTile);
             tma_load_4d(odst, &tmdO, fb, 0, it.a * BT, it.d, (int)bh);
             tma_load_4d(odst + kBox, &tmdO, fb, 64, it.a * BT, it.d, (int)bh);
         }
@@ -243,7 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(smem_u32(&bars->s_full));
             return true;
         };
-        auto issue_dp = [&](int t) {
+        auto issue_dp = [&](int t) -> bool {
+            if (!mbar_wait(smem_u32(&bars->do_full[t % QS]), (t / QS) & 1, p.err)) return false;
+            tc_fence_after();
             const uint32_t oaddr = sbase + kQOff + (t % QS) * 2 * kTile + kTile;
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk) {
@@ -252,9 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                        id_kk, kk > 0 ? 1u : 0u);
             }
             mma_commit(smem_u32(&bars->dp_full));
+            return true;
         };
         bool ok = mbar_wait(smem_u32(&bars->kv_full), 0, p.err) && issue_s(0);
-        if (ok) issue_dp(0);
+        if (ok) ok = issue_dp(0);
         for (int i = 0; i < nt && ok; ++i) {
             const int s = i % QS;
             const uint32_t qaddr = sbase + kQOff + s * 2 * kTile;
@@ -281,12 +296,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < BT / 16; ++kk)
                 mma_ss(tdK, sdesc_sw128(sbase + kDSOff + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024),
                        sdesc_sw128(qaddr + kk * 2048, kBox, 1024), id_kmn, (i > 0 || kk > 0) ? 1u : 0u);
-            // the Q_i buffer is free once dK_i completes (it becomes dQ_i staging)
-            mma_commit(smem_u32(&bars->dk_done));
+            // Q_i (and its statistics) are free once dK_i completes
+            if (i + QS < nt) mma_commit(smem_u32(&bars->q_empty[s]));
             if (i + 1 < nt) {
                 if (!mbar_wait(smem_u32(&bars->dq_free), i & 1, p.err)) break;
                 tc_fence_after();
-                issue_dp(i + 1);
+                if (!issue_dp(i + 1)) break;
             }
         }
         if (ok) mma_commit(smem_u32(&bars->acc_done));
@@ -402,38 +417,51 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
-            // dQ_i -> fp32 accumulator by TMA reduce-add.  Staging: warpgroup 0
-            // uses the dO_i tile buffer (dead once dV_i, covered by dq_full, is
-            // done), warpgroup 1 the Q_i buffer (dead once dK_i is done); two
-            // 128-byte-swizzled 32-column boxes.  Each warp reduces its own 32
-            // rows, so no warpgroup barrier is needed.
+            // dQ_i -> fp32 accumulator, split over two paths so neither the
+            // TMA engine nor the load/store unit carries all of it: warpgroup 0
+            // adds its 64 columns with vector reductions; warpgroup 1 stages its
+            // 64 columns in the dO_i buffer (dead once dV_i, covered by
+            // dq_full, is done) as two 128-byte-swizzled 32-column boxes and
+            // each warp bulk-reduces its own 32 rows, then returns the buffer.
             const int s = i % QS;
-            uint32_t stage = sbase + kQOff + s * 2 * kTile + (wg == 0 ? kTile : 0);
-            if (wg == 1 && !mbar_wait(smem_u32(&bars->dk_done), i & 1, p.err)) {
-                ok = false;
-                break;
-            }
+            if (wg == 0) {
+                const int64_t qi = (int64_t)done.a * BT + row;
+                if (qi < g.L) {
+                    float *dst =
+                        p.dq_acc + (bh * g.stride_bh + (int64_t)done.d * g.stripe_stride + qi * HD + cbase);
 #pragma unroll
-            for (int box = 0; box < 2; ++box) {
-                const uint32_t(&src)[32] = box ? q1 : q0;
+                    for (int v = 0; v < 8; ++v)
+                        red_add_v4(dst + 4 * v, __uint_as_float(q0[4 * v]), __uint_as_float(q0[4 * v + 1]),
+                                   __uint_as_float(q0[4 * v + 2]), __uint_as_float(q0[4 * v + 3]));
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t addr = stage + box * kBox + row * 128 + ((j ^ (row & 7)) * 16);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(src[4 * j]),
-                                 "r"(src[4 * j + 1]), "r"(src[4 * j + 2]), "r"(src[4 * j + 3])
-                                 : "memory");
+                    for (int v = 0; v < 8; ++v)
+                        red_add_v4(dst + 32 + 4 * v, __uint_as_float(q1[4 * v]), __uint_as_float(q1[4 * v + 1]),
+                                   __uint_as_float(q1[4 * v + 2]), __uint_as_float(q1[4 * v + 3]));
                 }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                const uint32_t wofs = (uint32_t)quarter * 32 * 128;
-                const int r0 = done.a * BT + quarter * 32;
-                tma_reduce_add_4d(&tmdQ, stage + wofs, cbase, r0, done.d, (int)bh);
-                tma_reduce_add_4d(&tmdQ, stage + kBox + wofs, cbase + 32, r0, done.d, (int)bh);
-                bulk_commit_group();
-                bulk_wait_group_read0();
-                mbar_arrive(smem_u32(&bars->q_empty[s]));
+            } else {
+                const uint32_t stage = sbase + kQOff + s * 2 * kTile + kTile;
+#pragma unroll
+                for (int box = 0; box < 2; ++box) {
+                    const uint32_t(&src)[32] = box ? q1 : q0;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t addr = stage + box * kBox + row * 128 + ((j ^ (row & 7)) * 16);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(src[4 * j]),
+                                     "r"(src[4 * j + 1]), "r"(src[4 * j + 2]), "r"(src[4 * j + 3])
+                                     : "memory");
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t wofs = (uint32_t)quarter * 32 * 128;
+                    const int r0 = done.a * BT + quarter * 32;
+                    tma_reduce_add_4d(&tmdQ, stage + wofs, cbase, r0, done.d, (int)bh);
+                    tma_reduce_add_4d(&tmdQ, stage + kBox + wofs, cbase + 32, r0, done.d, (int)bh);
+                    bulk_commit_group();
+                    bulk_wait_group_read0();
+                    mbar_arrive(smem_u32(&bars->do_empty[s]));
+                }
             }
         }
         if (lane == 0) bulk_wait_group0();
