@@ -35,6 +35,13 @@ WORKLOAD = {"workload": "long-context striped causal attention fwd+bwd", "B": 1,
             "l2": "inputs larger than L2 (each tensor 2.1 GB > 129 MB)"}
 
 
+# DRAM bytes (read + write) of one tc_bwd_kernel launch on this workload:
+# ncu capture of the same kernel on B=1, H=8, S=65536 (1.405 GB, see
+# profiles/tc_bwd_kernel__B1_H8_S65536_N8.md) scaled by B*H*S (x16).
+BWD_TRAFFIC_BYTES = 16 * 1.405e9
+BWD_TRAFFIC_NOTE = "ncu dram bytes of tc_bwd_kernel at B=1,H=8,S=65536 scaled by B*H*S"
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -290,6 +297,7 @@ def run_gpu(args, rank, world, local_rank):
         return
 
     peaks = _peaks()
+    perm_bytes = 8 * 2 * B * H * S * D * 2  # 4 permutes + 4 unpermutes, read + write, bf16
     bwd_fl = _flops(B, H, S, D, 10)
     bwd_achieved = bwd_fl / (bwd_ms / 1000.0) / 1e12
     line = {
@@ -303,10 +311,15 @@ def run_gpu(args, rank, world, local_rank):
         "breakdown_ms": {"fwd": fwd_ms, "bwd": bwd_ms, "permute+unpermute": perm_ms,
                          "fwd_tflops": _flops(B, H, S, D, 4) / (fwd_ms / 1000) / 1e12,
                          "bwd_tflops": bwd_achieved},
-        "roofline": {"kernel": "striped_attn_bwd (tcgen05 main loop + Delta/dQ passes)", "bound": "tensor",
+        "roofline": {"kernel": "striped_attn_bwd (tcgen05 main loop + statistics/dQ passes)", "bound": "tensor",
                      "achieved": bwd_achieved, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                      "peak_kind": f"sustained bf16 ({peaks['source']})",
-                     "frac": bwd_achieved / peaks["bf16_tflops_sustained"], "traffic": None},
+                     "frac": bwd_achieved / peaks["bf16_tflops_sustained"],
+                     "traffic": BWD_TRAFFIC_BYTES if (B, H, S, N) == (1, 32, 262144, 8) else None,
+                     "traffic_note": BWD_TRAFFIC_NOTE},
+        "roofline_permute": {"kernel": "stripe_permute_kernel (8 launches per step)", "bound": "hbm",
+                             "achieved": perm_bytes / (perm_ms / 1000.0) / 1e9, "peak": peaks["hbm_gbs"],
+                             "unit": "GB/s", "frac": perm_bytes / (perm_ms / 1000.0) / 1e9 / peaks["hbm_gbs"]},
         "tile_counts": {"T": T, "per_step_all_heads_full": int(stats_np[0].sum()),
                         "per_step_all_heads_partial": int(stats_np[1].sum()),
                         "critical_path_striped": sp.critical_path(S, N, T, T, sp.STRIPED),
