@@ -32,8 +32,10 @@
 //              busy while the compute warps form dS_i, P_{i+1} and read dQ_i
 //              out.  dQ_i goes to the fp32 accumulator half by vector
 //              reductions (warpgroup 0) and half by TMA bulk reduce-add from
-//              the dO_i buffer, dead by then (warpgroup 1); Q_i is released
-//              as soon as dK_i completes so the next Q tile loads early.
+//              the dO_i buffer, dead by then (warpgroup 1; the wait for the
+//              reduce to read the buffer is deferred by one tile); Q_i is
+//              released as soon as dK_i completes so the next Q tile loads
+//              early.
 //   bwd_post   dQ = bf16(scale * accumulator)
 #include <math.h>
 
@@ -360,6 +362,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
 
         QTileIter cur = qiter_begin(g.layout, N, e, b, nq, rows_b);
+        // warpgroup 1, lane 0: stage whose dQ bulk reduce still reads shared
+        // memory (-1: none); the wait for it is deferred to the next tile
+        int pending = -1;
+        auto release_pending = [&]() {
+            if (pending >= 0) {
+                bulk_wait_group_read0();
+                mbar_arrive(smem_u32(&bars->do_empty[pending]));
+                pending = -1;
+            }
+        };
         if (ok) ok = compute_p(cur, 0);
         for (int i = 0; i < nt && ok; ++i) {
             // ---- dS = P * (dP - Delta) -> smem (A operand of dQ and dK)
@@ -394,6 +406,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready));
+            // the previous tile's dQ reduce has had dS_i's time to read its
+            // staging: return that dO buffer to the producer now
+            if (wg == 1 && lane == 0) release_pending();
             // ---- P of the next tile while the tensor core runs dQ_i / dK_i
             const QTileIter done = cur;
             if (i + 1 < nt) {
@@ -459,11 +474,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_reduce_add_4d(&tmdQ, stage + wofs, cbase, r0, done.d, (int)bh);
                     tma_reduce_add_4d(&tmdQ, stage + kBox + wofs, cbase + 32, r0, done.d, (int)bh);
                     bulk_commit_group();
-                    bulk_wait_group_read0();
-                    mbar_arrive(smem_u32(&bars->do_empty[s]));
+                    pending = s;
                 }
             }
         }
+        if (wg == 1 && lane == 0) release_pending();
         if (lane == 0) bulk_wait_group0();
         if (ok) {
             ok = mbar_wait(smem_u32(&bars->acc_done), 0, p.err);
