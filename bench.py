@@ -57,6 +57,24 @@ def _flops(B, H, S, D, per_pair):
     return per_pair * D * B * H * S * (S + 1) / 2
 
 
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """The largest of every rank's value (the slowest rank's time); the
+    identity on one process.  Works over NCCL (device tensor) or gloo (CPU)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flop_per_rank_step: float, ms_per_step: float, world: int) -> float:
+    """Whole-job throughput: all ranks' unmasked FLOPs over the slowest
+    rank's time per step (independent replicas, weak scaling)."""
+    return world * flop_per_rank_step / (ms_per_step / 1000.0) / 1e12
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle sampling during the timed region."""
 
@@ -182,8 +200,9 @@ def run_gpu(args, rank, world, local_rank):
     stats = sp.new_tile_stats(N, dev)
     ev = {k: [] for k in ("fwd", "bwd", "perm")}
 
-    def step(record=False, layout=sp.STRIPED, src=None):
+    def step(record=False, layout=sp.STRIPED, src=None, dst=None):
         src = src if src is not None else x
+        dst = dst if dst is not None else outs
         if layout == sp.STRIPED:
             e_p0 = torch.cuda.Event(enable_timing=True) if record else None
             if record:
@@ -202,8 +221,8 @@ def run_gpu(args, rank, world, local_rank):
         sp.striped_attn_bwd(q_, k_, v_, o, lse, do_, N, layout, workspace=ws, dq=dq, dk=dk, dv=dv)
         e2.record()
         if layout == sp.STRIPED:
-            for t, dst in zip((o, dq, dk, dv), outs):
-                sp.striped_unpermute(t, N, out=dst)
+            for t, y in zip((o, dq, dk, dv), dst):
+                sp.striped_unpermute(t, N, out=y)
         if record:
             e3 = torch.cuda.Event(enable_timing=True)
             e3.record()
@@ -235,13 +254,10 @@ def run_gpu(args, rank, world, local_rank):
         dist.barrier()
     ms_total = t_start.elapsed_time(t_end)
     err = sp.check_error()
-    ms = torch.tensor([ms_total], device=dev, dtype=torch.float64)
-    if dist is not None:
-        dist.all_reduce(ms, op=dist.ReduceOp.MAX)
-    ms_step = float(ms.item()) / args.steps
+    ms_step = max_over_ranks(ms_total, dist, dev) / args.steps
 
     fl_step = _flops(B, H, S, D, 14)
-    value = world * fl_step / (ms_step / 1000.0) / 1e12
+    value = job_tflops(fl_step, ms_step, world)
     fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["fwd"])
     bwd_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["bwd"])
     perm_ms = statistics.mean(a.elapsed_time(b) + c.elapsed_time(d) for a, b, c, d in ev["perm"])
@@ -264,32 +280,69 @@ def run_gpu(args, rank, world, local_rank):
         cms = c0.elapsed_time(c1) / nc
         contig = {"ms_per_step": cms, "tflops": fl_step / (cms / 1000.0) / 1e12}
 
-    # end to end through the C ABI with host buffers (pinned), copies timed
+    # End to end through the C ABI with host buffers (pinned): every step
+    # copies its Q, K, V, dO in from host memory and its O, dQ, dK, dV back
+    # out, inside the timed region.  Copies run on their own streams and are
+    # double-buffered, so step k's compute overlaps step k+1's inputs and
+    # step k-1's outputs.
     e2e = None
     if args.e2e_steps > 0:
-        host_in = {k: torch.empty(x[k].shape, dtype=x[k].dtype, pin_memory=True) for k in ("q", "k", "v", "do")}
-        for k_ in host_in:
+        names = ("q", "k", "v", "do")
+        host_in = {k_: torch.empty(x[k_].shape, dtype=x[k_].dtype, pin_memory=True) for k_ in names}
+        for k_ in names:
             host_in[k_].copy_(x[k_])
-        host_out = [torch.empty(x["q"].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(4)]
-        dev_in = {k: torch.empty_like(x[k]) for k in host_in}
+        host_out = [[torch.empty(x["q"].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(4)]
+                    for _ in range(2)]
+        dev_in = [{k_: torch.empty_like(x[k_]) for k_ in names} for _ in range(2)]
+        dev_out = [[torch.empty_like(x["q"]) for _ in range(4)] for _ in range(2)]
+        s_comp = torch.cuda.current_stream()
+        s_h2d = torch.cuda.Stream()
+        s_d2h = torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_done = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
         torch.cuda.synchronize()
         h0 = torch.cuda.Event(enable_timing=True)
         h1 = torch.cuda.Event(enable_timing=True)
-        h0.record()
-        for _ in range(args.e2e_steps):
-            for k_ in host_in:
-                dev_in[k_].copy_(host_in[k_], non_blocking=True)
-            step(src=dev_in)
-            for t, h in zip(outs, host_out):
-                h.copy_(t, non_blocking=True)
-        h1.record()
+        h0.record(s_comp)
+        s_h2d.wait_stream(s_comp)
+        s_d2h.wait_stream(s_comp)
+        K = args.e2e_steps
+
+        def load(kk):
+            bb = kk % 2
+            with torch.cuda.stream(s_h2d):
+                if kk >= 2:
+                    s_h2d.wait_event(ev_done[bb])  # step kk-2 no longer reads this buffer
+                for k_ in names:
+                    dev_in[bb][k_].copy_(host_in[k_], non_blocking=True)
+                ev_in[bb].record(s_h2d)
+
+        load(0)
+        for kk in range(K):
+            bb = kk % 2
+            if kk + 1 < K:
+                load(kk + 1)
+            s_comp.wait_event(ev_in[bb])
+            if kk >= 2:
+                s_comp.wait_event(ev_out[bb])  # step kk-2's results have left this buffer
+            step(src=dev_in[bb], dst=dev_out[bb])
+            ev_done[bb].record(s_comp)
+            with torch.cuda.stream(s_d2h):
+                s_d2h.wait_event(ev_done[bb])
+                for t, h in zip(dev_out[bb], host_out[bb]):
+                    h.copy_(t, non_blocking=True)
+                ev_out[bb].record(s_d2h)
+        s_comp.wait_stream(s_d2h)
+        h1.record(s_comp)
         torch.cuda.synchronize()
-        e_ms = h0.elapsed_time(h1) / args.e2e_steps
+        e_ms = max_over_ranks(h0.elapsed_time(h1), dist, dev) / K
         bi = sum(t.numel() * t.element_size() for t in host_in.values())
-        bo = sum(t.numel() * t.element_size() for t in host_out)
-        e2e = {"value": world * fl_step / (e_ms / 1000.0) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
-               "d2h_bytes_per_step": bo, "ms_per_step": e_ms}
-        del host_in, host_out, dev_in
+        bo = sum(t.numel() * t.element_size() for t in host_out[0])
+        e2e = {"value": job_tflops(fl_step, e_ms, world), "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
+               "d2h_bytes_per_step": bo, "ms_per_step": e_ms, "steps": K,
+               "copies": "pinned host buffers, own streams, double-buffered (overlapped with compute)"}
+        del host_in, host_out, dev_in, dev_out
 
     if rank != 0:
         if dist is not None:
@@ -348,7 +401,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-sample", type=int, default=24576,
                     help="causal-prefix length of the timed CPU-oracle sample (0 disables)")
-    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-compare", dest="compare", action="store_false")
     for key in ("B", "H", "S", "N"):
         ap.add_argument(f"--{key}", type=int, default=None, help="override the workload (profiling cases)")
