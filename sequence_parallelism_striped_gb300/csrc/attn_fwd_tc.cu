@@ -241,13 +241,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 float sv[BN];
+                {
+                    // all four loads in flight before one wait
+                    uint32_t r0[32], r1[32], r2[32], r3[32];
+                    tmem_ld32(tS, r0);
+                    tmem_ld32(tS + 32, r1);
+                    tmem_ld32(tS + 64, r2);
+                    tmem_ld32(tS + 96, r3);
+                    tmem_ld_wait(r0);
+                    tmem_ld_wait(r1);
+                    tmem_ld_wait(r2);
+                    tmem_ld_wait(r3);
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t rr[32];
-                    tmem_ld32(tS + c * 32, rr);
-                    tmem_ld_wait(rr);
-#pragma unroll
-                    for (int u = 0; u < 32; ++u) sv[c * 32 + u] = __uint_as_float(rr[u]);
+                    for (int u = 0; u < 32; ++u) {
+                        sv[u] = __uint_as_float(r0[u]);
+                        sv[32 + u] = __uint_as_float(r1[u]);
+                        sv[64 + u] = __uint_as_float(r2[u]);
+                        sv[96 + u] = __uint_as_float(r3[u]);
+                    }
                 }
                 const bool diag = sp.has_diag && b == sp.nfull;
                 const int kv_valid = tile_rows(g.L, b);
@@ -257,24 +268,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < BN; ++c)
                         if (c > lim) sv[c] = -INFINITY;
                 }
-                float mx = sv[0];
+                // row max as 8 independent chains (a single chain of 128
+                // dependent max operations would be pure latency)
+                float mx8[8];
 #pragma unroll
-                for (int c = 1; c < BN; ++c) mx = fmaxf(mx, sv[c]);
+                for (int t = 0; t < 8; ++t) mx8[t] = sv[t];
+#pragma unroll
+                for (int c = 8; c < BN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sv[c]);
+                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
                 const float m_tile = mx * cl2;
                 // lazy rescale: move the reference only when the max grows a lot
                 bool move = (j == 0) ? true : (m_tile > m_ref + kRescaleThreshold);
                 const float m_new = move ? fmaxf(m_ref, m_tile) : m_ref;
                 const float alpha = (j == 0 || !move) ? 1.f : ex2(m_ref - m_new);
                 const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-                float sum = 0.f;
+                float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
                 uint32_t pk[BN / 2];
 #pragma unroll
                 for (int c = 0; c < BN / 2; ++c) {
                     const float p0 = ex2(fmaf(sv[2 * c], cl2, -m_use));
                     const float p1 = ex2(fmaf(sv[2 * c + 1], cl2, -m_use));
-                    sum += p0 + p1;
+                    sum8[c & 7] += p0 + p1;
                     pk[c] = pack_bf16x2(p0, p1);
                 }
+                const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                                  ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
                 {
                     uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
                     uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);

@@ -88,3 +88,59 @@ def test_full_size_sampled_parity(name):
     ek, ev = float(np.abs(dk_s - dk_ref).max()), float(np.abs(dv_s - dv_ref).max())
     print(name, "tail-key max errors dk dv", ek, ev)
     assert ek <= 2e-2 and ev <= 2e-2
+
+
+def test_mid_contiguous_and_per_round_sampled():
+    """Mid workload (B=1, H=24, S=65536, N=8) in the contiguous placement
+    (batched forward + backward) and through the per-round path (8 x 8
+    ring_round_fwd calls merged in ring order), on 2048 sampled rows."""
+    B, H, S, D, N = WORKLOADS["mid"]
+    scale = 1.0 / D ** 0.5
+    x = attention_inputs(B, H, S, D, torch.bfloat16, seed=1)
+    q, k, v, do = (x[n].to(DEV) for n in ("q", "k", "v", "do"))  # contiguous = position order
+    stats = sp.new_tile_stats(N, DEV)
+    o, lse = sp.striped_attn_fwd(q, k, v, N, sp.CONTIGUOUS, tile_stats=stats)
+    dq, dk, dv = sp.striped_attn_bwd(q, k, v, o, lse, do, N, sp.CONTIGUOUS)
+    # per-round path on the striped layout
+    qs, ks, vs = (sp.striped_permute(t, N) for t in (q, k, v))
+    o_acc = torch.empty(B, H, S, D, dtype=torch.float32, device=DEV)
+    lse_acc = torch.empty(B, H, S, dtype=torch.float32, device=DEV)
+    rstats = sp.new_tile_stats(N, DEV)
+    for d in range(N):
+        for r in range(N):
+            sp.ring_round_fwd(qs, ks, vs, o_acc, lse_acc, d, (d - r) % N, N, sp.STRIPED,
+                              first_round=(r == 0), tile_stats=rstats)
+    torch.cuda.synchronize()
+    assert sp.check_error() == 0
+    full, part = oracle.tile_counts_closed(S, N, 128, sp.CONTIGUOUS)
+    st = stats.cpu().numpy()
+    assert np.array_equal(st[0], B * H * full) and np.array_equal(st[1], B * H * part)
+    fs, ps = oracle.tile_counts_closed(S, N, 128, sp.STRIPED)
+    rs = rstats.cpu().numpy()
+    assert np.array_equal(rs[0], B * H * fs) and np.array_equal(rs[1], B * H * ps)
+
+    rows = sample_rows(2048, B, H, S, seed=1).numpy()
+    bidx, hidx = torch.as_tensor(rows[:, 0], device=DEV), torch.as_tensor(rows[:, 1], device=DEV)
+    pidx = torch.as_tensor(rows[:, 2], device=DEV)
+    sidx = torch.as_tensor(_row_of_position(rows[:, 2], S, N), device=DEV)
+    got = {"o": o[bidx, hidx, pidx].double().cpu().numpy(), "lse": lse[bidx, hidx, pidx].double().cpu().numpy(),
+           "dq": dq[bidx, hidx, pidx].double().cpu().numpy(),
+           "o_round": o_acc[bidx, hidx, sidx].double().cpu().numpy(),
+           "lse_round": lse_acc[bidx, hidx, sidx].double().cpu().numpy()}
+    worst = dict.fromkeys(got, 0.0)
+    for (b, h) in sorted({(int(r[0]), int(r[1])) for r in rows}):
+        sel = np.nonzero((rows[:, 0] == b) & (rows[:, 1] == h))[0]
+        pos = rows[sel, 2]
+        args = [x[n][b, h].double().numpy() for n in ("q", "k", "v", "do")]
+        o_ref, lse_ref = oracle.attn_fwd(args[0], args[1], args[2], scale, rows=pos)
+        _, _, dq_ref = oracle.bwd_rows(*args, scale, rows=pos)
+        for key, ref in (("o", o_ref), ("lse", lse_ref), ("dq", dq_ref), ("o_round", o_ref),
+                         ("lse_round", lse_ref)):
+            worst[key] = max(worst[key], float(np.abs(got[key][sel] - ref).max()))
+    print("mid contiguous / per-round max errors", worst)
+    assert worst["o"] <= 2e-2 and worst["dq"] <= 2e-2 and worst["o_round"] <= 2e-2
+    assert worst["lse"] <= 1e-3 and worst["lse_round"] <= 1e-3
+    # gradient invariants of the contiguous backward on every head
+    assert float((dv.double().sum(2) - do.double().sum(2)).abs().max()) <= \
+        np.sqrt(S) * 2.0 ** -9 * float(dv.abs().max()) + 2e-2
+    assert float(dk.double().sum(2).abs().max()) <= np.sqrt(S) * 2.0 ** -9 * float(dk.abs().max()) + 2e-2
