@@ -207,8 +207,8 @@ def run_gpu(args, rank, world, local_rank):
             e_p0 = torch.cuda.Event(enable_timing=True) if record else None
             if record:
                 e_p0.record()
-            for name, dst in (("q", qs), ("k", ks), ("v", vs), ("do", dos)):
-                sp.striped_permute(src[name], N, out=dst)
+            for name, buf in (("q", qs), ("k", ks), ("v", vs), ("do", dos)):
+                sp.striped_permute(src[name], N, out=buf)
             q_, k_, v_, do_ = qs, ks, vs, dos
         else:
             q_, k_, v_, do_ = src["q"], src["k"], src["v"], src["do"]
@@ -254,6 +254,10 @@ def run_gpu(args, rank, world, local_rank):
         dist.barrier()
     ms_total = t_start.elapsed_time(t_end)
     err = sp.check_error()
+    # the step's unpermuted outputs are the striped results put back in
+    # position order (checked outside the timed region)
+    outs_ok = all(torch.equal(sp.striped_unpermute(t, N), y) for t, y in zip((o, dk, dv), (outs[0], outs[2], outs[3])))
+    outs_ok = outs_ok and bool(torch.allclose(sp.striped_unpermute(dq, N).float(), outs[1].float(), atol=2e-2))
     ms_step = max_over_ranks(ms_total, dist, dev) / args.steps
 
     fl_step = _flops(B, H, S, D, 14)
@@ -337,6 +341,11 @@ def run_gpu(args, rank, world, local_rank):
         h1.record(s_comp)
         torch.cuda.synchronize()
         e_ms = max_over_ranks(h0.elapsed_time(h1), dist, dev) / K
+        # the copied-out results of the last step match the device results
+        last = host_out[(K - 1) % 2]
+        for t, h in zip((o, dq, dk, dv), last):
+            ref = sp.striped_unpermute(t, N)[0, 0, :4096].float().cpu()
+            outs_ok = outs_ok and bool(torch.allclose(ref, h[0, 0, :4096].float(), atol=2e-2))
         bi = sum(t.numel() * t.element_size() for t in host_in.values())
         bo = sum(t.numel() * t.element_size() for t in host_out[0])
         e2e = {"value": job_tflops(fl_step, e_ms, world), "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
@@ -379,6 +388,7 @@ def run_gpu(args, rank, world, local_rank):
                         "critical_path_contiguous": sp.critical_path(S, N, T, T, sp.CONTIGUOUS)},
         "gpu_launches": 12 * args.steps,
         "device_error": err,
+        "outputs_match": outs_ok,
     }
     if contig is not None:
         line["contiguous_layout"] = contig
