@@ -17,7 +17,10 @@ Causal Transformers"):
   ("an exact attention algorithm");
 * stripe placement "every N-th token" -- research.elamur.ai, §Summary;
 * contiguous placement and per-round work of Ring Attention -- §Summary,
-  first paragraph; per-round balance -- §Key points "Imbalance".
+  first paragraph; per-round balance -- §Key points "Imbalance";
+* the zig-zag placement (2N chunks, device d holds chunks d and 2N-1-d) is
+  not on the pages: it is the usual load-balanced alternative, defined in
+  ``oracle.c`` and compared against the striped placement.
 
 Pins: every function here is checked in ``tests/test_oracle.py`` against
 things other than itself (closed forms, special cases, library routines,
@@ -41,6 +44,7 @@ _lib = None
 
 STRIPED = 0
 CONTIGUOUS = 1
+ZIGZAG = 2
 
 
 def build(force: bool = False) -> str:
@@ -68,6 +72,7 @@ def _load():
             lib.oracle_position_of_row.argtypes = [I64, I64, I, I]
             lib.oracle_position_of_row.restype = I64
             lib.oracle_stripe_positions.argtypes = [I64, I, P]
+            lib.oracle_zigzag_positions.argtypes = [I64, I, P]
             lib.oracle_attn_fwd.argtypes = [P, P, P, I64, I64, Dbl, P, I64, P, P, P, I]
             lib.oracle_bwd_rows.argtypes = [P, P, P, P, I64, I64, Dbl, P, I64, P, P, P, I]
             lib.oracle_bwd_keys.argtypes = [P, P, P, P, I64, I64, Dbl, P, P, I64, P, I64, P, P, I]
@@ -109,6 +114,23 @@ def stripe_positions(S: int, N: int) -> np.ndarray:
     out = np.empty(S, dtype=np.int64)
     _load().oracle_stripe_positions(S, N, _ptr(out))
     return out
+
+
+def zigzag_positions(S: int, N: int) -> np.ndarray:
+    """pos[row] for the zig-zag layout, built by enumerating the positions
+    whose chunk (of S/(2N)) is d or 2N-1-d."""
+    out = np.empty(S, dtype=np.int64)
+    _load().oracle_zigzag_positions(S, N, _ptr(out))
+    return out
+
+
+def layout_positions(S: int, N: int, layout: int) -> np.ndarray:
+    """pos[row] of any layout (enumeration for striped and zig-zag)."""
+    if layout == STRIPED:
+        return stripe_positions(S, N)
+    if layout == ZIGZAG:
+        return zigzag_positions(S, N)
+    return np.arange(S, dtype=np.int64)
 
 
 # --------------------------------------------------------------------------

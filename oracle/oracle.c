@@ -31,6 +31,11 @@
  *    stripe-major row d*L + i holds position i*N + d (L = S/N).  The
  *    contiguous (Ring Attention) placement gives device d positions
  *    [d*L, (d+1)*L) (§Summary, first paragraph).
+ *  - A third placement that the pages do not describe, kept for comparison
+ *    with the striped one: the zig-zag (load-balanced) placement cuts the
+ *    sequence into 2N chunks of C = S/(2N) positions and gives device d
+ *    chunk d followed by chunk 2N-1-d (one chunk from each end), so row
+ *    d*L + i holds d*C + i for i < C and (2N-1-d)*C + (i - C) otherwise.
  *  - Per-round work: in round r device d holds the key/value stripe of
  *    device e = (d - r) mod N (key/value blocks circulate around the ring,
  *    §Summary).  A Tq x Tk tile of (query, key) pairs of that round is
@@ -109,11 +114,17 @@ static double dot(const double *a, const double *b, int64_t D) {
 
 /* Global position held by row `row` of the layout.
  * layout 0 = striped: row d*L + i holds position i*N + d.
- * layout 1 = contiguous: row r holds position r.                           */
+ * layout 1 = contiguous: row r holds position r.
+ * layout 2 = zig-zag: row d*L + i holds d*C + i (i < C) or
+ *            (2N-1-d)*C + (i - C) (i >= C), C = S/(2N).                    */
 int64_t oracle_position_of_row(int64_t row, int64_t S, int N, int layout) {
     if (layout == 1) return row;
     int64_t L = S / N;
     int64_t d = row / L, i = row % L;
+    if (layout == 2) {
+        int64_t C = S / (2 * (int64_t)N);
+        return i < C ? d * C + i : (2 * (int64_t)N - 1 - d) * C + (i - C);
+    }
     return i * (int64_t)N + d;
 }
 
@@ -124,6 +135,18 @@ void oracle_stripe_positions(int64_t S, int N, int64_t *pos) {
     for (int d = 0; d < N; ++d)
         for (int64_t p = 0; p < S; ++p)
             if (p % N == d) pos[row++] = p;
+}
+
+/* Fill pos[row] for the zig-zag placement, by enumerating positions: device
+ * d collects, in increasing order, every position whose chunk index p / C
+ * is d or 2N-1-d (C = S/(2N), S divisible by 2N). */
+void oracle_zigzag_positions(int64_t S, int N, int64_t *pos) {
+    int64_t C = S / (2 * (int64_t)N), row = 0;
+    for (int d = 0; d < N; ++d)
+        for (int64_t p = 0; p < S; ++p) {
+            int64_t chunk = p / C;
+            if (chunk == d || chunk == 2 * (int64_t)N - 1 - d) pos[row++] = p;
+        }
 }
 
 /* ------------------------------------------------------------------------ */
@@ -352,7 +375,14 @@ void oracle_tile_counts_bruteforce(int64_t S, int N, int64_t Tq, int64_t Tk, int
  *              when e <= d and j < i when e > d, so for T >= 2 it is
  *              partial, and for T = 1 it is full (e <= d) or empty (e > d).
  *  contiguous: e < d: n^2 full; e == d: n(n-1)/2 full + n diagonal tiles
- *              (partial for T >= 2, full for T = 1); e > d: nothing.     */
+ *              (partial for T >= 2, full for T = 1); e > d: nothing.
+ *  zig-zag (T dividing C = S/(2N), c = C/T tiles per chunk): a query chunk
+ *              keeps a whole key chunk of lower index and the causal
+ *              triangle of its own.  e == d: chunks (d,d) and (2N-1-d,
+ *              2N-1-d) are triangles of c(c-1)/2 full + c diagonal tiles,
+ *              (2N-1-d, d) is c^2 full; e != d: exactly two chunk pairs
+ *              are kept in full (e < d: (d,e), (2N-1-d,e); e > d:
+ *              (2N-1-d,e), (2N-1-d,2N-1-e)), so 2c^2 full tiles.         */
 void oracle_tile_counts_closed(int64_t S, int N, int64_t T, int layout, int64_t *full,
                                int64_t *partial) {
     int64_t L = S / N, n = L / T;
@@ -361,7 +391,16 @@ void oracle_tile_counts_closed(int64_t S, int N, int64_t T, int layout, int64_t 
             int e = ((d - r) % N + N) % N;
             int64_t nf = 0, np = 0;
             int diag_kept_all = (T == 1);
-            if (layout == 0) {
+            if (layout == 2) {
+                int64_t c = (S / (2 * (int64_t)N)) / T;
+                if (e == d) {
+                    nf = c * (c - 1) + c * c;
+                    if (diag_kept_all) nf += 2 * c;
+                    else np = 2 * c;
+                } else {
+                    nf = 2 * c * c;
+                }
+            } else if (layout == 0) {
                 nf = n * (n - 1) / 2;
                 if (T >= 2) np = n;
                 else if (e <= d) nf += n;

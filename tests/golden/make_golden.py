@@ -1,8 +1,8 @@
 """Write tests/golden/tile_counts.json from the CPU oracle only.
 
 Per-round tile tables and modelled ring critical paths (sum over rounds of
-the busiest device's tile count) for the benchmark workloads, both
-placements.  Small workloads use the oracle's pair-by-pair brute force; the
+the busiest device's tile count) for the benchmark workloads, all three
+placements (striped, contiguous, zig-zag).  Small workloads use the oracle's pair-by-pair brute force; the
 large ones its closed forms (which the oracle tests pin to the brute force).
 Run:  python tests/golden/make_golden.py
 """
@@ -32,7 +32,8 @@ def main():
            "workloads": []}
     for name, S, N, T in WORKLOADS:
         entry = {"name": name, "S": S, "N": N, "T": T}
-        for lname, layout in (("striped", oracle.STRIPED), ("contiguous", oracle.CONTIGUOUS)):
+        for lname, layout in (("striped", oracle.STRIPED), ("contiguous", oracle.CONTIGUOUS),
+                              ("zigzag", oracle.ZIGZAG)):
             if S <= 8192:
                 full, part = oracle.tile_counts_bruteforce(S, N, T, T, layout)
             else:

@@ -15,7 +15,7 @@ import torch
 from scipy.special import logsumexp
 
 import oracle
-from oracle import CONTIGUOUS, STRIPED
+from oracle import CONTIGUOUS, STRIPED, ZIGZAG
 
 
 def _rand(S, D, seed, scale=1.0):
@@ -49,6 +49,27 @@ def test_stripe_positions_every_nth_token(oracle_lib, S, N):
 
 def test_stripe_positions_n1_is_identity(oracle_lib):
     assert np.array_equal(oracle.stripe_positions(40, 1), np.arange(40))
+
+
+@pytest.mark.parametrize("S,N", [(8, 1), (8, 2), (16, 4), (256, 4), (64, 8), (96, 16)])
+def test_zigzag_positions_one_chunk_from_each_end(oracle_lib, S, N):
+    """Device d holds chunk d, then chunk 2N-1-d, each ascending and whole
+    (chunks of S/(2N)); the map is a permutation and position_of_row agrees
+    with the enumeration."""
+    L, C = S // N, S // (2 * N)
+    pos = oracle.zigzag_positions(S, N)
+    assert sorted(pos.tolist()) == list(range(S))
+    for d in range(N):
+        dev = pos[d * L:(d + 1) * L]
+        assert dev[:C].tolist() == list(range(d * C, (d + 1) * C))
+        assert dev[C:].tolist() == list(range((2 * N - 1 - d) * C, (2 * N - d) * C))
+    for row in range(S):
+        assert oracle.position_of_row(row, S, N, ZIGZAG) == pos[row]
+    assert np.array_equal(oracle.layout_positions(S, N, ZIGZAG), pos)
+
+
+def test_zigzag_n1_is_identity(oracle_lib):
+    assert np.array_equal(oracle.zigzag_positions(40, 1), np.arange(40))
 
 
 # ---------------------------------------------------------------- forward
@@ -130,7 +151,7 @@ def test_selected_rows_match_all_rows(oracle_lib):
     assert np.array_equal(o2, o[rows]) and np.array_equal(lse2, lse[rows])
 
 
-@pytest.mark.parametrize("layout", [STRIPED, CONTIGUOUS])
+@pytest.mark.parametrize("layout", [STRIPED, CONTIGUOUS, ZIGZAG])
 def test_round_partials_merge_to_full(oracle_lib, layout):
     """Per-round partial results over each device's key set, merged with the
     log-sum-exp rule in ring order, reproduce full causal attention."""
@@ -246,6 +267,28 @@ def test_tile_counts_bruteforce_equals_closed_form(oracle_lib, S, N, T, layout):
     assert np.array_equal(bf[0], cf[0]) and np.array_equal(bf[1], cf[1])
 
 
+@pytest.mark.parametrize("S,N,T", [(16, 1, 4), (64, 4, 4), (256, 4, 16), (256, 4, 32), (96, 8, 3),
+                                   (128, 8, 1), (8192, 8, 128), (64, 2, 2), (1536, 12, 64)])
+def test_zigzag_bruteforce_equals_closed_form(oracle_lib, S, N, T):
+    bf = oracle.tile_counts_bruteforce(S, N, T, T, ZIGZAG)
+    cf = oracle.tile_counts_closed(S, N, T, ZIGZAG)
+    assert np.array_equal(bf[0], cf[0]) and np.array_equal(bf[1], cf[1])
+
+
+def test_zigzag_rounds_balanced_without_diagonals(oracle_lib):
+    """Zig-zag: after round 0 every device keeps exactly two whole chunk
+    pairs (2c^2 full tiles, no partial tile); round 0 is two causal chunk
+    triangles plus one whole chunk pair (2c^2 + c tiles, 2c of them
+    partial).  Its total equals the contiguous placement's."""
+    S, N, T = 8192, 8, 128
+    c = S // (2 * N) // T
+    full, part = oracle.tile_counts_bruteforce(S, N, T, T, ZIGZAG)
+    assert np.all(part[1:] == 0) and np.all(full[1:] == 2 * c * c)
+    assert np.all(full[0] + part[0] == 2 * c * c + c) and np.all(part[0] == 2 * c)
+    cf, cp = oracle.tile_counts_bruteforce(S, N, T, T, CONTIGUOUS)
+    assert full.sum() + part.sum() == cf.sum() + cp.sum()
+
+
 def test_striped_rounds_skip_about_half(oracle_lib):
     """Striped: every device does the same work in every round, about half
     of the n^2 tiles of the round (the balance claim)."""
@@ -301,10 +344,22 @@ def test_critical_path_values(oracle_lib):
     assert oracle.critical_path(*bf) == 58
 
 
+def test_zigzag_critical_path(oracle_lib):
+    """Zig-zag critical path 2N c^2 + c (c = S/(2N)/T): below the striped
+    N n(n+1)/2 = 2N c^2 + N c by the (N-1) c diagonal tiles striped adds."""
+    for S, N, T in [(256, 4, 16), (8192, 8, 128), (262144, 8, 128), (786432, 16, 128)]:
+        c = S // (2 * N) // T
+        cp_z = oracle.critical_path(*oracle.tile_counts_closed(S, N, T, ZIGZAG))
+        cp_s = oracle.critical_path(*oracle.tile_counts_closed(S, N, T, STRIPED))
+        assert cp_z == 2 * N * c * c + c
+        assert cp_s - cp_z == (N - 1) * c
+    assert oracle.critical_path(*oracle.tile_counts_bruteforce(256, 4, 16, 16, ZIGZAG)) == 2 * 4 * 4 + 2
+
+
 def test_kept_pairs_equal_causal_total(oracle_lib):
     """With T = 1 every kept pair is one full tile: the total over rounds and
     devices is S(S+1)/2 for both placements."""
     S, N = 96, 8
-    for layout in (STRIPED, CONTIGUOUS):
+    for layout in (STRIPED, CONTIGUOUS, ZIGZAG):
         full, part = oracle.tile_counts_bruteforce(S, N, 1, 1, layout)
         assert part.sum() == 0 and full.sum() == S * (S + 1) // 2
