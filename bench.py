@@ -167,6 +167,81 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def _time_rounds(sp, torch, q, k, v, o_acc, lse_acc, N, layout, B, H, S, D, steps=1):
+    """Time the per-round forward: for r = 0..N-1, every device d runs
+    ring_round_fwd against stripe (d - r) mod N (N*N launches per step)."""
+    def rounds():
+        for r in range(N):
+            for d in range(N):
+                sp.ring_round_fwd(q, k, v, o_acc, lse_acc, d, (d - r) % N, N, layout, first_round=(r == 0))
+
+    rounds()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        rounds()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"ms": ms, "tflops": _flops(B, H, S, D, 4) / (ms / 1000.0) / 1e12, "launches": N * N}
+
+
+def short_sequence_report(sp, torch, dev):
+    """Short-sequence regime (B=1, H=8, S=8192, D=128, N=8): batched
+    fwd+bwd per placement, batched and per-round forward, each step timed
+    alone with the L2 flushed (a 256 MB write) before it; medians of 20."""
+    from seeded_inputs import device_inputs
+
+    B, H, S, D, N = 1, 8, 8192, 128, 8
+    x = device_inputs(B, H, S, D, torch.bfloat16, seed=3, device=dev)
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    ws = sp.new_workspace(B, H, S, D, N, torch.bfloat16, dev)
+    o_acc = torch.empty(B, H, S, D, dtype=torch.float32, device=dev)
+    lse_acc = torch.empty(B, H, S, dtype=torch.float32, device=dev)
+
+    def timed(fn, reps=20):
+        fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    out = {"workload": {"B": B, "H": H, "S": S, "D": D, "N": N, "dtype": "bf16"},
+           "timing": "median of 20, L2 flushed before each", "T": 128}
+    for lname, layout in (("striped", sp.STRIPED), ("contiguous", sp.CONTIGUOUS), ("zigzag", sp.ZIGZAG)):
+        q, k, v, do = (sp.layout_permute(x[n], N, layout) for n in ("q", "k", "v", "do"))
+        o, lse = sp.striped_attn_fwd(q, k, v, N, layout)
+
+        def fwd():
+            sp.striped_attn_fwd(q, k, v, N, layout, out=o, lse_out=lse)
+
+        def fwd_bwd():
+            fwd()
+            sp.striped_attn_bwd(q, k, v, o, lse, do, N, layout, workspace=ws)
+
+        def rounds():
+            for r in range(N):
+                for d in range(N):
+                    sp.ring_round_fwd(q, k, v, o_acc, lse_acc, d, (d - r) % N, N, layout, first_round=(r == 0))
+
+        t_fb, t_f, t_r = timed(fwd_bwd), timed(fwd), timed(rounds)
+        out[lname] = {"fwd_bwd_ms": t_fb, "fwd_bwd_tflops": _flops(B, H, S, D, 14) / (t_fb / 1e3) / 1e12,
+                      "fwd_ms": t_f, "fwd_tflops": _flops(B, H, S, D, 4) / (t_f / 1e3) / 1e12,
+                      "per_round_fwd_ms": t_r, "per_round_launches": N * N,
+                      "critical_path_tiles": sp.critical_path(S, N, 128, 128, layout),
+                      "total_tiles": int(sum(t.sum() for t in sp.tile_counts(S, N, 128, 128, layout)))}
+    return out
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
 
@@ -203,12 +278,15 @@ def run_gpu(args, rank, world, local_rank):
     def step(record=False, layout=sp.STRIPED, src=None, dst=None):
         src = src if src is not None else x
         dst = dst if dst is not None else outs
-        if layout == sp.STRIPED:
+        if layout != sp.CONTIGUOUS:
             e_p0 = torch.cuda.Event(enable_timing=True) if record else None
             if record:
                 e_p0.record()
             for name, buf in (("q", qs), ("k", ks), ("v", vs), ("do", dos)):
-                sp.striped_permute(src[name], N, out=buf)
+                if layout == sp.STRIPED:
+                    sp.striped_permute(src[name], N, out=buf)
+                else:
+                    sp.layout_permute(src[name], N, layout, out=buf)
             q_, k_, v_, do_ = qs, ks, vs, dos
         else:
             q_, k_, v_, do_ = src["q"], src["k"], src["v"], src["do"]
@@ -223,6 +301,9 @@ def run_gpu(args, rank, world, local_rank):
         if layout == sp.STRIPED:
             for t, y in zip((o, dq, dk, dv), dst):
                 sp.striped_unpermute(t, N, out=y)
+        elif layout == sp.ZIGZAG:
+            for t, y in zip((o, dq, dk, dv), dst):
+                sp.layout_unpermute(t, N, layout, out=y)
         if record:
             e3 = torch.cuda.Event(enable_timing=True)
             e3.record()
@@ -268,21 +349,49 @@ def run_gpu(args, rank, world, local_rank):
     stats_np = stats.cpu().numpy() // args.steps  # counters of one step, all heads
     T = sp.kernel_tile(torch.bfloat16, D)
 
-    # contiguous layout (Ring Attention placement) for comparison, 1-2 steps
-    contig = None
+    # the other placements on the same inputs, for comparison: contiguous
+    # (Ring Attention) and zig-zag (load-balanced), 2 timed steps each
+    contig = zigzag = None
     if args.compare:
-        step(layout=sp.CONTIGUOUS)
-        torch.cuda.synchronize()
-        c0 = torch.cuda.Event(enable_timing=True)
-        c1 = torch.cuda.Event(enable_timing=True)
-        c0.record()
-        nc = 2
-        for _ in range(nc):
-            step(layout=sp.CONTIGUOUS)
-        c1.record()
-        torch.cuda.synchronize()
-        cms = c0.elapsed_time(c1) / nc
-        contig = {"ms_per_step": cms, "tflops": fl_step / (cms / 1000.0) / 1e12}
+        def layout_steps(layout, nc=2):
+            step(layout=layout)
+            torch.cuda.synchronize()
+            c0 = torch.cuda.Event(enable_timing=True)
+            c1 = torch.cuda.Event(enable_timing=True)
+            c0.record()
+            for _ in range(nc):
+                step(layout=layout)
+            c1.record()
+            torch.cuda.synchronize()
+            cms = c0.elapsed_time(c1) / nc
+            return {"ms_per_step": cms, "tflops": fl_step / (cms / 1000.0) / 1e12}
+
+        contig = layout_steps(sp.CONTIGUOUS)
+        zigzag = layout_steps(sp.ZIGZAG)
+
+    # per-round variant: N x N ring_round_fwd launches (one per device and
+    # ring round, merged into an fp32 (O, LSE) accumulator) against the
+    # batched forward of the same layout
+    per_round = None
+    if args.compare:
+        per_round = {}
+        o_acc = torch.empty(B, H, S, D, dtype=torch.float32, device=dev)
+        lse_acc = torch.empty(B, H, S, dtype=torch.float32, device=dev)
+        for lname, layout in (("striped", sp.STRIPED), ("zigzag", sp.ZIGZAG), ("contiguous", sp.CONTIGUOUS)):
+            if layout == sp.STRIPED:
+                q_, k_, v_ = (sp.striped_permute(x[n_], N, out=buf) for n_, buf in (("q", qs), ("k", ks), ("v", vs)))
+            elif layout == sp.ZIGZAG:
+                q_, k_, v_ = (sp.layout_permute(x[n_], N, layout, out=buf) for n_, buf in (("q", qs), ("k", ks),
+                                                                                        ("v", vs)))
+            else:
+                q_, k_, v_ = x["q"], x["k"], x["v"]
+            per_round[lname] = _time_rounds(sp, torch, q_, k_, v_, o_acc, lse_acc, N, layout, B, H, S, D)
+            sp.striped_attn_fwd(q_, k_, v_, N, layout, out=o, lse_out=lse)
+            torch.cuda.synchronize()
+            per_round[lname]["lse_matches_batched"] = bool((lse_acc - lse).abs().max().item() <= 1e-3)
+            per_round[lname]["o_matches_batched"] = bool(
+                (o_acc[:, :, ::97].to(torch.bfloat16).float() - o[:, :, ::97].float()).abs().max().item() <= 2e-2)
+        del o_acc, lse_acc
 
     # End to end through the C ABI with host buffers (pinned): every step
     # copies its Q, K, V, dO in from host memory and its O, dQ, dK, dV back
@@ -385,13 +494,20 @@ def run_gpu(args, rank, world, local_rank):
         "tile_counts": {"T": T, "per_step_all_heads_full": int(stats_np[0].sum()),
                         "per_step_all_heads_partial": int(stats_np[1].sum()),
                         "critical_path_striped": sp.critical_path(S, N, T, T, sp.STRIPED),
-                        "critical_path_contiguous": sp.critical_path(S, N, T, T, sp.CONTIGUOUS)},
+                        "critical_path_contiguous": sp.critical_path(S, N, T, T, sp.CONTIGUOUS),
+                        "critical_path_zigzag": sp.critical_path(S, N, T, T, sp.ZIGZAG)},
         "gpu_launches": 12 * args.steps,
         "device_error": err,
         "outputs_match": outs_ok,
     }
     if contig is not None:
         line["contiguous_layout"] = contig
+    if zigzag is not None:
+        line["zigzag_layout"] = zigzag
+    if per_round is not None:
+        line["per_round_fwd"] = per_round
+    if args.compare and args.short:
+        line["short_sequence"] = short_sequence_report(sp, torch, dev)
     if e2e is not None:
         line["e2e"] = e2e
     line["clocks"] = clk.summary()
@@ -413,6 +529,8 @@ def main():
                     help="causal-prefix length of the timed CPU-oracle sample (0 disables)")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-compare", dest="compare", action="store_false")
+    ap.add_argument("--no-short", dest="short", action="store_false",
+                    help="skip the short-sequence (S=8192) comparison")
     for key in ("B", "H", "S", "N"):
         ap.add_argument(f"--{key}", type=int, default=None, help="override the workload (profiling cases)")
     args = ap.parse_args()

@@ -23,6 +23,15 @@
  *      STRIPED_LAYOUT_STRIPED:    row d*L + i holds position i*N + d
  *      STRIPED_LAYOUT_CONTIGUOUS: row r holds position r (device d owns rows
  *                                 [d*L, (d+1)*L))
+ *      STRIPED_LAYOUT_ZIGZAG:     row d*L + i holds d*C + i for i < C and
+ *                                 (2N-1-d)*C + (i - C) for i >= C, C = S/(2N):
+ *                                 device d owns chunk d and chunk 2N-1-d of
+ *                                 2N equal chunks (not on the pages; the
+ *                                 usual load-balanced placement, kept for
+ *                                 comparison).  Attention calls need C to be
+ *                                 a multiple of the kernel tile
+ *                                 (striped_kernel_tile), else
+ *                                 STRIPED_ERR_UNSUPPORTED.
  *    with L = S / N.  LSE arrays are fp32 [B, H, S] in the same row order.
  *  - dtype: STRIPED_BF16 (bf16 storage, fp32 accumulation, tensor cores) or
  *    STRIPED_FP32 (fp32 storage and arithmetic on the CUDA cores).
@@ -67,6 +76,7 @@ extern "C" {
 /* row orders */
 #define STRIPED_LAYOUT_STRIPED 0
 #define STRIPED_LAYOUT_CONTIGUOUS 1
+#define STRIPED_LAYOUT_ZIGZAG 2
 
 /*
  * Stripe permutation (§Summary "every N-th token"; §Key points: applied once
@@ -83,13 +93,29 @@ int striped_unpermute(const void *x, void *y, int64_t B, int64_t H, int64_t S, i
                       int dtype, void *stream);
 
 /*
+ * The same permutation for any `layout`: y[b,h,row,:] = x[b,h,pos(row),:]
+ * with pos the layout's row -> position map (see the conventions above;
+ * STRIPED_LAYOUT_STRIPED is striped_permute, STRIPED_LAYOUT_CONTIGUOUS a
+ * plain copy).  STRIPED_LAYOUT_ZIGZAG requires S % (2N) == 0, else
+ * STRIPED_ERR_INVALID_ARG.  Same argument rules and bit-exact result as
+ * striped_permute.
+ */
+int striped_layout_permute(const void *x, void *y, int64_t B, int64_t H, int64_t S, int64_t D, int N,
+                           int layout, int dtype, void *stream);
+
+/* Inverse of striped_layout_permute: y[b,h,pos(row),:] = x[b,h,row,:]. */
+int striped_layout_unpermute(const void *x, void *y, int64_t B, int64_t H, int64_t S, int64_t D,
+                             int N, int layout, int dtype, void *stream);
+
+/*
  * Causal attention forward over all N ring rounds in one launch (§Summary:
  * each device attends to every circulating key/value stripe; exact result,
  * pith.science abstract).  For each query row of stripe d, rounds
  * r = 0..N-1 visit key stripe e = (d - r) mod N; a (query local i, key local
  * j) pair is kept iff the key's position <= the query's position, which in
- * the striped layout is  j < i  or  (j == i and e <= d),  and in the
- * contiguous layout is  e < d,  or  e == d and j <= i.  Fully masked tiles
+ * the striped layout is  j < i  or  (j == i and e <= d),  in the
+ * contiguous layout is  e < d,  or  e == d and j <= i,  and in the zig-zag
+ * layout follows the chunk positions above.  Fully masked tiles
  * are skipped; partial results of all rounds are merged by the online
  * softmax, so o = softmax(scale * q k^T + causal mask) v exactly up to
  * rounding, and lse = natural-log log-sum-exp of each row's kept scores.

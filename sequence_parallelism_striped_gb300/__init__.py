@@ -20,6 +20,7 @@ from . import build as _build
 
 STRIPED = 0
 CONTIGUOUS = 1
+ZIGZAG = 2
 BF16 = 0
 FP32 = 1
 
@@ -60,6 +61,8 @@ def load(build_if_missing: bool = True):
         P, I64, I, F, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.striped_permute.argtypes = [P, P, I64, I64, I64, I64, I, I, P]
         lib.striped_unpermute.argtypes = [P, P, I64, I64, I64, I64, I, I, P]
+        lib.striped_layout_permute.argtypes = [P, P, I64, I64, I64, I64, I, I, I, P]
+        lib.striped_layout_unpermute.argtypes = [P, P, I64, I64, I64, I64, I, I, I, P]
         lib.striped_attn_fwd.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I, I, I, F, P, P]
         lib.striped_workspace_size.argtypes = [I64, I64, I64, I64, I, I]
         lib.striped_workspace_size.restype = SZ
@@ -126,6 +129,24 @@ def striped_unpermute(x: torch.Tensor, N: int, out: torch.Tensor | None = None, 
     y = torch.empty_like(x) if out is None else out
     _check(load().striped_unpermute(_dev(x, "x"), _dev(y, "y"), B, H, S, D, N, _dtype_code(x),
                                     _stream(stream)), "striped_unpermute")
+    return y
+
+
+def layout_permute(x: torch.Tensor, N: int, layout: int, out: torch.Tensor | None = None, stream=None):
+    """Position order -> `layout` row order (striped, contiguous or zig-zag)."""
+    B, H, S, D = x.shape
+    y = torch.empty_like(x) if out is None else out
+    _check(load().striped_layout_permute(_dev(x, "x"), _dev(y, "y"), B, H, S, D, N, layout, _dtype_code(x),
+                                         _stream(stream)), "striped_layout_permute")
+    return y
+
+
+def layout_unpermute(x: torch.Tensor, N: int, layout: int, out: torch.Tensor | None = None, stream=None):
+    """Inverse of layout_permute."""
+    B, H, S, D = x.shape
+    y = torch.empty_like(x) if out is None else out
+    _check(load().striped_layout_unpermute(_dev(x, "x"), _dev(y, "y"), B, H, S, D, N, layout,
+                                           _dtype_code(x), _stream(stream)), "striped_layout_unpermute")
     return y
 
 

@@ -91,17 +91,29 @@ static int check_sizes(int64_t B, int64_t H, int64_t S, int64_t D, int N) {
     return STRIPED_OK;
 }
 
+static bool valid_layout(int layout) {
+    return layout == STRIPED_LAYOUT_STRIPED || layout == STRIPED_LAYOUT_CONTIGUOUS ||
+           layout == STRIPED_LAYOUT_ZIGZAG;
+}
+
 static int check_attn(int64_t B, int64_t H, int64_t S, int64_t D, int N, int layout, int dtype) {
     int st = check_sizes(B, H, S, D, N);
     if (st) return st;
-    if (layout != STRIPED_LAYOUT_STRIPED && layout != STRIPED_LAYOUT_CONTIGUOUS)
-        return STRIPED_ERR_INVALID_ARG;
+    if (!valid_layout(layout)) return STRIPED_ERR_INVALID_ARG;
+    int64_t tile;
     if (dtype == STRIPED_BF16) {
         if (D != 128) return STRIPED_ERR_UNSUPPORTED;
+        tile = kTcTile;
     } else if (dtype == STRIPED_FP32) {
         if (D % 8 != 0 || D > 128) return STRIPED_ERR_UNSUPPORTED;
+        tile = kSimtTile;
     } else {
         return STRIPED_ERR_INVALID_ARG;
+    }
+    if (layout == STRIPED_LAYOUT_ZIGZAG) {
+        // whole chunks of C = S/(2N) rows, each a whole number of tiles
+        if (S % (2 * (int64_t)N) != 0) return STRIPED_ERR_INVALID_ARG;
+        if ((S / (2 * (int64_t)N)) % tile != 0) return STRIPED_ERR_UNSUPPORTED;
     }
     return STRIPED_OK;
 }
@@ -190,10 +202,12 @@ int striped_kernel_tile(int dtype, int64_t D, int *Tq, int *Tk) {
 
 // ---------------------------------------------------------------- permutation
 static int permute_common(const void *x, void *y, int64_t B, int64_t H, int64_t S, int64_t D, int N,
-                          int dtype, void *stream, bool gather) {
+                          int layout, int dtype, void *stream, bool gather) {
     if (!x || !y) return STRIPED_ERR_INVALID_ARG;
     int st = check_sizes(B, H, S, D, N);
     if (st) return st;
+    if (!valid_layout(layout)) return STRIPED_ERR_INVALID_ARG;
+    if (layout == STRIPED_LAYOUT_ZIGZAG && S % (2 * (int64_t)N) != 0) return STRIPED_ERR_INVALID_ARG;
     int64_t esize;
     if (dtype == STRIPED_BF16) esize = 2;
     else if (dtype == STRIPED_FP32) esize = 4;
@@ -203,17 +217,27 @@ static int permute_common(const void *x, void *y, int64_t B, int64_t H, int64_t 
     const char *xb = (const char *)x, *yb = (const char *)y;
     const int64_t bytes = B * H * S * D * esize;
     if (xb < yb + bytes && yb < xb + bytes) return STRIPED_ERR_INVALID_ARG;  // overlap
-    return launch_stripe_permute(x, y, B * H, S, D * esize, N, gather, (cudaStream_t)stream);
+    return launch_stripe_permute(x, y, B * H, S, D * esize, N, layout, gather, (cudaStream_t)stream);
 }
 
 int striped_permute(const void *x, void *y, int64_t B, int64_t H, int64_t S, int64_t D, int N,
                     int dtype, void *stream) {
-    return permute_common(x, y, B, H, S, D, N, dtype, stream, true);
+    return permute_common(x, y, B, H, S, D, N, STRIPED_LAYOUT_STRIPED, dtype, stream, true);
 }
 
 int striped_unpermute(const void *x, void *y, int64_t B, int64_t H, int64_t S, int64_t D, int N,
                       int dtype, void *stream) {
-    return permute_common(x, y, B, H, S, D, N, dtype, stream, false);
+    return permute_common(x, y, B, H, S, D, N, STRIPED_LAYOUT_STRIPED, dtype, stream, false);
+}
+
+int striped_layout_permute(const void *x, void *y, int64_t B, int64_t H, int64_t S, int64_t D, int N,
+                           int layout, int dtype, void *stream) {
+    return permute_common(x, y, B, H, S, D, N, layout, dtype, stream, true);
+}
+
+int striped_layout_unpermute(const void *x, void *y, int64_t B, int64_t H, int64_t S, int64_t D,
+                             int N, int layout, int dtype, void *stream) {
+    return permute_common(x, y, B, H, S, D, N, layout, dtype, stream, false);
 }
 
 // ---------------------------------------------------------------- attention

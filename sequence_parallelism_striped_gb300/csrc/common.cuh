@@ -44,7 +44,11 @@ __device__ __forceinline__ void record_timeout(int *err) {
 // rows inside the tile).  Positions: striped row d*L+i holds i*N+d, so the
 // pair (i, j) is kept iff j*N+e <= i*N+d, i.e. j <= i - 1 + [e <= d];
 // contiguous rows hold their own position, so the pair is kept iff e < d, or
-// e == d and j <= i.  `rows_a` is the number of in-range rows of tile a
+// e == d and j <= i.  Zig-zag rows i < C hold d*C + i and rows i >= C hold
+// (2N-1-d)*C + i - C (C = L/2, a multiple of T, so with c = nk/2 tiles per
+// chunk, tiles a < c lie in chunk d and tiles a >= c in chunk 2N-1-d); a
+// query chunk keeps every key chunk of lower index in full and the causal
+// triangle of its own.  `rows_a` is the number of in-range rows of tile a
 // (T, or fewer for the last, ragged tile); key tiles have the same edge T.
 struct RoundSpan {
     int nfull;     // fully kept key tiles b = 0 .. nfull-1
@@ -55,6 +59,18 @@ struct RoundSpan {
 __host__ __device__ __forceinline__ RoundSpan round_span(int layout, int d, int e, int a, int nk,
                                                          int rows_a) {
     RoundSpan s{0, 0, 0};
+    if (layout == STRIPED_LAYOUT_ZIGZAG) {
+        const int c = nk / 2;
+        if (e == d) {  // own chunks: everything below the diagonal tile a
+            s.nfull = a;
+            s.has_diag = 1;
+        } else if (a < c) {  // query chunk d: key chunk e < d only
+            s.nfull = (e < d) ? c : 0;
+        } else {  // query chunk 2N-1-d: key chunk e always, 2N-1-e if e > d
+            s.nfull = (e > d) ? 2 * c : c;
+        }
+        return s;
+    }
     if (layout == STRIPED_LAYOUT_STRIPED) {
         const int off = (e <= d) ? 0 : -1;
         s.nfull = a;
@@ -93,6 +109,18 @@ struct QuerySpan {
 __host__ __device__ __forceinline__ QuerySpan query_span(int layout, int d, int e, int b, int nq,
                                                          int rows_b) {
     QuerySpan s{nq, 0, 0};
+    if (layout == STRIPED_LAYOUT_ZIGZAG) {
+        const int c = nq / 2;
+        if (e == d) {  // own chunks: the diagonal tile b and every tile after it
+            s.a_lo = b;
+            s.has_diag = 1;
+        } else if (b < c) {  // key chunk e: all of query chunk 2N-1-d, and chunk d if e < d
+            s.a_lo = (e < d) ? 0 : c;
+        } else {  // key chunk 2N-1-e: only query chunk 2N-1-d, and only if e > d
+            s.a_lo = (e > d) ? c : nq;
+        }
+        return s;
+    }
     if (layout == STRIPED_LAYOUT_STRIPED) {
         const int off = (e <= d) ? 0 : -1;
         if (rows_b >= 2) {

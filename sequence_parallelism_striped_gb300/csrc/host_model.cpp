@@ -9,8 +9,13 @@
 //   striped    (row d*L+i holds i*N+d):  j <= i + c,  c = [e <= d] - 1
 //   contiguous (row d*L+i holds d*L+i):  e < d: all;  e == d: j <= i;
 //                                        e > d: none.
+//   zig-zag (row d*L+i holds d*C+i for i < C, (2N-1-d)*C+i-C otherwise,
+//            C = S/(2N)): compare the positions directly.
 // For "j <= i + c" a tile has a kept pair iff j0 <= (i1 - 1) + c and all
-// pairs kept iff (j1 - 1) <= i0 + c, so each tile is classified in O(1).
+// pairs kept iff (j1 - 1) <= i0 + c; in general, since positions grow with
+// the row inside a device, a tile has a kept pair iff pos(j0) <= pos(i1-1)
+// and all pairs kept iff pos(j1-1) <= pos(i0).  Each tile is classified in
+// O(1).
 // Critical path: each round lasts as long as its busiest device (§Summary:
 // rounds run at the pace of the slowest device), summed over rounds.
 #include <stdint.h>
@@ -20,8 +25,20 @@
 
 namespace {
 
+// Zig-zag position of row i of device d (C = L / 2 positions per chunk).
+inline int64_t zigzag_pos(int64_t d, int64_t i, int64_t C, int N) {
+    return i < C ? d * C + i : (2 * (int64_t)N - 1 - d) * C + (i - C);
+}
+
 // class of one tile: 0 = skipped, 1 = full, 2 = partial
-inline int classify(int layout, int d, int e, int64_t i0, int64_t i1, int64_t j0, int64_t j1) {
+inline int classify(int layout, int N, int64_t L, int d, int e, int64_t i0, int64_t i1, int64_t j0,
+                    int64_t j1) {
+    if (layout == STRIPED_LAYOUT_ZIGZAG) {
+        const int64_t C = L / 2;
+        if (zigzag_pos(e, j0, C, N) > zigzag_pos(d, i1 - 1, C, N)) return 0;
+        if (zigzag_pos(e, j1 - 1, C, N) <= zigzag_pos(d, i0, C, N)) return 1;
+        return 2;
+    }
     int64_t c;
     if (layout == STRIPED_LAYOUT_STRIPED) {
         c = (e <= d) ? 0 : -1;
@@ -41,7 +58,9 @@ extern "C" {
 
 int striped_tile_counts(int64_t S, int N, int Tq, int Tk, int layout, int64_t *full, int64_t *partial) {
     if (S < 1 || N < 1 || Tq < 1 || Tk < 1 || S % N != 0) return STRIPED_ERR_INVALID_ARG;
-    if (layout != STRIPED_LAYOUT_STRIPED && layout != STRIPED_LAYOUT_CONTIGUOUS) return STRIPED_ERR_INVALID_ARG;
+    if (layout != STRIPED_LAYOUT_STRIPED && layout != STRIPED_LAYOUT_CONTIGUOUS && layout != STRIPED_LAYOUT_ZIGZAG)
+        return STRIPED_ERR_INVALID_ARG;
+    if (layout == STRIPED_LAYOUT_ZIGZAG && S % (2 * (int64_t)N) != 0) return STRIPED_ERR_INVALID_ARG;
     const int64_t L = S / N;
     for (int r = 0; r < N; ++r) {
         for (int d = 0; d < N; ++d) {
@@ -51,11 +70,10 @@ int striped_tile_counts(int64_t S, int N, int Tq, int Tk, int layout, int64_t *f
                 const int64_t i1 = (i0 + Tq < L) ? i0 + Tq : L;
                 for (int64_t j0 = 0; j0 < L; j0 += Tk) {
                     const int64_t j1 = (j0 + Tk < L) ? j0 + Tk : L;
-                    const int k = classify(layout, d, e, i0, i1, j0, j1);
+                    const int k = classify(layout, N, L, d, e, i0, i1, j0, j1);
                     if (k == 0) {
-                        // key tiles further right are masked too (j0 grows)
-                        if (layout == STRIPED_LAYOUT_STRIPED || e == d) break;
-                        continue;
+                        // key positions grow with j, so later key tiles are masked too
+                        break;
                     }
                     if (k == 1) ++nf;
                     else ++np;

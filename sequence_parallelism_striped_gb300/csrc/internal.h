@@ -35,7 +35,7 @@ struct AttnGeom {
 
 // ---- permute.cu
 int launch_stripe_permute(const void *x, void *y, int64_t BH, int64_t S, int64_t row_bytes, int N,
-                          bool gather, cudaStream_t stream);
+                          int layout, bool gather, cudaStream_t stream);
 
 // ---- attn_simt.cu (fp32 CUDA-core path, tile edge kSimtTile)
 constexpr int kSimtTile = 16;

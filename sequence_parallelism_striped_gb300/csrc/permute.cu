@@ -8,6 +8,10 @@
 //   permute   (gather):  y[d*L + i] = x[i*N + d]
 //   unpermute (scatter): y[i*N + d] = x[d*L + i]
 //
+// The same kernel serves the other row orders with their own row -> position
+// map: contiguous (position d*L + i, a copy) and zig-zag (device d holds
+// chunk d then chunk 2N-1-d of 2N chunks of C = L/2 positions).
+//
 // One block moves a run of consecutive stripe rows of one (b, h) head; the
 // stripe index d is uniform per block (no per-element division).  Each row
 // is D*esize bytes moved as 16-byte vectors; a thread issues all its loads
@@ -20,7 +24,18 @@ namespace striped {
 constexpr int kPermThreads = 256;
 constexpr int kPermVecPerThread = 8;  // 16-byte vectors per thread per block
 
-template <bool kGather>
+// Position of row i of device d under the placement kLayout.
+template <int kLayout>
+__device__ __forceinline__ int64_t position_of(int64_t d, int64_t i, int64_t L, int N) {
+    if (kLayout == STRIPED_LAYOUT_CONTIGUOUS) return d * L + i;
+    if (kLayout == STRIPED_LAYOUT_ZIGZAG) {
+        const int64_t C = L >> 1;
+        return i < C ? d * C + i : (2 * (int64_t)N - 1 - d) * C + (i - C);
+    }
+    return i * N + d;
+}
+
+template <int kLayout, bool kGather>
 __global__ void __launch_bounds__(kPermThreads) stripe_permute_kernel(
     const uint4 *__restrict__ x, uint4 *__restrict__ y, int64_t S, int64_t L, int N, int vec_per_row_log2,
     int rows_per_block, int blocks_per_stripe) {
@@ -42,7 +57,7 @@ __global__ void __launch_bounds__(kPermThreads) stripe_permute_kernel(
             const int c = v & (vpr - 1);
             if (i < L) {
                 const int64_t striped_row = head + (int64_t)d * L + i;
-                const int64_t pos_row = head + i * N + d;
+                const int64_t pos_row = head + position_of<kLayout>(d, i, L, N);
                 const int64_t src = (kGather ? pos_row : striped_row) * vpr + c;
                 dst_idx[u] = (kGather ? striped_row : pos_row) * vpr + c;
                 buf[u] = __ldg(x + src);
@@ -54,8 +69,19 @@ __global__ void __launch_bounds__(kPermThreads) stripe_permute_kernel(
         if (dst_idx[u] >= 0) y[dst_idx[u]] = buf[u];
 }
 
+template <int kLayout>
+static void launch_layout(dim3 grid, cudaStream_t stream, bool gather, const void *x, void *y, int64_t S,
+                          int64_t L, int N, int vlog, int rows_per_block, int bps) {
+    if (gather)
+        stripe_permute_kernel<kLayout, true><<<grid, kPermThreads, 0, stream>>>(
+            (const uint4 *)x, (uint4 *)y, S, L, N, vlog, rows_per_block, bps);
+    else
+        stripe_permute_kernel<kLayout, false><<<grid, kPermThreads, 0, stream>>>(
+            (const uint4 *)x, (uint4 *)y, S, L, N, vlog, rows_per_block, bps);
+}
+
 int launch_stripe_permute(const void *x, void *y, int64_t BH, int64_t S, int64_t row_bytes, int N,
-                          bool gather, cudaStream_t stream) {
+                          int layout, bool gather, cudaStream_t stream) {
     const int64_t L = S / N;
     const int64_t vpr = row_bytes / 16;
     int vlog = 0;
@@ -66,12 +92,13 @@ int launch_stripe_permute(const void *x, void *y, int64_t BH, int64_t S, int64_t
     const int64_t bps = (L + rows_per_block - 1) / rows_per_block;
     if (bps * N > 0x7fffffffll || BH > 65535) return STRIPED_ERR_UNSUPPORTED;
     dim3 grid((unsigned)(bps * N), (unsigned)BH);
-    if (gather)
-        stripe_permute_kernel<true><<<grid, kPermThreads, 0, stream>>>(
-            (const uint4 *)x, (uint4 *)y, S, L, N, vlog, rows_per_block, (int)bps);
+    if (layout == STRIPED_LAYOUT_ZIGZAG)
+        launch_layout<STRIPED_LAYOUT_ZIGZAG>(grid, stream, gather, x, y, S, L, N, vlog, rows_per_block, (int)bps);
+    else if (layout == STRIPED_LAYOUT_CONTIGUOUS)
+        launch_layout<STRIPED_LAYOUT_CONTIGUOUS>(grid, stream, gather, x, y, S, L, N, vlog, rows_per_block,
+                                                 (int)bps);
     else
-        stripe_permute_kernel<false><<<grid, kPermThreads, 0, stream>>>(
-            (const uint4 *)x, (uint4 *)y, S, L, N, vlog, rows_per_block, (int)bps);
+        launch_layout<STRIPED_LAYOUT_STRIPED>(grid, stream, gather, x, y, S, L, N, vlog, rows_per_block, (int)bps);
     return cuda_status(cudaGetLastError());
 }
 

@@ -12,9 +12,7 @@ TOL = {torch.float32: {"o": 1e-4, "lse": 1e-4, "grad": 1e-4},
 
 def positions(S, N, layout):
     """pos[row] = sequence position held by layout row (from the oracle)."""
-    if layout == sp.CONTIGUOUS:
-        return np.arange(S)
-    return oracle.stripe_positions(S, N)
+    return oracle.layout_positions(S, N, layout)
 
 
 def to_layout(x_cpu, N, layout, dev):
@@ -23,6 +21,8 @@ def to_layout(x_cpu, N, layout, dev):
     xd = x_cpu.to(dev).contiguous()
     if layout == sp.STRIPED:
         return sp.striped_permute(xd, N)
+    if layout == sp.ZIGZAG:
+        return sp.layout_permute(xd, N, sp.ZIGZAG)
     return xd
 
 

@@ -60,7 +60,21 @@ def test_bwd_bf16_small(B, H, S, D, N, layout):
     _check(x, grads, stats, B, H, S, D, N, layout, torch.bfloat16)
 
 
-@pytest.mark.parametrize("layout", [sp.STRIPED, sp.CONTIGUOUS])
+@pytest.mark.parametrize("B,H,S,D,N", [(1, 1, 256, 64, 4), (1, 2, 128, 32, 4), (2, 1, 256, 128, 8),
+                                       (1, 1, 512, 64, 16)])
+def test_bwd_fp32_zigzag(B, H, S, D, N):
+    x, grads, stats = _run(B, H, S, D, N, sp.ZIGZAG, torch.float32)
+    _check(x, grads, stats, B, H, S, D, N, sp.ZIGZAG, torch.float32)
+
+
+@pytest.mark.parametrize("B,H,S,D,N", [(1, 2, 1024, 128, 4), (2, 1, 2048, 128, 4), (1, 1, 512, 128, 1),
+                                       (1, 1, 4096, 128, 16)])
+def test_bwd_bf16_zigzag(B, H, S, D, N):
+    x, grads, stats = _run(B, H, S, D, N, sp.ZIGZAG, torch.bfloat16, seed=1)
+    _check(x, grads, stats, B, H, S, D, N, sp.ZIGZAG, torch.bfloat16)
+
+
+@pytest.mark.parametrize("layout", [sp.STRIPED, sp.CONTIGUOUS, sp.ZIGZAG])
 def test_bwd_bf16_short_sequence_full(layout):
     """Short-sequence workload B=1, H=8, S=8192, D=128, N=8: every row."""
     B, H, S, D, N = 1, 8, 8192, 128, 8

@@ -72,6 +72,32 @@ def test_fwd_bf16_short_sequence_full(layout):
     _check_fwd(x, o, lse, stats, B, H, S, D, N, layout, torch.bfloat16)
 
 
+@pytest.mark.parametrize("B,H,S,D,N", [(1, 1, 256, 64, 4), (1, 2, 128, 32, 4), (2, 1, 256, 128, 8),
+                                       (1, 1, 64, 64, 1), (1, 1, 512, 64, 16)])
+def test_fwd_fp32_zigzag(B, H, S, D, N):
+    x, o, lse, stats = _run_fwd(B, H, S, D, N, sp.ZIGZAG, torch.float32)
+    _check_fwd(x, o, lse, stats, B, H, S, D, N, sp.ZIGZAG, torch.float32)
+
+
+@pytest.mark.parametrize("B,H,S,D,N", [(1, 2, 1024, 128, 4),   # one tile per chunk
+                                       (2, 1, 2048, 128, 4),   # two tiles per chunk
+                                       (1, 1, 512, 128, 1),    # N=1: plain causal attention
+                                       (1, 1, 4096, 128, 16)])
+def test_fwd_bf16_zigzag(B, H, S, D, N):
+    x, o, lse, stats = _run_fwd(B, H, S, D, N, sp.ZIGZAG, torch.bfloat16, seed=1)
+    _check_fwd(x, o, lse, stats, B, H, S, D, N, sp.ZIGZAG, torch.bfloat16)
+
+
+def test_fwd_bf16_zigzag_short_sequence_full():
+    """Short-sequence workload B=1, H=8, S=8192, D=128, N=8, zig-zag
+    placement: every row, and the per-round counters (no partial tile after
+    round 0)."""
+    B, H, S, D, N = 1, 8, 8192, 128, 8
+    x, o, lse, stats = _run_fwd(B, H, S, D, N, sp.ZIGZAG, torch.bfloat16)
+    _check_fwd(x, o, lse, stats, B, H, S, D, N, sp.ZIGZAG, torch.bfloat16)
+    assert int(stats[1, 1:].sum()) == 0
+
+
 def test_striped_equals_contiguous_after_unpermute():
     """Permutation equivariance on the GPU path itself: striped output mapped
     back to positions equals the contiguous-layout output."""

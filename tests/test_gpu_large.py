@@ -144,3 +144,43 @@ def test_mid_contiguous_and_per_round_sampled():
     assert float((dv.double().sum(2) - do.double().sum(2)).abs().max()) <= \
         np.sqrt(S) * 2.0 ** -9 * float(dv.abs().max()) + 2e-2
     assert float(dk.double().sum(2).abs().max()) <= np.sqrt(S) * 2.0 ** -9 * float(dk.abs().max()) + 2e-2
+
+
+def test_mid_zigzag_sampled():
+    """Mid workload (B=1, H=24, S=65536, N=8) in the zig-zag placement
+    (permuted on the GPU): batched forward and backward on 2048 sampled
+    query rows, per-round counters against the oracle's closed form, and
+    the gradient invariants on every head."""
+    B, H, S, D, N = WORKLOADS["mid"]
+    scale = 1.0 / D ** 0.5
+    x = attention_inputs(B, H, S, D, torch.bfloat16, seed=2)
+    q, k, v, do = (sp.layout_permute(x[n].to(DEV), N, sp.ZIGZAG) for n in ("q", "k", "v", "do"))
+    stats = sp.new_tile_stats(N, DEV)
+    o, lse = sp.striped_attn_fwd(q, k, v, N, sp.ZIGZAG, tile_stats=stats)
+    dq, dk, dv = sp.striped_attn_bwd(q, k, v, o, lse, do, N, sp.ZIGZAG)
+    torch.cuda.synchronize()
+    assert sp.check_error() == 0
+    full, part = oracle.tile_counts_closed(S, N, 128, oracle.ZIGZAG)
+    st = stats.cpu().numpy()
+    assert np.array_equal(st[0], B * H * full) and np.array_equal(st[1], B * H * part)
+    rows = sample_rows(2048, B, H, S, seed=2).numpy()
+    inv = np.empty(S, dtype=np.int64)
+    inv[oracle.zigzag_positions(S, N)] = np.arange(S)  # position -> zig-zag row
+    bidx, hidx = torch.as_tensor(rows[:, 0], device=DEV), torch.as_tensor(rows[:, 1], device=DEV)
+    zidx = torch.as_tensor(inv[rows[:, 2]], device=DEV)
+    got = {"o": o[bidx, hidx, zidx].double().cpu().numpy(), "lse": lse[bidx, hidx, zidx].double().cpu().numpy(),
+           "dq": dq[bidx, hidx, zidx].double().cpu().numpy()}
+    worst = dict.fromkeys(got, 0.0)
+    for (b, h) in sorted({(int(r[0]), int(r[1])) for r in rows}):
+        sel = np.nonzero((rows[:, 0] == b) & (rows[:, 1] == h))[0]
+        pos = rows[sel, 2]
+        args = [x[n][b, h].double().numpy() for n in ("q", "k", "v", "do")]
+        o_ref, lse_ref = oracle.attn_fwd(args[0], args[1], args[2], scale, rows=pos)
+        _, _, dq_ref = oracle.bwd_rows(*args, scale, rows=pos)
+        for key, ref in (("o", o_ref), ("lse", lse_ref), ("dq", dq_ref)):
+            worst[key] = max(worst[key], float(np.abs(got[key][sel] - ref).max()))
+    print("mid zig-zag max errors", worst)
+    assert worst["o"] <= 2e-2 and worst["dq"] <= 2e-2 and worst["lse"] <= 1e-3
+    assert float((dv.double().sum(2) - do.double().sum(2)).abs().max()) <= \
+        np.sqrt(S) * 2.0 ** -9 * float(dv.abs().max()) + 2e-2
+    assert float(dk.double().sum(2).abs().max()) <= np.sqrt(S) * 2.0 ** -9 * float(dk.abs().max()) + 2e-2

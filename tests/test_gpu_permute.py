@@ -1,8 +1,10 @@
 """Stripe permutation on the GPU: bit-exact against the placement the oracle
-builds by enumeration ("every N-th token"), and round trip."""
+builds by enumeration ("every N-th token"; for the zig-zag placement, chunks
+d and 2N-1-d), and round trip."""
 import pytest
 import torch
 
+import oracle
 import sequence_parallelism_striped_gb300 as sp
 from tests._util import positions
 
@@ -41,3 +43,35 @@ def test_permute_full_size_long_context():
     want = x[0, heads.to(dev), (i * N + d).to(dev)]
     assert torch.equal(got, want)
     assert torch.equal(sp.striped_unpermute(y, N), x)
+
+
+@pytest.mark.parametrize("layout", [sp.ZIGZAG, sp.CONTIGUOUS, sp.STRIPED])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("B,H,S,D,N", [(1, 1, 256, 64, 4), (2, 3, 1200, 128, 4), (1, 8, 8192, 128, 8),
+                                       (1, 2, 4096, 64, 16), (1, 1, 48, 128, 8), (1, 2, 384, 128, 1),
+                                       (1, 1, 96, 32, 48)])
+def test_layout_permute_bit_exact(B, H, S, D, N, dtype, layout):
+    dev = torch.device("cuda")
+    g = torch.Generator(device="cpu").manual_seed(321)
+    x = torch.randn(B, H, S, D, generator=g).to(dtype)
+    pos = torch.as_tensor(positions(S, N, layout))
+    y = sp.layout_permute(x.to(dev), N, layout)
+    assert torch.equal(y.cpu(), x[:, :, pos])
+    assert torch.equal(sp.layout_unpermute(y, N, layout).cpu(), x)
+
+
+def test_zigzag_permute_full_size_long_context():
+    """Zig-zag placement of the largest benchmark tensor (B=1, H=32,
+    S=262144, D=128, bf16, N=8): sampled rows bit-exact, round trip exact."""
+    dev = torch.device("cuda")
+    B, H, S, D, N = 1, 32, 262144, 128, 8
+    g = torch.Generator(device=dev).manual_seed(6)
+    x = torch.randn(B, H, S, D, generator=g, device=dev).to(torch.bfloat16)
+    y = sp.layout_permute(x, N, sp.ZIGZAG)
+    rows = torch.randint(0, S, (4096,), generator=torch.Generator().manual_seed(11))
+    heads = torch.randint(0, H, (4096,), generator=torch.Generator().manual_seed(12))
+    pos = torch.as_tensor([int(oracle.position_of_row(int(r), S, N, oracle.ZIGZAG)) for r in rows])
+    got = y[0, heads.to(dev), rows.to(dev)]
+    want = x[0, heads.to(dev), pos.to(dev)]
+    assert torch.equal(got, want)
+    assert torch.equal(sp.layout_unpermute(y, N, sp.ZIGZAG), x)

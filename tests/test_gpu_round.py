@@ -18,6 +18,17 @@ DEV = torch.device("cuda")
                                              (torch.bfloat16, 1, 4, 8192, 128, 8)])
 @pytest.mark.parametrize("layout", [sp.STRIPED, sp.CONTIGUOUS])
 def test_rounds_merge_to_full_attention(dtype, B, H, S, D, N, layout):
+    _rounds_merge(dtype, B, H, S, D, N, layout)
+
+
+@pytest.mark.parametrize("dtype,B,H,S,D,N", [(torch.float32, 1, 1, 256, 64, 4),
+                                             (torch.bfloat16, 1, 2, 2048, 128, 4),
+                                             (torch.bfloat16, 1, 4, 8192, 128, 8)])
+def test_zigzag_rounds_merge_to_full_attention(dtype, B, H, S, D, N):
+    _rounds_merge(dtype, B, H, S, D, N, sp.ZIGZAG)
+
+
+def _rounds_merge(dtype, B, H, S, D, N, layout):
     x = inputs(B, H, S, D, dtype, seed=2, with_do=False)
     q, k, v = (to_layout(x[n], N, layout, DEV) for n in ("q", "k", "v"))
     o_acc = torch.empty(B, H, S, D, dtype=torch.float32, device=DEV)

@@ -46,11 +46,23 @@ def test_tile_counts_match_oracle_bruteforce(lib, S, N, Tq, Tk, layout):
     assert sp.critical_path(S, N, Tq, Tk, layout) == oracle.critical_path(bf, bp)
 
 
+@pytest.mark.parametrize("S,N,Tq,Tk", [(256, 4, 16, 16), (1024, 4, 128, 128), (1200, 4, 128, 128),
+                                       (96, 8, 3, 3), (90, 3, 4, 7), (48, 8, 1, 1), (8192, 8, 128, 128),
+                                       (64, 1, 16, 16), (8, 4, 128, 128), (1536, 12, 64, 32)])
+def test_zigzag_tile_counts_match_oracle_bruteforce(lib, S, N, Tq, Tk):
+    """Zig-zag placement, including tiles that straddle the chunk boundary
+    (C not a multiple of T) and Tq != Tk."""
+    full, part = sp.tile_counts(S, N, Tq, Tk, sp.ZIGZAG)
+    bf, bp = oracle.tile_counts_bruteforce(S, N, Tq, Tk, oracle.ZIGZAG)
+    assert np.array_equal(full, bf) and np.array_equal(part, bp)
+    assert sp.critical_path(S, N, Tq, Tk, sp.ZIGZAG) == oracle.critical_path(bf, bp)
+
+
 def test_golden_tables(lib):
     gold = json.load(open(os.path.join(ROOT, "tests", "golden", "tile_counts.json")))
     for w in gold["workloads"]:
         S, N, T = w["S"], w["N"], w["T"]
-        for name, layout in (("striped", sp.STRIPED), ("contiguous", sp.CONTIGUOUS)):
+        for name, layout in (("striped", sp.STRIPED), ("contiguous", sp.CONTIGUOUS), ("zigzag", sp.ZIGZAG)):
             full, part = sp.tile_counts(S, N, T, T, layout)
             assert full.tolist() == w[name]["full"], (w["name"], name)
             assert part.tolist() == w[name]["partial"], (w["name"], name)
@@ -92,6 +104,13 @@ def test_invalid_arguments_rejected_on_host(lib):
                               1.0, 1, None, None) == -1
     assert lib.striped_tile_counts(65, 4, 16, 16, 0, None, None) == -1
     assert lib.striped_critical_path(64, 0, 16, 16, 0) < 0
+    # zig-zag: S must split into 2N chunks; chunks must be whole kernel tiles
+    assert lib.striped_attn_fwd(fake, fake, fake, fake, fake, 1, 1, 1028, 128, 4, 2, 0, 1.0, None, None) == -1
+    assert lib.striped_attn_fwd(fake, fake, fake, fake, fake, 1, 1, 1200, 128, 4, 2, 0, 1.0, None, None) == -2
+    assert lib.striped_attn_fwd(fake, fake, fake, fake, fake, 1, 1, 200, 64, 4, 2, 1, 1.0, None, None) == -2
+    assert lib.striped_layout_permute(fake, P(1 << 24), 1, 1, 12, 128, 4, 2, 0, None) == -1
+    assert lib.striped_layout_permute(fake, P(1 << 24), 1, 1, 16, 128, 4, 3, 0, None) == -1
+    assert lib.striped_tile_counts(36, 4, 16, 16, 2, None, None) == -1
 
 
 def test_workspace_size(lib):
