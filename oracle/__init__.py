@@ -20,7 +20,10 @@ Causal Transformers"):
   first paragraph; per-round balance -- §Key points "Imbalance";
 * the zig-zag placement (2N chunks, device d holds chunks d and 2N-1-d) is
   not on the pages: it is the usual load-balanced alternative, defined in
-  ``oracle.c`` and compared against the striped placement.
+  ``oracle.c`` and compared against the striped placement;
+* grouped-query attention (query head h reads key/value head h // G) is not
+  on the pages either: ``attn_fwd_gqa`` / ``attn_bwd_gqa`` compose the
+  per-head definition, summing the gradients of a shared key/value head.
 
 Pins: every function here is checked in ``tests/test_oracle.py`` against
 things other than itself (closed forms, special cases, library routines,
@@ -224,6 +227,37 @@ def critical_path(full: np.ndarray, partial: np.ndarray) -> int:
     f = np.ascontiguousarray(full, dtype=np.int64)
     p = np.ascontiguousarray(partial, dtype=np.int64)
     return int(_load().oracle_critical_path(_ptr(f), _ptr(p), f.shape[0]))
+
+
+# --------------------------------------------------------------------------
+# grouped-query attention (not on the pages): H query heads share Hkv
+# key/value heads, query head h reading key/value head h // (H / Hkv)
+# --------------------------------------------------------------------------
+def attn_fwd_gqa(q, k, v, scale: float, nthreads: int | None = None):
+    """q [H, S, D], k and v [Hkv, S, D] (one batch entry) -> (O [H, S, D],
+    LSE [H, S]): each query head is plain causal attention against its
+    group's key/value head."""
+    H, Hkv = q.shape[0], k.shape[0]
+    G = H // Hkv
+    outs = [attn_fwd(q[h], k[h // G], v[h // G], scale, nthreads=nthreads) for h in range(H)]
+    return np.stack([o for o, _ in outs]), np.stack([l for _, l in outs])
+
+
+def attn_bwd_gqa(q, k, v, dO, scale: float, nthreads: int | None = None):
+    """Gradients of attn_fwd_gqa: dQ per query head; dK and dV of a shared
+    key/value head are the sums of the gradients of every query head that
+    reads it (the head is used G times)."""
+    H, Hkv = q.shape[0], k.shape[0]
+    G = H // Hkv
+    dq = np.empty_like(np.asarray(q, dtype=np.float64))
+    dk = np.zeros(np.shape(k), dtype=np.float64)
+    dv = np.zeros(np.shape(v), dtype=np.float64)
+    for h in range(H):
+        gq, gk, gv = attn_bwd(q[h], k[h // G], v[h // G], dO[h], scale, nthreads=nthreads)
+        dq[h] = gq
+        dk[h // G] += gk
+        dv[h // G] += gv
+    return dq, dk, dv
 
 
 def merge_rounds(o_a, lse_a, o_b, lse_b):

@@ -363,3 +363,30 @@ def test_kept_pairs_equal_causal_total(oracle_lib):
     for layout in (STRIPED, CONTIGUOUS, ZIGZAG):
         full, part = oracle.tile_counts_bruteforce(S, N, 1, 1, layout)
         assert part.sum() == 0 and full.sum() == S * (S + 1) // 2
+
+
+# ---------------------------------------------------------------- grouped-query attention
+@pytest.mark.parametrize("H,Hkv", [(2, 2), (4, 2), (4, 1), (6, 2)])
+def test_gqa_matches_torch_autograd_with_repeated_kv(oracle_lib, H, Hkv):
+    """torch's fp64 causal SDPA on K/V repeated to every query head of its
+    group (repeat_interleave), differentiated by autograd: the gradient of a
+    shared head is what autograd accumulates through the repeat."""
+    S, D = 24, 8
+    rng = np.random.default_rng(40 + H + Hkv)
+    q = rng.standard_normal((H, S, D))
+    k = rng.standard_normal((Hkv, S, D))
+    v = rng.standard_normal((Hkv, S, D))
+    do = rng.standard_normal((H, S, D))
+    scale = 0.4
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    G = H // Hkv
+    o = torch.nn.functional.scaled_dot_product_attention(
+        tq[None], tk.repeat_interleave(G, dim=0)[None], tv.repeat_interleave(G, dim=0)[None],
+        is_causal=True, scale=scale)[0]
+    o.backward(torch.tensor(do))
+    o_ref, _ = oracle.attn_fwd_gqa(q, k, v, scale)
+    assert np.allclose(o_ref, o.detach().numpy(), atol=1e-12)
+    dq, dk, dv = oracle.attn_bwd_gqa(q, k, v, do, scale)
+    assert np.allclose(dq, tq.grad.numpy(), atol=1e-11)
+    assert np.allclose(dk, tk.grad.numpy(), atol=1e-11)
+    assert np.allclose(dv, tv.grad.numpy(), atol=1e-11)
