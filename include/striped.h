@@ -127,6 +127,19 @@ int striped_attn_fwd(const void *q, const void *k, const void *v, void *o, float
                      int64_t H, int64_t S, int64_t D, int N, int layout, int dtype, float scale,
                      int64_t *tile_stats, void *stream);
 
+/*
+ * Grouped-query attention form of striped_attn_fwd (not on the pages; for
+ * models whose H query heads share Hkv key/value heads).  q, o: [B,H,S,D];
+ * k, v: [B,Hkv,S,D]; lse: [B,H,S].  Query head h of batch entry b attends
+ * with key/value head h / (H/Hkv) of the same entry (consecutive query heads
+ * share one).  Requires 1 <= Hkv, H % Hkv == 0 (else STRIPED_ERR_INVALID_ARG).
+ * Everything else as striped_attn_fwd, which is this call with Hkv = H.
+ * tile_stats counts per query head (sums over all B*H).
+ */
+int striped_attn_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                         int64_t H, int64_t Hkv, int64_t S, int64_t D, int N, int layout, int dtype,
+                         float scale, int64_t *tile_stats, void *stream);
+
 /* Bytes of device workspace striped_attn_bwd needs for these sizes (fp32 dQ
  * accumulator and per-row softmax statistics padded to whole tiles), or 0
  * for invalid sizes. */
@@ -147,6 +160,18 @@ int striped_attn_bwd(const void *q, const void *k, const void *v, const void *o,
                      const void *dO, void *dq, void *dk, void *dv, void *workspace,
                      size_t ws_bytes, int64_t B, int64_t H, int64_t S, int64_t D, int N,
                      int layout, int dtype, float scale, int64_t *tile_stats, void *stream);
+
+/*
+ * Backward of striped_attn_fwd_gqa.  q, o, dO, dq: [B,H,S,D]; k, v, dk, dv:
+ * [B,Hkv,S,D].  dk and dv of a key/value head are the sums over the H/Hkv
+ * query heads that read it (accumulated on chip, no atomics); the workspace
+ * is striped_workspace_size(B, H, S, D, N, dtype) (dQ is per query head).
+ * striped_attn_bwd is this call with Hkv = H.
+ */
+int striped_attn_bwd_gqa(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                         const void *dO, void *dq, void *dk, void *dv, void *workspace,
+                         size_t ws_bytes, int64_t B, int64_t H, int64_t Hkv, int64_t S, int64_t D, int N,
+                         int layout, int dtype, float scale, int64_t *tile_stats, void *stream);
 
 /*
  * striped_attn_bwd for callers that cannot allocate device memory (the paper

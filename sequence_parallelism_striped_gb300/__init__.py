@@ -64,10 +64,13 @@ def load(build_if_missing: bool = True):
         lib.striped_layout_permute.argtypes = [P, P, I64, I64, I64, I64, I, I, I, P]
         lib.striped_layout_unpermute.argtypes = [P, P, I64, I64, I64, I64, I, I, I, P]
         lib.striped_attn_fwd.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I, I, I, F, P, P]
+        lib.striped_attn_fwd_gqa.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I, I, I, F, P, P]
         lib.striped_workspace_size.argtypes = [I64, I64, I64, I64, I, I]
         lib.striped_workspace_size.restype = SZ
         lib.striped_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, I64, I64, I64, I64, I, I, I, F,
                                          P, P]
+        lib.striped_attn_bwd_gqa.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, I64, I64, I64, I64, I64, I, I, I,
+                                             F, P, P]
         lib.ring_round_fwd.argtypes = [P, P, P, P, P, P, I, I, I64, I64, I64, I64, I, I64, I64, I, I, F, I,
                                        P, P]
         lib.striped_kernel_tile.argtypes = [I, I64, P, P]
@@ -165,7 +168,10 @@ def new_tile_stats(N: int, device) -> torch.Tensor:
 
 def striped_attn_fwd(q, k, v, N: int, layout: int = STRIPED, scale: float | None = None,
                      tile_stats: torch.Tensor | None = None, out=None, lse_out=None, stream=None):
-    """Causal attention of all N ring rounds; returns (o, lse)."""
+    """Causal attention of all N ring rounds; returns (o, lse).  k and v may
+    have fewer heads than q (grouped-query attention, striped_attn_fwd_gqa)."""
+    if k.shape[1] != q.shape[1]:
+        return striped_attn_fwd_gqa(q, k, v, N, layout, scale, tile_stats, out, lse_out, stream)
     B, H, S, D = q.shape
     if scale is None:
         scale = 1.0 / D ** 0.5
@@ -174,6 +180,23 @@ def striped_attn_fwd(q, k, v, N: int, layout: int = STRIPED, scale: float | None
     _check(load().striped_attn_fwd(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(o, "o"), _dev(lse, "lse"),
                                    B, H, S, D, N, layout, _dtype_code(q), float(scale),
                                    _ptr_or_null(tile_stats), _stream(stream)), "striped_attn_fwd")
+    return o, lse
+
+
+def striped_attn_fwd_gqa(q, k, v, N: int, layout: int = STRIPED, scale: float | None = None,
+                         tile_stats: torch.Tensor | None = None, out=None, lse_out=None, stream=None):
+    """Grouped-query form: q [B,H,S,D], k and v [B,Hkv,S,D] (H % Hkv == 0);
+    query head h reads key/value head h // (H/Hkv).  Returns (o, lse)."""
+    B, H, S, D = q.shape
+    Hkv = k.shape[1]
+    if scale is None:
+        scale = 1.0 / D ** 0.5
+    o = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse_out is None else lse_out
+    _check(load().striped_attn_fwd_gqa(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(o, "o"),
+                                       _dev(lse, "lse"), B, H, Hkv, S, D, N, layout, _dtype_code(q),
+                                       float(scale), _ptr_or_null(tile_stats), _stream(stream)),
+           "striped_attn_fwd_gqa")
     return o, lse
 
 
@@ -190,20 +213,28 @@ def new_workspace(B, H, S, D, N, dtype, device) -> torch.Tensor:
 def striped_attn_bwd(q, k, v, o, lse, dO, N: int, layout: int = STRIPED, scale: float | None = None,
                      workspace: torch.Tensor | None = None, tile_stats: torch.Tensor | None = None,
                      dq=None, dk=None, dv=None, stream=None):
-    """Backward of striped_attn_fwd; returns (dq, dk, dv)."""
+    """Backward of striped_attn_fwd; returns (dq, dk, dv).  k and v may have
+    fewer heads than q (grouped-query attention, striped_attn_bwd_gqa)."""
     B, H, S, D = q.shape
+    Hkv = k.shape[1]
     if scale is None:
         scale = 1.0 / D ** 0.5
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     ws = new_workspace(B, H, S, D, N, q.dtype, q.device) if workspace is None else workspace
-    _check(load().striped_attn_bwd(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(o, "o"), _dev(lse, "lse"),
-                                   _dev(dO, "dO"), _dev(dq, "dq"), _dev(dk, "dk"), _dev(dv, "dv"),
-                                   _dev(ws, "workspace"), ws.numel() * ws.element_size(), B, H, S, D, N,
-                                   layout, _dtype_code(q), float(scale), _ptr_or_null(tile_stats),
-                                   _stream(stream)), "striped_attn_bwd")
+    args = [_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(o, "o"), _dev(lse, "lse"), _dev(dO, "dO"),
+            _dev(dq, "dq"), _dev(dk, "dk"), _dev(dv, "dv"), _dev(ws, "workspace"),
+            ws.numel() * ws.element_size()]
+    tail = [S, D, N, layout, _dtype_code(q), float(scale), _ptr_or_null(tile_stats), _stream(stream)]
+    if Hkv != H:
+        _check(load().striped_attn_bwd_gqa(*args, B, H, Hkv, *tail), "striped_attn_bwd_gqa")
+    else:
+        _check(load().striped_attn_bwd(*args, B, H, *tail), "striped_attn_bwd")
     return dq, dk, dv
+
+
+striped_attn_bwd_gqa = striped_attn_bwd  # same call; k, v (and dk, dv) carry Hkv heads
 
 
 def ring_round_fwd(q, k, v, o_acc, lse_acc, d: int, e: int, N: int, layout: int = STRIPED,

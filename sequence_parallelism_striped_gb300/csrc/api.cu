@@ -118,9 +118,11 @@ static int check_attn(int64_t B, int64_t H, int64_t S, int64_t D, int N, int lay
     return STRIPED_OK;
 }
 
-static AttnGeom full_geom(int64_t B, int64_t H, int64_t S, int64_t D, int N, int layout, float scale) {
+static AttnGeom full_geom(int64_t B, int64_t H, int64_t Hkv, int64_t S, int64_t D, int N, int layout,
+                          float scale) {
     AttnGeom g;
     g.BH = B * H;
+    g.G = H / Hkv;
     g.L = S / N;
     g.D = D;
     g.N = N;
@@ -241,14 +243,25 @@ int striped_layout_unpermute(const void *x, void *y, int64_t B, int64_t H, int64
 }
 
 // ---------------------------------------------------------------- attention
+static int check_heads(int64_t H, int64_t Hkv) {
+    return (Hkv >= 1 && Hkv <= H && H % Hkv == 0) ? STRIPED_OK : STRIPED_ERR_INVALID_ARG;
+}
+
 int striped_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
                      int64_t H, int64_t S, int64_t D, int N, int layout, int dtype, float scale,
                      int64_t *tile_stats, void *stream) {
+    return striped_attn_fwd_gqa(q, k, v, o, lse, B, H, H, S, D, N, layout, dtype, scale, tile_stats, stream);
+}
+
+int striped_attn_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                         int64_t H, int64_t Hkv, int64_t S, int64_t D, int N, int layout, int dtype,
+                         float scale, int64_t *tile_stats, void *stream) {
     if (!q || !k || !v || !o || !lse) return STRIPED_ERR_INVALID_ARG;
     int st = check_attn(B, H, S, D, N, layout, dtype);
     if (st) return st;
+    if ((st = check_heads(H, Hkv))) return st;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return STRIPED_ERR_ALIGN;
-    const AttnGeom g = full_geom(B, H, S, D, N, layout, scale);
+    const AttnGeom g = full_geom(B, H, Hkv, S, D, N, layout, scale);
     cudaStream_t s = (cudaStream_t)stream;
     if (dtype == STRIPED_FP32)
         return launch_simt_fwd((const float *)q, (const float *)k, (const float *)v, (float *)o, lse, g,
@@ -277,16 +290,25 @@ int striped_attn_bwd(const void *q, const void *k, const void *v, const void *o,
                      const void *dO, void *dq, void *dk, void *dv, void *workspace,
                      size_t ws_bytes, int64_t B, int64_t H, int64_t S, int64_t D, int N,
                      int layout, int dtype, float scale, int64_t *tile_stats, void *stream) {
+    return striped_attn_bwd_gqa(q, k, v, o, lse, dO, dq, dk, dv, workspace, ws_bytes, B, H, H, S, D, N, layout,
+                                dtype, scale, tile_stats, stream);
+}
+
+int striped_attn_bwd_gqa(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                         const void *dO, void *dq, void *dk, void *dv, void *workspace,
+                         size_t ws_bytes, int64_t B, int64_t H, int64_t Hkv, int64_t S, int64_t D, int N,
+                         int layout, int dtype, float scale, int64_t *tile_stats, void *stream) {
     if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return STRIPED_ERR_INVALID_ARG;
     int st = check_attn(B, H, S, D, N, layout, dtype);
     if (st) return st;
+    if ((st = check_heads(H, Hkv))) return st;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
         !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
         return STRIPED_ERR_ALIGN;
     const size_t need = striped_workspace_size(B, H, S, D, N, dtype);
     if (!workspace || ws_bytes < need) return STRIPED_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return STRIPED_ERR_ALIGN;
-    const AttnGeom g = full_geom(B, H, S, D, N, layout, scale);
+    const AttnGeom g = full_geom(B, H, Hkv, S, D, N, layout, scale);
     cudaStream_t s = (cudaStream_t)stream;
     if (dtype == STRIPED_FP32)
         return launch_simt_bwd((const float *)q, (const float *)k, (const float *)v, (const float *)o, lse,
@@ -314,6 +336,7 @@ int ring_round_fwd(const void *q_d, const void *k_e, const void *v_e, float *o_a
     if ((stride_bh * esize) % 16 != 0 || (stride_bh * 4) % 16 != 0) return STRIPED_ERR_ALIGN;
     AttnGeom g;
     g.BH = B * H;
+    g.G = 1;
     g.L = L;
     g.D = D;
     g.N = N;

@@ -89,39 +89,46 @@ __device__ __forceinline__ int tile_rows(int64_t L, int t) {
 #ifndef BWD_ASCENDING
 #define BWD_ASCENDING 0
 #endif
-// Order in which a key tile visits its query tiles: stripes d = d0, d0+1,
-// ... (mod N), and within a stripe the tiles that see the key tile, in
-// ascending or descending order.
+// Order in which a key tile visits its query tiles: the G query heads that
+// read its key/value head (grouped-query attention; G = 1 otherwise), per
+// head the stripes d = d0, d0+1, ... (mod N), and within a stripe the tiles
+// that see the key tile, in ascending or descending order.
 struct QTileIter {
-    int k, d, a, a_lo, has_diag, diag_off;
+    int h, k, d, a, a_lo, has_diag, diag_off;
 };
 
-__device__ __forceinline__ void qiter_seek(QTileIter &it, int layout, int N, int e, int b, int nq, int rows_b) {
-    while (it.k < N) {
-        it.d = BWD_RING_ORDER ? (e + it.k) % N : it.k;
-        const QuerySpan sp = query_span(layout, it.d, e, b, nq, rows_b);
-        if (sp.a_lo < nq) {
-            it.a_lo = sp.a_lo;
-            it.has_diag = sp.has_diag;
-            it.diag_off = sp.diag_off;
-            it.a = BWD_ASCENDING ? sp.a_lo : nq - 1;
-            return;
+__device__ __forceinline__ void qiter_seek(QTileIter &it, int layout, int N, int G, int e, int b, int nq,
+                                           int rows_b) {
+    while (it.h < G) {
+        while (it.k < N) {
+            it.d = BWD_RING_ORDER ? (e + it.k) % N : it.k;
+            const QuerySpan sp = query_span(layout, it.d, e, b, nq, rows_b);
+            if (sp.a_lo < nq) {
+                it.a_lo = sp.a_lo;
+                it.has_diag = sp.has_diag;
+                it.diag_off = sp.diag_off;
+                it.a = BWD_ASCENDING ? sp.a_lo : nq - 1;
+                return;
+            }
+            ++it.k;
         }
-        ++it.k;
+        it.k = 0;
+        ++it.h;
     }
 }
 
-__device__ __forceinline__ QTileIter qiter_begin(int layout, int N, int e, int b, int nq, int rows_b) {
-    QTileIter it{0, 0, 0, 0, 0, 0};
-    qiter_seek(it, layout, N, e, b, nq, rows_b);
+__device__ __forceinline__ QTileIter qiter_begin(int layout, int N, int G, int e, int b, int nq, int rows_b) {
+    QTileIter it{0, 0, 0, 0, 0, 0, 0};
+    qiter_seek(it, layout, N, G, e, b, nq, rows_b);
     return it;
 }
 
-__device__ __forceinline__ void qiter_next(QTileIter &it, int layout, int N, int e, int b, int nq, int rows_b) {
+__device__ __forceinline__ void qiter_next(QTileIter &it, int layout, int N, int G, int e, int b, int nq,
+                                           int rows_b) {
     const bool end = BWD_ASCENDING ? (++it.a >= nq) : (--it.a < it.a_lo);
     if (end) {
         ++it.k;
-        qiter_seek(it, layout, N, e, b, nq, rows_b);
+        qiter_seek(it, layout, N, G, e, b, nq, rows_b);
     }
 }
 
@@ -143,9 +150,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int N = g.N;
     const int nq = (int)((g.L + BT - 1) / BT);
 
-    // Head-major order: resident CTAs belong to one head and sweep its query
-    // tiles in the same order, sharing Q/dO tiles and dQ accumulator lines
-    // in L2.  Within a head the heaviest key tiles (small b) go first.
+    // Head-major order: resident CTAs belong to one key/value head and sweep
+    // its query tiles in the same order, sharing Q/dO tiles and dQ
+    // accumulator lines in L2.  Within a head the heaviest key tiles (small
+    // b) go first.  bh is the key/value head; query head bh*G + it.h.
+    const int G = (int)g.G;
     const int64_t id = blockIdx.x;
     const int64_t per_head = (int64_t)nq * N;
     const int64_t bh = id / per_head;
@@ -156,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     int nt = 0;
     for (int d = 0; d < N; ++d) nt += nq - query_span(g.layout, d, e, b, nq, rows_b).a_lo;
+    nt *= G;
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bars->kv_full), 1);
@@ -180,9 +190,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (cnt == 0) continue;
                 const int rr = ring_round_of(d, e, N);
                 atomicAdd((unsigned long long *)&p.tile_stats[rr * N + d],
-                          (unsigned long long)(cnt - sp.has_diag));
+                          (unsigned long long)(G * (cnt - sp.has_diag)));
                 atomicAdd((unsigned long long *)&p.tile_stats[N * N + rr * N + d],
-                          (unsigned long long)sp.has_diag);
+                          (unsigned long long)(G * sp.has_diag));
             }
         }
     }
@@ -208,31 +218,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(sbase + kKOff + kBox, &tmK, kb, 64, b * BT, e, (int)bh);
         tma_load_4d(sbase + kVOff, &tmV, kb, 0, b * BT, e, (int)bh);
         tma_load_4d(sbase + kVOff + kBox, &tmV, kb, 64, b * BT, e, (int)bh);
-        QTileIter it = qiter_begin(g.layout, N, e, b, nq, rows_b);
-        for (int i = 0; i < nt; ++i, qiter_next(it, g.layout, N, e, b, nq, rows_b)) {
+        QTileIter it = qiter_begin(g.layout, N, G, e, b, nq, rows_b);
+        for (int i = 0; i < nt; ++i, qiter_next(it, g.layout, N, G, e, b, nq, rows_b)) {
             const int s = i % QS;
             if (i >= QS && !mbar_wait(smem_u32(&bars->q_empty[s]), ((i / QS) + 1) & 1, p.err)) break;
             const uint32_t fb = smem_u32(&bars->q_full[s]);
             const uint32_t qdst = sbase + kQOff + s * 2 * kTile;
+            const int64_t bq = bh * G + it.h;  // query head
             mbar_arrive_expect_tx(fb, kTile + kStatBytes);
             bulk_load(sbase + kStatOff + s * kStatBytes,
-                      p.stats + (((bh * N + it.d) * (int64_t)nq + it.a) << 8), kStatBytes, fb);
-            tma_load_4d(qdst, &tmQ, fb, 0, it.a * BT, it.d, (int)bh);
-            tma_load_4d(qdst + kBox, &tmQ, fb, 64, it.a * BT, it.d, (int)bh);
+                      p.stats + (((bq * N + it.d) * (int64_t)nq + it.a) << 8), kStatBytes, fb);
+            tma_load_4d(qdst, &tmQ, fb, 0, it.a * BT, it.d, (int)bq);
+            tma_load_4d(qdst + kBox, &tmQ, fb, 64, it.a * BT, it.d, (int)bq);
         }
     } else if (warp == 2 && lane == 0 && nt > 0) {
         // ---------------- TMA producer: dO_i (its own stream: the buffer is
         // released later than Q_i's, after the dQ_i half staged in it is read)
         tma_prefetch_desc(&tmdO);
-        QTileIter it = qiter_begin(g.layout, N, e, b, nq, rows_b);
-        for (int i = 0; i < nt; ++i, qiter_next(it, g.layout, N, e, b, nq, rows_b)) {
+        QTileIter it = qiter_begin(g.layout, N, G, e, b, nq, rows_b);
+        for (int i = 0; i < nt; ++i, qiter_next(it, g.layout, N, G, e, b, nq, rows_b)) {
             const int s = i % QS;
             if (i >= QS && !mbar_wait(smem_u32(&bars->do_empty[s]), ((i / QS) + 1) & 1, p.err)) break;
             const uint32_t fb = smem_u32(&bars->do_full[s]);
             const uint32_t odst = sbase + kQOff + s * 2 * kTile + kTile;
+            const int bq = (int)(bh * G + it.h);
             mbar_arrive_expect_tx(fb, kTile);
-            tma_load_4d(odst, &tmdO, fb, 0, it.a * BT, it.d, (int)bh);
-            tma_load_4d(odst + kBox, &tmdO, fb, 64, it.a * BT, it.d, (int)bh);
+            tma_load_4d(odst, &tmdO, fb, 0, it.a * BT, it.d, bq);
+            tma_load_4d(odst + kBox, &tmdO, fb, 64, it.a * BT, it.d, bq);
         }
     } else if (warp == 1 && lane == 0 && nt > 0) {
         // ---------------- MMA issuer
@@ -361,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             return true;
         };
 
-        QTileIter cur = qiter_begin(g.layout, N, e, b, nq, rows_b);
+        QTileIter cur = qiter_begin(g.layout, N, G, e, b, nq, rows_b);
         // warpgroup 1, lane 0: stage whose dQ bulk reduce still reads shared
         // memory (-1: none); the wait for it is deferred to the next tile
         int pending = -1;
@@ -412,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- P of the next tile while the tensor core runs dQ_i / dK_i
             const QTileIter done = cur;
             if (i + 1 < nt) {
-                qiter_next(cur, g.layout, N, e, b, nq, rows_b);
+                qiter_next(cur, g.layout, N, G, e, b, nq, rows_b);
                 if (!compute_p(cur, i + 1)) {
                     ok = false;
                     break;
@@ -439,11 +451,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // dq_full, is done) as two 128-byte-swizzled 32-column boxes and
             // each warp bulk-reduces its own 32 rows, then returns the buffer.
             const int s = i % QS;
+            const int64_t bq = bh * G + done.h;  // query head of tile i
             if (wg == 0) {
                 const int64_t qi = (int64_t)done.a * BT + row;
                 if (qi < g.L) {
                     float *dst =
-                        p.dq_acc + (bh * g.stride_bh + (int64_t)done.d * g.stripe_stride + qi * HD + cbase);
+                        p.dq_acc + (bq * g.stride_bh + (int64_t)done.d * g.stripe_stride + qi * HD + cbase);
 #pragma unroll
                     for (int v = 0; v < 8; ++v)
                         red_add_v4(dst + 4 * v, __uint_as_float(q0[4 * v]), __uint_as_float(q0[4 * v + 1]),
@@ -471,8 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     const uint32_t wofs = (uint32_t)quarter * 32 * 128;
                     const int r0 = done.a * BT + quarter * 32;
-                    tma_reduce_add_4d(&tmdQ, stage + wofs, cbase, r0, done.d, (int)bh);
-                    tma_reduce_add_4d(&tmdQ, stage + kBox + wofs, cbase + 32, r0, done.d, (int)bh);
+                    tma_reduce_add_4d(&tmdQ, stage + wofs, cbase, r0, done.d, (int)bq);
+                    tma_reduce_add_4d(&tmdQ, stage + kBox + wofs, cbase + 32, r0, done.d, (int)bq);
                     bulk_commit_group();
                     pending = s;
                 }
@@ -615,9 +628,10 @@ int launch_tc_bwd(const void *q, const void *k, const void *v, const void *o, co
     int st = cuda_status(cudaGetLastError());
     if (st != STRIPED_OK) return st;
     CUtensorMap mq, mk, mv, mdo;
+    const int64_t bh_kv = g.BH / g.G;
     if ((st = make_bf16_map(&mq, q, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 128)) ||
-        (st = make_bf16_map(&mk, k, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 128)) ||
-        (st = make_bf16_map(&mv, v, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 128)) ||
+        (st = make_bf16_map(&mk, k, g.D, g.L, g.N, bh_kv, g.stripe_stride, g.stride_bh, 128)) ||
+        (st = make_bf16_map(&mv, v, g.D, g.L, g.N, bh_kv, g.stripe_stride, g.stride_bh, 128)) ||
         (st = make_bf16_map(&mdo, dO, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 128)))
         return st;
     CUtensorMap mdq;
@@ -631,7 +645,7 @@ int launch_tc_bwd(const void *q, const void *k, const void *v, const void *o, co
     p.tile_stats = tile_stats;
     p.err = device_error_word();
     const int64_t nk = (g.L + BT - 1) / BT;
-    const int64_t nblocks = nk * g.N * g.BH;
+    const int64_t nblocks = nk * g.N * bh_kv;  // one CTA per key tile of every key/value head
     if (nblocks > 0x7fffffffll) return STRIPED_ERR_UNSUPPORTED;
     tc_bwd_kernel<<<(unsigned)nblocks, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, p);
     st = cuda_status(cudaGetLastError());

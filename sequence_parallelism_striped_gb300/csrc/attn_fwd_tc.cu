@@ -149,6 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS0 = tmem, tS1 = tmem + 128, tO = tmem + 256;
 
     const int qstripe = kRound ? 0 : d;
+    const int kvh = (int)(bh / g.G);  // key/value head read by query head bh
     if (warp == 0 && lane == 0 && nt > 0) {
         // ---------------- TMA producer
         tma_prefetch_desc(&tmQ);
@@ -175,10 +176,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t kdst = sbase + kKVOff + s * kStageBytes;
                 const uint32_t vdst = kdst + kTileBytes;
                 mbar_arrive_expect_tx(fb, 2 * kTileBytes);
-                tma_load_4d(kdst, &tmK, fb, 0, b * BN, kstripe, (int)bh);
-                tma_load_4d(kdst + kBoxBytes, &tmK, fb, 64, b * BN, kstripe, (int)bh);
-                tma_load_4d(vdst, &tmV, fb, 0, b * BN, kstripe, (int)bh);
-                tma_load_4d(vdst + kBoxBytes, &tmV, fb, 64, b * BN, kstripe, (int)bh);
+                tma_load_4d(kdst, &tmK, fb, 0, b * BN, kstripe, kvh);
+                tma_load_4d(kdst + kBoxBytes, &tmK, fb, 64, b * BN, kstripe, kvh);
+                tma_load_4d(vdst, &tmV, fb, 0, b * BN, kstripe, kvh);
+                tma_load_4d(vdst + kBoxBytes, &tmV, fb, 64, b * BN, kstripe, kvh);
             }
         }
     } else if (warp == 1 && lane == 0 && nt > 0) {
@@ -440,9 +441,10 @@ int launch_tc_fwd(const void *q, const void *k, const void *v, void *o, float *l
     int st = set_smem_once();
     if (st != STRIPED_OK) return st;
     CUtensorMap mq, mk, mv;
+    const int64_t bh_kv = g.BH / g.G;
     if ((st = make_bf16_map(&mq, q, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 128)) ||
-        (st = make_bf16_map(&mk, k, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 128)) ||
-        (st = make_bf16_map(&mv, v, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 128)))
+        (st = make_bf16_map(&mk, k, g.D, g.L, g.N, bh_kv, g.stripe_stride, g.stride_bh, 128)) ||
+        (st = make_bf16_map(&mv, v, g.D, g.L, g.N, bh_kv, g.stripe_stride, g.stride_bh, 128)))
         return st;
     FwdParams p{};
     p.g = g;
@@ -470,6 +472,7 @@ int launch_tc_round(const void *q_d, const void *k_e, const void *v_e, float *o_
         return st;
     FwdParams p{};
     p.g = g;
+    p.g.G = 1;
     p.g.stripe_stride = 0;
     p.g.lse_stripe_stride = 0;
     p.d_fixed = d;

@@ -126,9 +126,10 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(const float *__restr
     const int a = nq - 1 - (int)(blockIdx.x % nq);  // heavy query tiles first
     const int d = (int)(blockIdx.x / nq);
     const int64_t bh = blockIdx.y;
+    const int64_t kvh = bh / g.G;  // key/value head of query head bh
     const float *q_stripe = q + bh * g.stride_bh + (int64_t)d * g.stripe_stride;
     RowState st;
-    fwd_tile(q_stripe, k + bh * g.stride_bh, v + bh * g.stride_bh, g, d, a, 0, g.N, -1, st,
+    fwd_tile(q_stripe, k + kvh * g.stride_bh, v + kvh * g.stride_bh, g, d, a, 0, g.N, -1, st,
              tile_stats, sK, sV);
     const int row = threadIdx.x / kTPR, sub = threadIdx.x % kTPR;
     const int64_t i = (int64_t)a * T + row;
@@ -236,8 +237,8 @@ __global__ void __launch_bounds__(kThreads) simt_dq_kernel(
             atomicAdd((unsigned long long *)&tile_stats[g.N * g.N + r * g.N + d],
                       (unsigned long long)sp.has_diag);
         }
-        const float *k_stripe = k + bh * g.stride_bh + (int64_t)e * g.stripe_stride;
-        const float *v_stripe = v + bh * g.stride_bh + (int64_t)e * g.stripe_stride;
+        const float *k_stripe = k + (bh / g.G) * g.stride_bh + (int64_t)e * g.stripe_stride;
+        const float *v_stripe = v + (bh / g.G) * g.stride_bh + (int64_t)e * g.stripe_stride;
         for (int b = 0; b < ntiles; ++b) {
             __syncthreads();
             stage_rows(sK, k_stripe, L, D, b);
@@ -269,8 +270,9 @@ __global__ void __launch_bounds__(kThreads) simt_dq_kernel(
     for (int u = 0; u < dpt; ++u) dq[qoff + u] = g.scale * acc[u];
 }
 
-// dK, dV: key tile b of stripe e; visits every query tile that sees it, in
-// ring order (round r: the key stripe sits on device d = e + r).
+// dK, dV: key tile b of stripe e of key/value head blockIdx.y; visits every
+// query tile that sees it, for each of the G query heads that read the head,
+// in ring order (round r: the key stripe sits on device d = e + r).
 __global__ void __launch_bounds__(kThreads) simt_dkdv_kernel(
     const float *__restrict__ q, const float *__restrict__ k, const float *__restrict__ v,
     const float *__restrict__ lse, const float *__restrict__ dO, const float *__restrict__ delta,
@@ -296,13 +298,15 @@ __global__ void __launch_bounds__(kThreads) simt_dkdv_kernel(
         ak[u] = av[u] = 0.f;
     }
     const int rows_b = rows_in_tile(L, b);
-    for (int r = 0; r < g.N; ++r) {
+    for (int hr = 0; hr < g.G * g.N; ++hr) {
+        const int64_t bq = bh * g.G + hr / g.N;  // query head
+        const int r = (int)(hr % g.N);
         const int d = (e + r) % g.N;
         const QuerySpan sp = query_span(g.layout, d, e, b, nq, rows_b);
-        const float *q_stripe = q + bh * g.stride_bh + (int64_t)d * g.stripe_stride;
-        const float *do_stripe = dO + bh * g.stride_bh + (int64_t)d * g.stripe_stride;
-        const float *l_stripe = lse + bh * g.lse_stride_bh + (int64_t)d * g.lse_stripe_stride;
-        const float *dl_stripe = delta + bh * g.lse_stride_bh + (int64_t)d * g.lse_stripe_stride;
+        const float *q_stripe = q + bq * g.stride_bh + (int64_t)d * g.stripe_stride;
+        const float *do_stripe = dO + bq * g.stride_bh + (int64_t)d * g.stripe_stride;
+        const float *l_stripe = lse + bq * g.lse_stride_bh + (int64_t)d * g.lse_stripe_stride;
+        const float *dl_stripe = delta + bq * g.lse_stride_bh + (int64_t)d * g.lse_stripe_stride;
         for (int a = sp.a_lo; a < nq; ++a) {
             __syncthreads();
             stage_rows(sQ, q_stripe, L, D, a);
@@ -385,8 +389,9 @@ int launch_simt_bwd(const float *q, const float *k, const float *v, const float 
     simt_dq_kernel<<<grid, kThreads, smem, stream>>>(q, k, v, lse, dO, delta_ws, dq, g, tile_stats);
     st = cuda_status(cudaGetLastError());
     if (st != STRIPED_OK) return st;
-    simt_dkdv_kernel<<<grid, kThreads, smem + 2 * T * sizeof(float), stream>>>(q, k, v, lse, dO,
-                                                                               delta_ws, dk, dv, g);
+    dim3 grid_kv((unsigned)(nq * g.N), (unsigned)(g.BH / g.G));  // key tiles of every key/value head
+    simt_dkdv_kernel<<<grid_kv, kThreads, smem + 2 * T * sizeof(float), stream>>>(q, k, v, lse, dO,
+                                                                                  delta_ws, dk, dv, g);
     return cuda_status(cudaGetLastError());
 }
 

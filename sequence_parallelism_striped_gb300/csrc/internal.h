@@ -22,8 +22,12 @@ int *device_error_word();
 // [BH][N stripes][L rows][D] with stripe e of head bh starting at element
 // bh*stride_bh + e*stripe_stride (stripe_stride = L*D for full tensors,
 // 0 when the pointers are already the stripe slices of one round).
+// Grouped-query attention: query head bh (of B*H) reads key/value head
+// bh / G (of B*H/G), i.e. G consecutive query heads share one; G = 1 is
+// plain multi-head attention.
 struct AttnGeom {
     int64_t BH, L, D;
+    int64_t G;                  // query heads per key/value head
     int N;
     int layout;
     int64_t stride_bh;          // elements between heads (q/k/v/o)

@@ -111,6 +111,13 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.striped_layout_permute(fake, P(1 << 24), 1, 1, 12, 128, 4, 2, 0, None) == -1
     assert lib.striped_layout_permute(fake, P(1 << 24), 1, 1, 16, 128, 4, 3, 0, None) == -1
     assert lib.striped_tile_counts(36, 4, 16, 16, 2, None, None) == -1
+    # grouped-query attention: Hkv must divide H
+    assert lib.striped_attn_fwd_gqa(fake, fake, fake, fake, fake, 1, 6, 4, 64, 128, 4, 0, 0, 1.0, None,
+                                    None) == -1
+    assert lib.striped_attn_fwd_gqa(fake, fake, fake, fake, fake, 1, 4, 0, 64, 128, 4, 0, 0, 1.0, None,
+                                    None) == -1
+    assert lib.striped_attn_bwd_gqa(fake, fake, fake, fake, fake, fake, fake, fake, fake, fake, 1 << 30, 1, 4, 8,
+                                    64, 128, 4, 0, 0, 1.0, None, None) == -1
 
 
 def test_workspace_size(lib):
