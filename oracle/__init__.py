@@ -23,7 +23,10 @@ Causal Transformers"):
   ``oracle.c`` and compared against the striped placement;
 * grouped-query attention (query head h reads key/value head h // G) is not
   on the pages either: ``attn_fwd_gqa`` / ``attn_bwd_gqa`` compose the
-  per-head definition, summing the gradients of a shared key/value head.
+  per-head definition, summing the gradients of a shared key/value head;
+* packed variable-length batches (not on the pages): ``attn_fwd_varlen`` /
+  ``attn_bwd_varlen`` apply the definition to each sequence on its own, and
+  ``varlen_positions`` places each sequence on its own inside every device.
 
 Pins: every function here is checked in ``tests/test_oracle.py`` against
 things other than itself (closed forms, special cases, library routines,
@@ -258,6 +261,52 @@ def attn_bwd_gqa(q, k, v, dO, scale: float, nthreads: int | None = None):
         dk[h // G] += gk
         dv[h // G] += gv
     return dq, dk, dv
+
+
+# --------------------------------------------------------------------------
+# packed variable-length batches (not on the pages): sequences
+# [cu[i], cu[i+1]) of one packed head attend only within themselves
+# --------------------------------------------------------------------------
+def varlen_positions(cu_seqlens, N: int, layout: int) -> np.ndarray:
+    """pos[row] of a packed head: device d's rows hold, sequence after
+    sequence, that sequence's rows of device d under `layout` (each sequence
+    placed on its own), so row d*L + cu[i]/N + j holds cu[i] + pos_i(d*L_i + j)
+    with L = S/N and L_i = (cu[i+1] - cu[i]) / N."""
+    cu = [int(c) for c in cu_seqlens]
+    S = cu[-1]
+    L = S // N
+    pos = np.empty(S, dtype=np.int64)
+    for i in range(len(cu) - 1):
+        Si = cu[i + 1] - cu[i]
+        Li = Si // N
+        own = layout_positions(Si, N, layout)  # row -> position inside sequence i
+        for d in range(N):
+            pos[d * L + cu[i] // N: d * L + cu[i] // N + Li] = cu[i] + own[d * Li:(d + 1) * Li]
+    return pos
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens, scale: float, nthreads: int | None = None):
+    """One packed head [S, D] in position order: causal attention inside each
+    sequence, nothing across sequences (block-diagonal causal mask)."""
+    cu = [int(c) for c in cu_seqlens]
+    o = np.empty((cu[-1], np.shape(v)[1]))
+    lse = np.empty(cu[-1])
+    for i in range(len(cu) - 1):
+        a, b = cu[i], cu[i + 1]
+        o[a:b], lse[a:b] = attn_fwd(q[a:b], k[a:b], v[a:b], scale, nthreads=nthreads)
+    return o, lse
+
+
+def attn_bwd_varlen(q, k, v, dO, cu_seqlens, scale: float, nthreads: int | None = None):
+    """Gradients of attn_fwd_varlen: each sequence's own backward."""
+    cu = [int(c) for c in cu_seqlens]
+    out = [np.empty((cu[-1], np.shape(q)[1])) for _ in range(3)]
+    for i in range(len(cu) - 1):
+        a, b = cu[i], cu[i + 1]
+        g = attn_bwd(q[a:b], k[a:b], v[a:b], dO[a:b], scale, nthreads=nthreads)
+        for t in range(3):
+            out[t][a:b] = g[t]
+    return tuple(out)
 
 
 def merge_rounds(o_a, lse_a, o_b, lse_b):

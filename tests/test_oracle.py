@@ -390,3 +390,46 @@ def test_gqa_matches_torch_autograd_with_repeated_kv(oracle_lib, H, Hkv):
     assert np.allclose(dq, tq.grad.numpy(), atol=1e-11)
     assert np.allclose(dk, tk.grad.numpy(), atol=1e-11)
     assert np.allclose(dv, tv.grad.numpy(), atol=1e-11)
+
+
+# ---------------------------------------------------------------- packed variable-length batches
+def test_varlen_matches_torch_block_diagonal_mask(oracle_lib):
+    """Packed sequences: torch's fp64 SDPA with an explicit block-diagonal
+    causal mask (keep t <= p inside one sequence), and its autograd."""
+    cu = [0, 8, 24, 28, 48]
+    S, D = cu[-1], 6
+    rng = np.random.default_rng(51)
+    q, k, v, do = (rng.standard_normal((S, D)) for _ in range(4))
+    seq = np.repeat(np.arange(len(cu) - 1), np.diff(cu))
+    keep = (seq[:, None] == seq[None, :]) & (np.arange(S)[None, :] <= np.arange(S)[:, None])
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(tq[None, None], tk[None, None], tv[None, None],
+                                                         attn_mask=torch.tensor(keep), scale=0.3)[0, 0]
+    o.backward(torch.tensor(do))
+    o_ref, _ = oracle.attn_fwd_varlen(q, k, v, cu, 0.3)
+    assert np.allclose(o_ref, o.detach().numpy(), atol=1e-12)
+    g = oracle.attn_bwd_varlen(q, k, v, do, cu, 0.3)
+    for got, t in zip(g, (tq, tk, tv)):
+        assert np.allclose(got, t.grad.numpy(), atol=1e-11)
+
+
+@pytest.mark.parametrize("layout", [STRIPED, CONTIGUOUS, ZIGZAG])
+def test_varlen_positions_place_each_sequence_on_its_own(oracle_lib, layout):
+    """Every device's rows hold, sequence after sequence, that sequence's own
+    placement; the map is a permutation; one sequence reduces to the plain
+    placement."""
+    N = 4
+    cu = [0, 16, 24, 56, 64]
+    pos = oracle.varlen_positions(cu, N, layout)
+    S = cu[-1]
+    assert sorted(pos.tolist()) == list(range(S))
+    L = S // N
+    for d in range(N):
+        rows = pos[d * L:(d + 1) * L]
+        off = 0
+        for i in range(len(cu) - 1):
+            Li = (cu[i + 1] - cu[i]) // N
+            own = oracle.layout_positions(cu[i + 1] - cu[i], N, layout)[d * Li:(d + 1) * Li]
+            assert np.array_equal(rows[off:off + Li], cu[i] + own)
+            off += Li
+    assert np.array_equal(oracle.varlen_positions([0, 64], N, layout), oracle.layout_positions(64, N, layout))
