@@ -108,6 +108,27 @@ int striped_layout_unpermute(const void *x, void *y, int64_t B, int64_t H, int64
                              int N, int layout, int dtype, void *stream);
 
 /*
+ * Packed variable-length batches (not on the pages; for training on packed
+ * documents).  One packed head holds nseq sequences, positions
+ * [cu_seqlens[i], cu_seqlens[i+1]) for sequence i; cu_seqlens is a HOST
+ * int32 array of nseq + 1 entries with cu_seqlens[0] = 0, S = cu_seqlens[nseq].
+ * Each sequence is placed on its own (`layout`, with its own length) and a
+ * device's slice of L = S/N rows holds, sequence after sequence, that
+ * sequence's L_i = S_i/N rows: row d*L + cu_seqlens[i]/N + j holds position
+ * cu_seqlens[i] + pos_i(d*L_i + j).  Tensors are [H, S, D] (one batch
+ * entry).  Every S_i must be a positive multiple of N (2N for zig-zag), else
+ * STRIPED_ERR_INVALID_ARG; at most 512 sequences (STRIPED_ERR_UNSUPPORTED
+ * beyond).  The table is checked on the host and passed to the kernels by
+ * value, so nothing is allocated.
+ */
+int striped_varlen_permute(const void *x, void *y, const int32_t *cu_seqlens, int nseq, int64_t H, int64_t D,
+                           int N, int layout, int dtype, void *stream);
+
+/* Inverse of striped_varlen_permute. */
+int striped_varlen_unpermute(const void *x, void *y, const int32_t *cu_seqlens, int nseq, int64_t H, int64_t D,
+                             int N, int layout, int dtype, void *stream);
+
+/*
  * Causal attention forward over all N ring rounds in one launch (§Summary:
  * each device attends to every circulating key/value stripe; exact result,
  * pith.science abstract).  For each query row of stripe d, rounds
@@ -139,6 +160,19 @@ int striped_attn_fwd(const void *q, const void *k, const void *v, void *o, float
 int striped_attn_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
                          int64_t H, int64_t Hkv, int64_t S, int64_t D, int N, int layout, int dtype,
                          float scale, int64_t *tile_stats, void *stream);
+
+/*
+ * Packed variable-length form of striped_attn_fwd_gqa: q, o [H,S,D], k, v
+ * [Hkv,S,D], lse [H,S], rows placed as striped_varlen_permute describes.
+ * Each sequence attends only within itself (causal inside the sequence):
+ * every kernel works on the tiles of one sequence at a time, so tiles across
+ * sequences are neither computed nor counted.  Every S_i must also be a
+ * whole number of kernel tiles per device: S_i a multiple of N*T (2N*T for
+ * zig-zag), T from striped_kernel_tile(), else STRIPED_ERR_UNSUPPORTED.
+ */
+int striped_attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                            const int32_t *cu_seqlens, int nseq, int64_t H, int64_t Hkv, int64_t D, int N,
+                            int layout, int dtype, float scale, int64_t *tile_stats, void *stream);
 
 /* Bytes of device workspace striped_attn_bwd needs for these sizes (fp32 dQ
  * accumulator and per-row softmax statistics padded to whole tiles), or 0
@@ -172,6 +206,15 @@ int striped_attn_bwd_gqa(const void *q, const void *k, const void *v, const void
                          const void *dO, void *dq, void *dk, void *dv, void *workspace,
                          size_t ws_bytes, int64_t B, int64_t H, int64_t Hkv, int64_t S, int64_t D, int N,
                          int layout, int dtype, float scale, int64_t *tile_stats, void *stream);
+
+/*
+ * Backward of striped_attn_fwd_varlen (same packed layout and limits); the
+ * workspace is striped_workspace_size(1, H, S, D, N, dtype).
+ */
+int striped_attn_bwd_varlen(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                            const void *dO, void *dq, void *dk, void *dv, void *workspace, size_t ws_bytes,
+                            const int32_t *cu_seqlens, int nseq, int64_t H, int64_t Hkv, int64_t D, int N,
+                            int layout, int dtype, float scale, int64_t *tile_stats, void *stream);
 
 /*
  * striped_attn_bwd for callers that cannot allocate device memory (the paper

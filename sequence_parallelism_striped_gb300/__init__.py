@@ -73,6 +73,11 @@ def load(build_if_missing: bool = True):
                                              F, P, P]
         lib.ring_round_fwd.argtypes = [P, P, P, P, P, P, I, I, I64, I64, I64, I64, I, I64, I64, I, I, F, I,
                                        P, P]
+        lib.striped_varlen_permute.argtypes = [P, P, P, I, I64, I64, I, I, I, P]
+        lib.striped_varlen_unpermute.argtypes = [P, P, P, I, I64, I64, I, I, I, P]
+        lib.striped_attn_fwd_varlen.argtypes = [P, P, P, P, P, P, I, I64, I64, I64, I, I, I, F, P, P]
+        lib.striped_attn_bwd_varlen.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, P, I, I64, I64, I64, I, I, I,
+                                                F, P, P]
         lib.striped_kernel_tile.argtypes = [I, I64, P, P]
         lib.striped_tile_counts.argtypes = [I64, I, I, I, I, P, P]
         lib.striped_critical_path.argtypes = [I64, I, I, I, I]
@@ -262,6 +267,76 @@ def ring_round_fwd(q, k, v, o_acc, lse_acc, d: int, e: int, N: int, layout: int 
     _check(load().ring_round_fwd(qd, ke, ve, oa, la, oo, d, e, B, H, L, D, N, S * D, S, layout,
                                  _dtype_code(q), float(scale), 1 if first_round else 0,
                                  _ptr_or_null(tile_stats), _stream(stream)), "ring_round_fwd")
+
+
+# ------------------------------------------------------------------ packed sequences
+def _cu_host(cu_seqlens):
+    """cu_seqlens (list, numpy or CPU tensor) -> contiguous host int32 array."""
+    import numpy as np
+
+    if isinstance(cu_seqlens, torch.Tensor):
+        cu_seqlens = cu_seqlens.cpu().numpy()
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    return cu, cu.ctypes.data_as(ctypes.c_void_p), len(cu) - 1
+
+
+def striped_varlen_permute(x: torch.Tensor, cu_seqlens, N: int, layout: int = STRIPED, out=None, stream=None):
+    """Packed head [H, S, D] in position order -> each sequence placed on
+    its own, device slices of all sequences concatenated."""
+    H, S, D = x.shape
+    y = torch.empty_like(x) if out is None else out
+    cu, cp, n = _cu_host(cu_seqlens)
+    _check(load().striped_varlen_permute(_dev(x, "x"), _dev(y, "y"), cp, n, H, D, N, layout, _dtype_code(x),
+                                         _stream(stream)), "striped_varlen_permute")
+    return y
+
+
+def striped_varlen_unpermute(x: torch.Tensor, cu_seqlens, N: int, layout: int = STRIPED, out=None, stream=None):
+    """Inverse of striped_varlen_permute."""
+    H, S, D = x.shape
+    y = torch.empty_like(x) if out is None else out
+    cu, cp, n = _cu_host(cu_seqlens)
+    _check(load().striped_varlen_unpermute(_dev(x, "x"), _dev(y, "y"), cp, n, H, D, N, layout, _dtype_code(x),
+                                           _stream(stream)), "striped_varlen_unpermute")
+    return y
+
+
+def striped_attn_fwd_varlen(q, k, v, cu_seqlens, N: int, layout: int = STRIPED, scale: float | None = None,
+                            tile_stats: torch.Tensor | None = None, out=None, lse_out=None, stream=None):
+    """Packed sequences: q [H,S,D], k and v [Hkv,S,D]; returns (o, lse [H,S])."""
+    H, S, D = q.shape
+    Hkv = k.shape[0]
+    if scale is None:
+        scale = 1.0 / D ** 0.5
+    o = torch.empty_like(q) if out is None else out
+    lse = torch.empty((H, S), dtype=torch.float32, device=q.device) if lse_out is None else lse_out
+    cu, cp, n = _cu_host(cu_seqlens)
+    _check(load().striped_attn_fwd_varlen(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(o, "o"),
+                                          _dev(lse, "lse"), cp, n, H, Hkv, D, N, layout, _dtype_code(q),
+                                          float(scale), _ptr_or_null(tile_stats), _stream(stream)),
+           "striped_attn_fwd_varlen")
+    return o, lse
+
+
+def striped_attn_bwd_varlen(q, k, v, o, lse, dO, cu_seqlens, N: int, layout: int = STRIPED,
+                            scale: float | None = None, workspace=None, tile_stats=None, dq=None, dk=None, dv=None,
+                            stream=None):
+    """Backward of striped_attn_fwd_varlen; returns (dq, dk, dv)."""
+    H, S, D = q.shape
+    Hkv = k.shape[0]
+    if scale is None:
+        scale = 1.0 / D ** 0.5
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws = new_workspace(1, H, S, D, N, q.dtype, q.device) if workspace is None else workspace
+    cu, cp, n = _cu_host(cu_seqlens)
+    _check(load().striped_attn_bwd_varlen(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(o, "o"),
+                                          _dev(lse, "lse"), _dev(dO, "dO"), _dev(dq, "dq"), _dev(dk, "dk"),
+                                          _dev(dv, "dv"), _dev(ws, "workspace"), ws.numel() * ws.element_size(),
+                                          cp, n, H, Hkv, D, N, layout, _dtype_code(q), float(scale),
+                                          _ptr_or_null(tile_stats), _stream(stream)), "striped_attn_bwd_varlen")
+    return dq, dk, dv
 
 
 # ------------------------------------------------------------------ host model

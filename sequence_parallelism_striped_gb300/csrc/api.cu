@@ -120,7 +120,7 @@ static int check_attn(int64_t B, int64_t H, int64_t S, int64_t D, int N, int lay
 
 static AttnGeom full_geom(int64_t B, int64_t H, int64_t Hkv, int64_t S, int64_t D, int N, int layout,
                           float scale) {
-    AttnGeom g;
+    AttnGeom g{};  // seqs.n = 0: dense
     g.BH = B * H;
     g.G = H / Hkv;
     g.L = S / N;
@@ -203,8 +203,32 @@ int striped_kernel_tile(int dtype, int64_t D, int *Tq, int *Tk) {
 }
 
 // ---------------------------------------------------------------- permutation
+// Packed sequences: check the HOST array cu_seqlens[0..nseq] (starts at 0,
+// every length a positive multiple of N * unit rows) and build the table
+// the kernels carry.  A length that is not a multiple of N (2N for zig-zag)
+// has no placement (invalid); one that is, but not a whole number of `unit`
+// rows per device, is a kernel restriction (unsupported).
+static int make_seq_table(const int32_t *cu, int nseq, int N, int layout, int64_t unit, SeqTable *t,
+                          int64_t *S) {
+    if (!cu || nseq < 1 || N < 1) return STRIPED_ERR_INVALID_ARG;
+    if (nseq > kMaxSeqs) return STRIPED_ERR_UNSUPPORTED;
+    if (cu[0] != 0) return STRIPED_ERR_INVALID_ARG;
+    const int64_t place = (layout == STRIPED_LAYOUT_ZIGZAG) ? 2 * (int64_t)N : (int64_t)N;
+    int status = STRIPED_OK;
+    for (int i = 0; i < nseq; ++i) {
+        const int64_t len = (int64_t)cu[i + 1] - cu[i];
+        if (len <= 0 || len % place != 0) return STRIPED_ERR_INVALID_ARG;
+        if ((len / place) % unit != 0) status = STRIPED_ERR_UNSUPPORTED;
+    }
+    if (status != STRIPED_OK) return status;
+    t->n = nseq;
+    for (int i = 0; i <= nseq; ++i) t->row_start[i] = cu[i] / N;
+    *S = cu[nseq];
+    return STRIPED_OK;
+}
+
 static int permute_common(const void *x, void *y, int64_t B, int64_t H, int64_t S, int64_t D, int N,
-                          int layout, int dtype, void *stream, bool gather) {
+                          int layout, int dtype, void *stream, bool gather, const SeqTable &seqs) {
     if (!x || !y) return STRIPED_ERR_INVALID_ARG;
     int st = check_sizes(B, H, S, D, N);
     if (st) return st;
@@ -219,27 +243,47 @@ static int permute_common(const void *x, void *y, int64_t B, int64_t H, int64_t 
     const char *xb = (const char *)x, *yb = (const char *)y;
     const int64_t bytes = B * H * S * D * esize;
     if (xb < yb + bytes && yb < xb + bytes) return STRIPED_ERR_INVALID_ARG;  // overlap
-    return launch_stripe_permute(x, y, B * H, S, D * esize, N, layout, gather, (cudaStream_t)stream);
+    return launch_stripe_permute(x, y, B * H, S, D * esize, N, layout, gather, seqs, (cudaStream_t)stream);
 }
+
+static const SeqTable kDense{};  // n = 0: one sequence per (batch, head)
 
 int striped_permute(const void *x, void *y, int64_t B, int64_t H, int64_t S, int64_t D, int N,
                     int dtype, void *stream) {
-    return permute_common(x, y, B, H, S, D, N, STRIPED_LAYOUT_STRIPED, dtype, stream, true);
+    return permute_common(x, y, B, H, S, D, N, STRIPED_LAYOUT_STRIPED, dtype, stream, true, kDense);
 }
 
 int striped_unpermute(const void *x, void *y, int64_t B, int64_t H, int64_t S, int64_t D, int N,
                       int dtype, void *stream) {
-    return permute_common(x, y, B, H, S, D, N, STRIPED_LAYOUT_STRIPED, dtype, stream, false);
+    return permute_common(x, y, B, H, S, D, N, STRIPED_LAYOUT_STRIPED, dtype, stream, false, kDense);
 }
 
 int striped_layout_permute(const void *x, void *y, int64_t B, int64_t H, int64_t S, int64_t D, int N,
                            int layout, int dtype, void *stream) {
-    return permute_common(x, y, B, H, S, D, N, layout, dtype, stream, true);
+    return permute_common(x, y, B, H, S, D, N, layout, dtype, stream, true, kDense);
 }
 
 int striped_layout_unpermute(const void *x, void *y, int64_t B, int64_t H, int64_t S, int64_t D,
                              int N, int layout, int dtype, void *stream) {
-    return permute_common(x, y, B, H, S, D, N, layout, dtype, stream, false);
+    return permute_common(x, y, B, H, S, D, N, layout, dtype, stream, false, kDense);
+}
+
+int striped_varlen_permute(const void *x, void *y, const int32_t *cu_seqlens, int nseq, int64_t H, int64_t D,
+                           int N, int layout, int dtype, void *stream) {
+    SeqTable t{};
+    int64_t S = 0;
+    const int st = make_seq_table(cu_seqlens, nseq, N, layout, 1, &t, &S);
+    if (st) return st;
+    return permute_common(x, y, 1, H, S, D, N, layout, dtype, stream, true, t);
+}
+
+int striped_varlen_unpermute(const void *x, void *y, const int32_t *cu_seqlens, int nseq, int64_t H, int64_t D,
+                             int N, int layout, int dtype, void *stream) {
+    SeqTable t{};
+    int64_t S = 0;
+    const int st = make_seq_table(cu_seqlens, nseq, N, layout, 1, &t, &S);
+    if (st) return st;
+    return permute_common(x, y, 1, H, S, D, N, layout, dtype, stream, false, t);
 }
 
 // ---------------------------------------------------------------- attention
@@ -253,20 +297,40 @@ int striped_attn_fwd(const void *q, const void *k, const void *v, void *o, float
     return striped_attn_fwd_gqa(q, k, v, o, lse, B, H, H, S, D, N, layout, dtype, scale, tile_stats, stream);
 }
 
-int striped_attn_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
-                         int64_t H, int64_t Hkv, int64_t S, int64_t D, int N, int layout, int dtype,
-                         float scale, int64_t *tile_stats, void *stream) {
+static int attn_fwd_common(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                           int64_t H, int64_t Hkv, int64_t S, int64_t D, int N, int layout, int dtype,
+                           float scale, int64_t *tile_stats, void *stream, const SeqTable &seqs) {
     if (!q || !k || !v || !o || !lse) return STRIPED_ERR_INVALID_ARG;
     int st = check_attn(B, H, S, D, N, layout, dtype);
     if (st) return st;
     if ((st = check_heads(H, Hkv))) return st;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return STRIPED_ERR_ALIGN;
-    const AttnGeom g = full_geom(B, H, Hkv, S, D, N, layout, scale);
+    AttnGeom g = full_geom(B, H, Hkv, S, D, N, layout, scale);
+    g.seqs = seqs;
     cudaStream_t s = (cudaStream_t)stream;
     if (dtype == STRIPED_FP32)
         return launch_simt_fwd((const float *)q, (const float *)k, (const float *)v, (float *)o, lse, g,
                                tile_stats, s);
     return launch_tc_fwd(q, k, v, o, lse, g, tile_stats, s);
+}
+
+int striped_attn_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                         int64_t H, int64_t Hkv, int64_t S, int64_t D, int N, int layout, int dtype,
+                         float scale, int64_t *tile_stats, void *stream) {
+    return attn_fwd_common(q, k, v, o, lse, B, H, Hkv, S, D, N, layout, dtype, scale, tile_stats, stream, kDense);
+}
+
+// the kernel tile for dtype (128 for bf16 tensor cores, 16 for fp32)
+static int64_t tile_of(int dtype) { return dtype == STRIPED_BF16 ? kTcTile : kSimtTile; }
+
+int striped_attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                            const int32_t *cu_seqlens, int nseq, int64_t H, int64_t Hkv, int64_t D, int N,
+                            int layout, int dtype, float scale, int64_t *tile_stats, void *stream) {
+    SeqTable t{};
+    int64_t S = 0;
+    const int st = make_seq_table(cu_seqlens, nseq, N, layout, tile_of(dtype), &t, &S);
+    if (st) return st;
+    return attn_fwd_common(q, k, v, o, lse, 1, H, Hkv, S, D, N, layout, dtype, scale, tile_stats, stream, t);
 }
 
 // bf16 workspace: fp32 dQ accumulator [B*H*S][D], then per (b, h, stripe)
@@ -294,10 +358,10 @@ int striped_attn_bwd(const void *q, const void *k, const void *v, const void *o,
                                 dtype, scale, tile_stats, stream);
 }
 
-int striped_attn_bwd_gqa(const void *q, const void *k, const void *v, const void *o, const float *lse,
-                         const void *dO, void *dq, void *dk, void *dv, void *workspace,
-                         size_t ws_bytes, int64_t B, int64_t H, int64_t Hkv, int64_t S, int64_t D, int N,
-                         int layout, int dtype, float scale, int64_t *tile_stats, void *stream) {
+static int attn_bwd_common(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                           const void *dO, void *dq, void *dk, void *dv, void *workspace, size_t ws_bytes,
+                           int64_t B, int64_t H, int64_t Hkv, int64_t S, int64_t D, int N, int layout,
+                           int dtype, float scale, int64_t *tile_stats, void *stream, const SeqTable &seqs) {
     if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return STRIPED_ERR_INVALID_ARG;
     int st = check_attn(B, H, S, D, N, layout, dtype);
     if (st) return st;
@@ -308,7 +372,8 @@ int striped_attn_bwd_gqa(const void *q, const void *k, const void *v, const void
     const size_t need = striped_workspace_size(B, H, S, D, N, dtype);
     if (!workspace || ws_bytes < need) return STRIPED_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return STRIPED_ERR_ALIGN;
-    const AttnGeom g = full_geom(B, H, Hkv, S, D, N, layout, scale);
+    AttnGeom g = full_geom(B, H, Hkv, S, D, N, layout, scale);
+    g.seqs = seqs;
     cudaStream_t s = (cudaStream_t)stream;
     if (dtype == STRIPED_FP32)
         return launch_simt_bwd((const float *)q, (const float *)k, (const float *)v, (const float *)o, lse,
@@ -317,6 +382,26 @@ int striped_attn_bwd_gqa(const void *q, const void *k, const void *v, const void
     float *dq_acc = (float *)workspace;
     float *stats = (float *)((char *)workspace + bf16_stats_offset(B, H, S, D));
     return launch_tc_bwd(q, k, v, o, lse, dO, dq, dk, dv, dq_acc, stats, g, tile_stats, s);
+}
+
+int striped_attn_bwd_gqa(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                         const void *dO, void *dq, void *dk, void *dv, void *workspace,
+                         size_t ws_bytes, int64_t B, int64_t H, int64_t Hkv, int64_t S, int64_t D, int N,
+                         int layout, int dtype, float scale, int64_t *tile_stats, void *stream) {
+    return attn_bwd_common(q, k, v, o, lse, dO, dq, dk, dv, workspace, ws_bytes, B, H, Hkv, S, D, N, layout,
+                           dtype, scale, tile_stats, stream, kDense);
+}
+
+int striped_attn_bwd_varlen(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                            const void *dO, void *dq, void *dk, void *dv, void *workspace, size_t ws_bytes,
+                            const int32_t *cu_seqlens, int nseq, int64_t H, int64_t Hkv, int64_t D, int N,
+                            int layout, int dtype, float scale, int64_t *tile_stats, void *stream) {
+    SeqTable t{};
+    int64_t S = 0;
+    const int st = make_seq_table(cu_seqlens, nseq, N, layout, tile_of(dtype), &t, &S);
+    if (st) return st;
+    return attn_bwd_common(q, k, v, o, lse, dO, dq, dk, dv, workspace, ws_bytes, 1, H, Hkv, S, D, N, layout,
+                           dtype, scale, tile_stats, stream, t);
 }
 
 int ring_round_fwd(const void *q_d, const void *k_e, const void *v_e, float *o_acc, float *lse_acc,
@@ -334,7 +419,7 @@ int ring_round_fwd(const void *q_d, const void *k_e, const void *v_e, float *o_a
         return STRIPED_ERR_ALIGN;
     const int64_t esize = dtype == STRIPED_BF16 ? 2 : 4;
     if ((stride_bh * esize) % 16 != 0 || (stride_bh * 4) % 16 != 0) return STRIPED_ERR_ALIGN;
-    AttnGeom g;
+    AttnGeom g{};  // seqs.n = 0: dense
     g.BH = B * H;
     g.G = 1;
     g.L = L;

@@ -133,6 +133,9 @@ __device__ __forceinline__ void qiter_next(QTileIter &it, int layout, int N, int
 }
 
 
+// kPacked: packed variable-length sequences (the sequence table is
+// consulted); the dense instantiation compiles the span as {0, nq}.
+template <bool kPacked>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -159,12 +162,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t per_head = (int64_t)nq * N;
     const int64_t bh = id / per_head;
     const int rem = (int)(id % per_head);
-    const int b = rem / N;
+    const int bg = rem / N;  // key tile in the slice of stripe e
     const int e = rem % N;
-    const int rows_b = tile_rows(g.L, b);
+    const int rows_b = tile_rows(g.L, bg);
+    // packed sequences: the key tile sees the query tiles of its own sequence
+    // only (tiles qbase .. qbase + nqs - 1 of every slice)
+    const SeqSpan sq = kPacked ? seq_of(g.seqs, bg, BT, nq) : SeqSpan{0, nq};
+    const int b = bg - sq.start;  // key tile inside the sequence
+    const int nqs = sq.count;
+    const int qbase = sq.start;
 
     int nt = 0;
-    for (int d = 0; d < N; ++d) nt += nq - query_span(g.layout, d, e, b, nq, rows_b).a_lo;
+    for (int d = 0; d < N; ++d) nt += nqs - query_span(g.layout, d, e, b, nqs, rows_b).a_lo;
     nt *= G;
 
     if (threadIdx.x == 0) {
@@ -185,8 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_barrier_init();
         if (p.tile_stats) {
             for (int d = 0; d < N; ++d) {
-                const QuerySpan sp = query_span(g.layout, d, e, b, nq, rows_b);
-                const int cnt = nq - sp.a_lo;
+                const QuerySpan sp = query_span(g.layout, d, e, b, nqs, rows_b);
+                const int cnt = nqs - sp.a_lo;
                 if (cnt == 0) continue;
                 const int rr = ring_round_of(d, e, N);
                 atomicAdd((unsigned long long *)&p.tile_stats[rr * N + d],
@@ -214,12 +223,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmdO);
         const uint32_t kb = smem_u32(&bars->kv_full);
         mbar_arrive_expect_tx(kb, 2 * kTile);
-        tma_load_4d(sbase + kKOff, &tmK, kb, 0, b * BT, e, (int)bh);
-        tma_load_4d(sbase + kKOff + kBox, &tmK, kb, 64, b * BT, e, (int)bh);
-        tma_load_4d(sbase + kVOff, &tmV, kb, 0, b * BT, e, (int)bh);
-        tma_load_4d(sbase + kVOff + kBox, &tmV, kb, 64, b * BT, e, (int)bh);
-        QTileIter it = qiter_begin(g.layout, N, G, e, b, nq, rows_b);
-        for (int i = 0; i < nt; ++i, qiter_next(it, g.layout, N, G, e, b, nq, rows_b)) {
+        tma_load_4d(sbase + kKOff, &tmK, kb, 0, bg * BT, e, (int)bh);
+        tma_load_4d(sbase + kKOff + kBox, &tmK, kb, 64, bg * BT, e, (int)bh);
+        tma_load_4d(sbase + kVOff, &tmV, kb, 0, bg * BT, e, (int)bh);
+        tma_load_4d(sbase + kVOff + kBox, &tmV, kb, 64, bg * BT, e, (int)bh);
+        QTileIter it = qiter_begin(g.layout, N, G, e, b, nqs, rows_b);
+        for (int i = 0; i < nt; ++i, qiter_next(it, g.layout, N, G, e, b, nqs, rows_b)) {
             const int s = i % QS;
             if (i >= QS && !mbar_wait(smem_u32(&bars->q_empty[s]), ((i / QS) + 1) & 1, p.err)) break;
             const uint32_t fb = smem_u32(&bars->q_full[s]);
@@ -227,24 +236,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t bq = bh * G + it.h;  // query head
             mbar_arrive_expect_tx(fb, kTile + kStatBytes);
             bulk_load(sbase + kStatOff + s * kStatBytes,
-                      p.stats + (((bq * N + it.d) * (int64_t)nq + it.a) << 8), kStatBytes, fb);
-            tma_load_4d(qdst, &tmQ, fb, 0, it.a * BT, it.d, (int)bq);
-            tma_load_4d(qdst + kBox, &tmQ, fb, 64, it.a * BT, it.d, (int)bq);
+                      p.stats + (((bq * N + it.d) * (int64_t)nq + qbase + it.a) << 8), kStatBytes, fb);
+            tma_load_4d(qdst, &tmQ, fb, 0, (qbase + it.a) * BT, it.d, (int)bq);
+            tma_load_4d(qdst + kBox, &tmQ, fb, 64, (qbase + it.a) * BT, it.d, (int)bq);
         }
     } else if (warp == 2 && lane == 0 && nt > 0) {
         // ---------------- TMA producer: dO_i (its own stream: the buffer is
         // released later than Q_i's, after the dQ_i half staged in it is read)
         tma_prefetch_desc(&tmdO);
-        QTileIter it = qiter_begin(g.layout, N, G, e, b, nq, rows_b);
-        for (int i = 0; i < nt; ++i, qiter_next(it, g.layout, N, G, e, b, nq, rows_b)) {
+        QTileIter it = qiter_begin(g.layout, N, G, e, b, nqs, rows_b);
+        for (int i = 0; i < nt; ++i, qiter_next(it, g.layout, N, G, e, b, nqs, rows_b)) {
             const int s = i % QS;
             if (i >= QS && !mbar_wait(smem_u32(&bars->do_empty[s]), ((i / QS) + 1) & 1, p.err)) break;
             const uint32_t fb = smem_u32(&bars->do_full[s]);
             const uint32_t odst = sbase + kQOff + s * 2 * kTile + kTile;
             const int bq = (int)(bh * G + it.h);
             mbar_arrive_expect_tx(fb, kTile);
-            tma_load_4d(odst, &tmdO, fb, 0, it.a * BT, it.d, bq);
-            tma_load_4d(odst + kBox, &tmdO, fb, 64, it.a * BT, it.d, bq);
+            tma_load_4d(odst, &tmdO, fb, 0, (qbase + it.a) * BT, it.d, bq);
+            tma_load_4d(odst + kBox, &tmdO, fb, 64, (qbase + it.a) * BT, it.d, bq);
         }
     } else if (warp == 1 && lane == 0 && nt > 0) {
         // ---------------- MMA issuer
@@ -373,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             return true;
         };
 
-        QTileIter cur = qiter_begin(g.layout, N, G, e, b, nq, rows_b);
+        QTileIter cur = qiter_begin(g.layout, N, G, e, b, nqs, rows_b);
         // warpgroup 1, lane 0: stage whose dQ bulk reduce still reads shared
         // memory (-1: none); the wait for it is deferred to the next tile
         int pending = -1;
@@ -424,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- P of the next tile while the tensor core runs dQ_i / dK_i
             const QTileIter done = cur;
             if (i + 1 < nt) {
-                qiter_next(cur, g.layout, N, G, e, b, nq, rows_b);
+                qiter_next(cur, g.layout, N, G, e, b, nqs, rows_b);
                 if (!compute_p(cur, i + 1)) {
                     ok = false;
                     break;
@@ -453,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = i % QS;
             const int64_t bq = bh * G + done.h;  // query head of tile i
             if (wg == 0) {
-                const int64_t qi = (int64_t)done.a * BT + row;
+                const int64_t qi = (int64_t)(qbase + done.a) * BT + row;
                 if (qi < g.L) {
                     float *dst =
                         p.dq_acc + (bq * g.stride_bh + (int64_t)done.d * g.stripe_stride + qi * HD + cbase);
@@ -483,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) {
                     const uint32_t wofs = (uint32_t)quarter * 32 * 128;
-                    const int r0 = done.a * BT + quarter * 32;
+                    const int r0 = (qbase + done.a) * BT + quarter * 32;
                     tma_reduce_add_4d(&tmdQ, stage + wofs, cbase, r0, done.d, (int)bq);
                     tma_reduce_add_4d(&tmdQ, stage + kBox + wofs, cbase + 32, r0, done.d, (int)bq);
                     bulk_commit_group();
@@ -498,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
         }
         // ---------------- epilogue: this warpgroup's columns of dK, dV
-        const int64_t kj = (int64_t)b * BT + row;
+        const int64_t kj = (int64_t)bg * BT + row;
         const int64_t krow = bh * g.stride_bh + (int64_t)e * g.stripe_stride + kj * HD + cbase;
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
@@ -615,8 +624,11 @@ int launch_tc_bwd(const void *q, const void *k, const void *v, const void *o, co
                   const AttnGeom &g, int64_t *tile_stats, cudaStream_t stream) {
     static int attr = 1;
     if (attr == 1) {
-        cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(tc_bwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemBytes);
         attr = cuda_status(e);
     }
     if (attr != STRIPED_OK) return attr;
@@ -647,7 +659,10 @@ int launch_tc_bwd(const void *q, const void *k, const void *v, const void *o, co
     const int64_t nk = (g.L + BT - 1) / BT;
     const int64_t nblocks = nk * g.N * bh_kv;  // one CTA per key tile of every key/value head
     if (nblocks > 0x7fffffffll) return STRIPED_ERR_UNSUPPORTED;
-    tc_bwd_kernel<<<(unsigned)nblocks, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, p);
+    if (g.seqs.n > 0)
+        tc_bwd_kernel<true><<<(unsigned)nblocks, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, p);
+    else
+        tc_bwd_kernel<false><<<(unsigned)nblocks, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, p);
     st = cuda_status(cudaGetLastError());
     if (st != STRIPED_OK) return st;
     bwd_post_kernel<<<sms * 8, 256, 0, stream>>>(dq_acc, (__nv_bfloat16 *)dq, rows * HD / 8, g.scale);

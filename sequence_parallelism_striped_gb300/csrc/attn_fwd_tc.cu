@@ -68,7 +68,9 @@ __device__ __forceinline__ int tile_rows(int64_t L, int t) {
     return r >= BM ? BM : (int)r;
 }
 
-template <bool kRound>
+// kPacked: packed variable-length sequences (the sequence table is
+// consulted); the dense instantiation compiles the span as {0, nq}.
+template <bool kRound, bool kPacked>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -81,10 +83,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
     const int nq = (int)((g.L + BM - 1) / BM);
-    int a, d;
+    int ag, d;  // ag: tile index in the device's slice
     int64_t bh;
     if (kRound) {
-        a = nq - 1 - (int)blockIdx.x;
+        ag = nq - 1 - (int)blockIdx.x;
         d = p.d_fixed;
         bh = blockIdx.y;
     } else {
@@ -95,11 +97,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t per_head = (int64_t)nq * g.N;
         bh = id / per_head;
         const int rem = (int)(id % per_head);
-        a = nq - 1 - rem / g.N;
+        ag = nq - 1 - rem / g.N;
         const int dd = rem % g.N;
         d = (g.layout == STRIPED_LAYOUT_CONTIGUOUS) ? g.N - 1 - dd : dd;
     }
-    const int rows_a = tile_rows(g.L, a);
+    const int rows_a = tile_rows(g.L, ag);
+    // packed sequences: the schedule works on tiles of the query tile's own
+    // sequence (tiles sq.start .. sq.start + nqs - 1 of every slice)
+    const SeqSpan sq = kPacked ? seq_of(g.seqs, ag, BM, nq) : SeqSpan{0, nq};
+    const int a = ag - sq.start;  // tile index inside the sequence
+    const int nqs = sq.count;
     const int nrounds = kRound ? 1 : g.N;
     const int e_fixed = p.e_fixed;
     // Key stripes are visited in the same global order e = 0..N-1 by every
@@ -111,7 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // number of key tiles this query tile visits
     int nt = 0;
     for (int r = 0; r < nrounds; ++r) {
-        const RoundSpan sp = round_span(g.layout, d, stripe_of(r), a, nq, rows_a);
+        const RoundSpan sp = round_span(g.layout, d, stripe_of(r), a, nqs, rows_a);
         nt += sp.nfull + sp.has_diag;
     }
 
@@ -129,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.tile_stats) {
             for (int r = 0; r < nrounds; ++r) {
                 const int e = stripe_of(r);
-                const RoundSpan sp = round_span(g.layout, d, e, a, nq, rows_a);
+                const RoundSpan sp = round_span(g.layout, d, e, a, nqs, rows_a);
                 if (sp.nfull + sp.has_diag == 0) continue;
                 const int rr = ring_round_of(d, e, g.N);
                 atomicAdd((unsigned long long *)&p.tile_stats[rr * g.N + d], (unsigned long long)sp.nfull);
@@ -157,17 +164,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmV);
         const uint32_t qb = smem_u32(&bars->q_full);
         mbar_arrive_expect_tx(qb, kTileBytes);
-        tma_load_4d(sbase + kQOff, &tmQ, qb, 0, a * BM, qstripe, (int)bh);
-        tma_load_4d(sbase + kQOff + kBoxBytes, &tmQ, qb, 64, a * BM, qstripe, (int)bh);
+        tma_load_4d(sbase + kQOff, &tmQ, qb, 0, ag * BM, qstripe, (int)bh);
+        tma_load_4d(sbase + kQOff + kBoxBytes, &tmQ, qb, 64, ag * BM, qstripe, (int)bh);
         int j = 0;
         bool ok = true;
         for (int r = 0; r < nrounds && ok; ++r) {
             const int e = stripe_of(r);
             const int kstripe = kRound ? 0 : e;
-            const RoundSpan sp = round_span(g.layout, d, e, a, nq, rows_a);
+            const RoundSpan sp = round_span(g.layout, d, e, a, nqs, rows_a);
             const int ntr = sp.nfull + sp.has_diag;
             for (int b = 0; b < ntr; ++b, ++j) {
                 const int s = j % NS;
+                const int kb = sq.start + b;  // key tile in the slice
                 if (j >= NS && !mbar_wait(smem_u32(&bars->kv_empty[s]), ((j / NS) + 1) & 1, p.err)) {
                     ok = false;
                     break;
@@ -176,10 +184,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t kdst = sbase + kKVOff + s * kStageBytes;
                 const uint32_t vdst = kdst + kTileBytes;
                 mbar_arrive_expect_tx(fb, 2 * kTileBytes);
-                tma_load_4d(kdst, &tmK, fb, 0, b * BN, kstripe, kvh);
-                tma_load_4d(kdst + kBoxBytes, &tmK, fb, 64, b * BN, kstripe, kvh);
-                tma_load_4d(vdst, &tmV, fb, 0, b * BN, kstripe, kvh);
-                tma_load_4d(vdst + kBoxBytes, &tmV, fb, 64, b * BN, kstripe, kvh);
+                tma_load_4d(kdst, &tmK, fb, 0, kb * BN, kstripe, kvh);
+                tma_load_4d(kdst + kBoxBytes, &tmK, fb, 64, kb * BN, kstripe, kvh);
+                tma_load_4d(vdst, &tmV, fb, 0, kb * BN, kstripe, kvh);
+                tma_load_4d(vdst + kBoxBytes, &tmV, fb, 64, kb * BN, kstripe, kvh);
             }
         }
     } else if (warp == 1 && lane == 0 && nt > 0) {
@@ -232,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int r = 0; r < nrounds && ok; ++r) {
             const int e = stripe_of(r);
-            const RoundSpan sp = round_span(g.layout, d, e, a, nq, rows_a);
+            const RoundSpan sp = round_span(g.layout, d, e, a, nqs, rows_a);
             const int ntr = sp.nfull + sp.has_diag;
             for (int b = 0; b < ntr; ++b, ++j) {
                 const uint32_t tS = ((j & 1) ? tS1 : tS0) + lane_off;
@@ -262,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 const bool diag = sp.has_diag && b == sp.nfull;
-                const int kv_valid = tile_rows(g.L, b);
+                const int kv_valid = tile_rows(g.L, sq.start + b);
                 if (diag || kv_valid < BN) {
                     const int lim = diag ? min(ri + sp.diag_off, kv_valid - 1) : kv_valid - 1;
 #pragma unroll
@@ -335,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = mbar_wait(smem_u32(&bars->o_done), (nt - 1) & 1, p.err);
             tc_fence_after();
         }
-        const int64_t i = (int64_t)a * BM + ri;
+        const int64_t i = (int64_t)ag * BM + ri;
         const bool valid_row = i < g.L;
         const bool empty = !(l > 0.f) || !ok;
         const float inv_l = empty ? 0.f : 1.f / l;
@@ -427,11 +435,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 static int set_smem_once() {
     static int status = 1;
     if (status == 1) {
-        cudaError_t e1 = cudaFuncSetAttribute(tc_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              (int)kSmemBytes);
-        cudaError_t e2 = cudaFuncSetAttribute(tc_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              (int)kSmemBytes);
-        status = (e1 == cudaSuccess && e2 == cudaSuccess) ? STRIPED_OK : cuda_status(e1 != cudaSuccess ? e1 : e2);
+        const cudaError_t e[3] = {
+            cudaFuncSetAttribute(tc_fwd_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemBytes),
+            cudaFuncSetAttribute(tc_fwd_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemBytes),
+            cudaFuncSetAttribute(tc_fwd_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemBytes)};
+        status = STRIPED_OK;
+        for (cudaError_t x : e)
+            if (x != cudaSuccess) status = cuda_status(x);
     }
     return status;
 }
@@ -455,7 +468,10 @@ int launch_tc_fwd(const void *q, const void *k, const void *v, void *o, float *l
     const int64_t nq = (g.L + BM - 1) / BM;
     const int64_t nblocks = nq * g.N * g.BH;
     if (nblocks > 0x7fffffffll) return STRIPED_ERR_UNSUPPORTED;
-    tc_fwd_kernel<false><<<(unsigned)nblocks, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+    if (g.seqs.n > 0)
+        tc_fwd_kernel<false, true><<<(unsigned)nblocks, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+    else
+        tc_fwd_kernel<false, false><<<(unsigned)nblocks, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
     return cuda_status(cudaGetLastError());
 }
 
@@ -486,7 +502,7 @@ int launch_tc_round(const void *q_d, const void *k_e, const void *v_e, float *o_
     const int64_t nq = (g.L + BM - 1) / BM;
     if (g.BH > 65535) return STRIPED_ERR_UNSUPPORTED;
     dim3 grid((unsigned)nq, (unsigned)g.BH);
-    tc_fwd_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+    tc_fwd_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
     return cuda_status(cudaGetLastError());
 }
 

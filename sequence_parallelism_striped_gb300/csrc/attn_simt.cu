@@ -53,18 +53,21 @@ struct RowState {
     float acc[kMaxDPT];
 };
 
-// Online-softmax forward of query tile a of stripe d over rounds
-// [r_lo, r_hi) (e_fixed >= 0: the single key stripe e_fixed).
+// Online-softmax forward of query tile ag of stripe d over rounds
+// [r_lo, r_hi) (e_fixed >= 0: the single key stripe e_fixed).  With packed
+// sequences the schedule runs over the tiles of ag's own sequence.
 __device__ void fwd_tile(const float *__restrict__ q_stripe, const float *__restrict__ k_head,
-                         const float *__restrict__ v_head, const AttnGeom &g, int d, int a, int r_lo,
+                         const float *__restrict__ v_head, const AttnGeom &g, int d, int ag, int r_lo,
                          int r_hi, int e_fixed, RowState &st, int64_t *tile_stats, float *sK,
                          float *sV) {
     const int64_t L = g.L, D = g.D;
     const int dpt = (int)D / kTPR;
     const int row = threadIdx.x / kTPR, sub = threadIdx.x % kTPR;
     const int nq = (int)((L + T - 1) / T);
-    const int rows_a = rows_in_tile(L, a);
-    const int64_t i = (int64_t)a * T + row;
+    const int rows_a = rows_in_tile(L, ag);
+    const int64_t i = (int64_t)ag * T + row;
+    const SeqSpan sq = seq_of(g.seqs, ag, T, nq);
+    const int a = ag - sq.start, nqs = sq.count;
     float qreg[kMaxDPT];
 #pragma unroll
     for (int c = 0; c < kMaxDPT; ++c)
@@ -76,7 +79,7 @@ __device__ void fwd_tile(const float *__restrict__ q_stripe, const float *__rest
 
     for (int r = r_lo; r < r_hi; ++r) {
         const int e = e_fixed >= 0 ? e_fixed : (d - r + g.N) % g.N;
-        const RoundSpan sp = round_span(g.layout, d, e, a, nq, rows_a);
+        const RoundSpan sp = round_span(g.layout, d, e, a, nqs, rows_a);
         const int ntiles = sp.nfull + sp.has_diag;
         if (tile_stats && threadIdx.x == 0 && ntiles > 0) {
             const int rr = ring_round_of(d, e, g.N);
@@ -88,10 +91,10 @@ __device__ void fwd_tile(const float *__restrict__ q_stripe, const float *__rest
         const float *v_stripe = v_head + (int64_t)e * g.stripe_stride;
         for (int b = 0; b < ntiles; ++b) {
             __syncthreads();
-            stage_rows(sK, k_stripe, L, D, b);
-            stage_rows(sV, v_stripe, L, D, b);
+            stage_rows(sK, k_stripe, L, D, sq.start + b);
+            stage_rows(sV, v_stripe, L, D, sq.start + b);
             __syncthreads();
-            const int rows_b = rows_in_tile(L, b);
+            const int rows_b = rows_in_tile(L, sq.start + b);
             const bool diag = sp.has_diag && b == sp.nfull;
             for (int c = 0; c < rows_b; ++c) {
                 float part = 0.f;
@@ -209,13 +212,15 @@ __global__ void __launch_bounds__(kThreads) simt_dq_kernel(
     float *sK = smem, *sV = smem + T * g.D;
     const int64_t L = g.L, D = g.D;
     const int nq = (int)((L + T - 1) / T);
-    const int a = nq - 1 - (int)(blockIdx.x % nq);
+    const int ag = nq - 1 - (int)(blockIdx.x % nq);
     const int d = (int)(blockIdx.x / nq);
     const int64_t bh = blockIdx.y;
     const int dpt = (int)D / kTPR;
     const int row = threadIdx.x / kTPR, sub = threadIdx.x % kTPR;
-    const int64_t i = (int64_t)a * T + row;
+    const int64_t i = (int64_t)ag * T + row;
     const bool valid = i < L;
+    const SeqSpan sq = seq_of(g.seqs, ag, T, nq);  // packed sequences: own sequence's tiles
+    const int a = ag - sq.start, nqs = sq.count;
     const int64_t qoff = bh * g.stride_bh + (int64_t)d * g.stripe_stride + i * D + sub * dpt;
     const int64_t soff = bh * g.lse_stride_bh + (int64_t)d * g.lse_stripe_stride + i;
     float qreg[kMaxDPT], doreg[kMaxDPT], acc[kMaxDPT];
@@ -227,10 +232,10 @@ __global__ void __launch_bounds__(kThreads) simt_dq_kernel(
     }
     const float lse_i = valid ? lse[soff] : 0.f;
     const float delta_i = valid ? delta[soff] : 0.f;
-    const int rows_a = rows_in_tile(L, a);
+    const int rows_a = rows_in_tile(L, ag);
     for (int r = 0; r < g.N; ++r) {
         const int e = (d - r + g.N) % g.N;
-        const RoundSpan sp = round_span(g.layout, d, e, a, nq, rows_a);
+        const RoundSpan sp = round_span(g.layout, d, e, a, nqs, rows_a);
         const int ntiles = sp.nfull + sp.has_diag;
         if (tile_stats && threadIdx.x == 0 && ntiles > 0) {
             atomicAdd((unsigned long long *)&tile_stats[r * g.N + d], (unsigned long long)sp.nfull);
@@ -241,10 +246,10 @@ __global__ void __launch_bounds__(kThreads) simt_dq_kernel(
         const float *v_stripe = v + (bh / g.G) * g.stride_bh + (int64_t)e * g.stripe_stride;
         for (int b = 0; b < ntiles; ++b) {
             __syncthreads();
-            stage_rows(sK, k_stripe, L, D, b);
-            stage_rows(sV, v_stripe, L, D, b);
+            stage_rows(sK, k_stripe, L, D, sq.start + b);
+            stage_rows(sV, v_stripe, L, D, sq.start + b);
             __syncthreads();
-            const int rows_b = rows_in_tile(L, b);
+            const int rows_b = rows_in_tile(L, sq.start + b);
             const bool diag = sp.has_diag && b == sp.nfull;
             for (int c = 0; c < rows_b; ++c) {
                 float ps = 0.f, pp = 0.f;
@@ -282,12 +287,14 @@ __global__ void __launch_bounds__(kThreads) simt_dkdv_kernel(
     float *sL = smem + 2 * T * g.D, *sDel = sL + T;
     const int64_t L = g.L, D = g.D;
     const int nq = (int)((L + T - 1) / T);
-    const int b = nq - 1 - (int)(blockIdx.x % nq);
+    const int bg = nq - 1 - (int)(blockIdx.x % nq);
     const int e = (int)(blockIdx.x / nq);
     const int64_t bh = blockIdx.y;
     const int dpt = (int)D / kTPR;
     const int row = threadIdx.x / kTPR, sub = threadIdx.x % kTPR;  // key row in the tile
-    const int64_t j = (int64_t)b * T + row;
+    const int64_t j = (int64_t)bg * T + row;
+    const SeqSpan sq = seq_of(g.seqs, bg, T, nq);  // packed sequences: own sequence's tiles
+    const int b = bg - sq.start, nqs = sq.count;
     const bool valid = j < L;
     const int64_t koff = bh * g.stride_bh + (int64_t)e * g.stripe_stride + j * D + sub * dpt;
     float kreg[kMaxDPT], vreg[kMaxDPT], ak[kMaxDPT], av[kMaxDPT];
@@ -297,25 +304,26 @@ __global__ void __launch_bounds__(kThreads) simt_dkdv_kernel(
         vreg[u] = (u < dpt && valid) ? v[koff + u] : 0.f;
         ak[u] = av[u] = 0.f;
     }
-    const int rows_b = rows_in_tile(L, b);
+    const int rows_b = rows_in_tile(L, bg);
     for (int hr = 0; hr < g.G * g.N; ++hr) {
         const int64_t bq = bh * g.G + hr / g.N;  // query head
         const int r = (int)(hr % g.N);
         const int d = (e + r) % g.N;
-        const QuerySpan sp = query_span(g.layout, d, e, b, nq, rows_b);
+        const QuerySpan sp = query_span(g.layout, d, e, b, nqs, rows_b);
         const float *q_stripe = q + bq * g.stride_bh + (int64_t)d * g.stripe_stride;
         const float *do_stripe = dO + bq * g.stride_bh + (int64_t)d * g.stripe_stride;
         const float *l_stripe = lse + bq * g.lse_stride_bh + (int64_t)d * g.lse_stripe_stride;
         const float *dl_stripe = delta + bq * g.lse_stride_bh + (int64_t)d * g.lse_stripe_stride;
-        for (int a = sp.a_lo; a < nq; ++a) {
+        for (int a = sp.a_lo; a < nqs; ++a) {
+            const int ag = sq.start + a;  // query tile in the slice
             __syncthreads();
-            stage_rows(sQ, q_stripe, L, D, a);
-            stage_rows(sdO, do_stripe, L, D, a);
-            const int rows_a = rows_in_tile(L, a);
+            stage_rows(sQ, q_stripe, L, D, ag);
+            stage_rows(sdO, do_stripe, L, D, ag);
+            const int rows_a = rows_in_tile(L, ag);
             if (threadIdx.x < T) {
-                sL[threadIdx.x] = threadIdx.x < rows_a ? l_stripe[(int64_t)a * T + threadIdx.x] : 0.f;
+                sL[threadIdx.x] = threadIdx.x < rows_a ? l_stripe[(int64_t)ag * T + threadIdx.x] : 0.f;
                 sDel[threadIdx.x] =
-                    threadIdx.x < rows_a ? dl_stripe[(int64_t)a * T + threadIdx.x] : 0.f;
+                    threadIdx.x < rows_a ? dl_stripe[(int64_t)ag * T + threadIdx.x] : 0.f;
             }
             __syncthreads();
             const bool diag = sp.has_diag && a == sp.a_lo;

@@ -145,6 +145,27 @@ __host__ __device__ __forceinline__ QuerySpan query_span(int layout, int d, int 
     return s;
 }
 
+// The packed sequence holding tile (or row) x of a device's slice, in units
+// of `unit` rows: its first unit and its length in units.  A dense launch
+// (table size 0) is one sequence of `total` units.  Binary search over the
+// table in the kernel parameters (uniform across the CTA).
+struct SeqSpan {
+    int start, count;
+};
+
+template <typename Table>
+__device__ __forceinline__ SeqSpan seq_of(const Table &t, int x, int unit, int total) {
+    if (t.n == 0) return SeqSpan{0, total};
+    int lo = 0, hi = t.n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (t.row_start[mid] / unit <= x) lo = mid;
+        else hi = mid - 1;
+    }
+    const int s0 = t.row_start[lo] / unit;
+    return SeqSpan{s0, t.row_start[lo + 1] / unit - s0};
+}
+
 __host__ __device__ __forceinline__ int ring_round_of(int d, int e, int N) {
     return ((d - e) % N + N) % N;
 }

@@ -22,6 +22,16 @@ int *device_error_word();
 // [BH][N stripes][L rows][D] with stripe e of head bh starting at element
 // bh*stride_bh + e*stripe_stride (stripe_stride = L*D for full tensors,
 // 0 when the pointers are already the stripe slices of one round).
+// Packed variable-length batches: the sequences of one packed head, as the
+// first row of each inside every device's slice (row_start[i] =
+// cu_seqlens[i] / N, row_start[n] = L).  n = 0 means one sequence per
+// (batch, head), the dense case.  Carried by value in the kernel parameters.
+constexpr int kMaxSeqs = 512;
+struct SeqTable {
+    int n;
+    int row_start[kMaxSeqs + 1];
+};
+
 // Grouped-query attention: query head bh (of B*H) reads key/value head
 // bh / G (of B*H/G), i.e. G consecutive query heads share one; G = 1 is
 // plain multi-head attention.
@@ -35,11 +45,12 @@ struct AttnGeom {
     int64_t lse_stride_bh;      // elements between heads of lse
     int64_t lse_stripe_stride;  // elements between stripes of lse
     float scale;
+    SeqTable seqs;              // packed sequences (seqs.n == 0: dense)
 };
 
 // ---- permute.cu
 int launch_stripe_permute(const void *x, void *y, int64_t BH, int64_t S, int64_t row_bytes, int N,
-                          int layout, bool gather, cudaStream_t stream);
+                          int layout, bool gather, const SeqTable &seqs, cudaStream_t stream);
 
 // ---- attn_simt.cu (fp32 CUDA-core path, tile edge kSimtTile)
 constexpr int kSimtTile = 16;

@@ -10,7 +10,9 @@
 //
 // The same kernel serves the other row orders with their own row -> position
 // map: contiguous (position d*L + i, a copy) and zig-zag (device d holds
-// chunk d then chunk 2N-1-d of 2N chunks of C = L/2 positions).
+// chunk d then chunk 2N-1-d of 2N chunks of C = L/2 positions), and packed
+// variable-length batches, where each sequence is placed on its own and a
+// device's slice holds its rows of every sequence in turn.
 //
 // One block moves a run of consecutive stripe rows of one (b, h) head; the
 // stripe index d is uniform per block (no per-element division).  Each row
@@ -35,10 +37,20 @@ __device__ __forceinline__ int64_t position_of(int64_t d, int64_t i, int64_t L, 
     return i * N + d;
 }
 
+// Position of row i of device d's slice in a packed head: the row's
+// sequence (its first row sq.start in the slice, sq.count rows per device)
+// starts at position sq.start * N.
+template <int kLayout>
+__device__ __forceinline__ int64_t packed_position_of(const SeqTable &seqs, int64_t d, int64_t i, int64_t L, int N) {
+    if (seqs.n == 0) return position_of<kLayout>(d, i, L, N);
+    const SeqSpan sq = seq_of(seqs, (int)i, 1, (int)L);
+    return (int64_t)sq.start * N + position_of<kLayout>(d, i - sq.start, sq.count, N);
+}
+
 template <int kLayout, bool kGather>
 __global__ void __launch_bounds__(kPermThreads) stripe_permute_kernel(
     const uint4 *__restrict__ x, uint4 *__restrict__ y, int64_t S, int64_t L, int N, int vec_per_row_log2,
-    int rows_per_block, int blocks_per_stripe) {
+    int rows_per_block, int blocks_per_stripe, const __grid_constant__ SeqTable seqs) {
     const int64_t bh = blockIdx.y;
     const int d = blockIdx.x / blocks_per_stripe;
     const int64_t i0 = (int64_t)(blockIdx.x % blocks_per_stripe) * rows_per_block;
@@ -57,7 +69,7 @@ __global__ void __launch_bounds__(kPermThreads) stripe_permute_kernel(
             const int c = v & (vpr - 1);
             if (i < L) {
                 const int64_t striped_row = head + (int64_t)d * L + i;
-                const int64_t pos_row = head + position_of<kLayout>(d, i, L, N);
+                const int64_t pos_row = head + packed_position_of<kLayout>(seqs, d, i, L, N);
                 const int64_t src = (kGather ? pos_row : striped_row) * vpr + c;
                 dst_idx[u] = (kGather ? striped_row : pos_row) * vpr + c;
                 buf[u] = __ldg(x + src);
@@ -71,17 +83,17 @@ __global__ void __launch_bounds__(kPermThreads) stripe_permute_kernel(
 
 template <int kLayout>
 static void launch_layout(dim3 grid, cudaStream_t stream, bool gather, const void *x, void *y, int64_t S,
-                          int64_t L, int N, int vlog, int rows_per_block, int bps) {
+                          int64_t L, int N, int vlog, int rows_per_block, int bps, const SeqTable &seqs) {
     if (gather)
         stripe_permute_kernel<kLayout, true><<<grid, kPermThreads, 0, stream>>>(
-            (const uint4 *)x, (uint4 *)y, S, L, N, vlog, rows_per_block, bps);
+            (const uint4 *)x, (uint4 *)y, S, L, N, vlog, rows_per_block, bps, seqs);
     else
         stripe_permute_kernel<kLayout, false><<<grid, kPermThreads, 0, stream>>>(
-            (const uint4 *)x, (uint4 *)y, S, L, N, vlog, rows_per_block, bps);
+            (const uint4 *)x, (uint4 *)y, S, L, N, vlog, rows_per_block, bps, seqs);
 }
 
 int launch_stripe_permute(const void *x, void *y, int64_t BH, int64_t S, int64_t row_bytes, int N,
-                          int layout, bool gather, cudaStream_t stream) {
+                          int layout, bool gather, const SeqTable &seqs, cudaStream_t stream) {
     const int64_t L = S / N;
     const int64_t vpr = row_bytes / 16;
     int vlog = 0;
@@ -93,12 +105,14 @@ int launch_stripe_permute(const void *x, void *y, int64_t BH, int64_t S, int64_t
     if (bps * N > 0x7fffffffll || BH > 65535) return STRIPED_ERR_UNSUPPORTED;
     dim3 grid((unsigned)(bps * N), (unsigned)BH);
     if (layout == STRIPED_LAYOUT_ZIGZAG)
-        launch_layout<STRIPED_LAYOUT_ZIGZAG>(grid, stream, gather, x, y, S, L, N, vlog, rows_per_block, (int)bps);
+        launch_layout<STRIPED_LAYOUT_ZIGZAG>(grid, stream, gather, x, y, S, L, N, vlog, rows_per_block, (int)bps,
+                                             seqs);
     else if (layout == STRIPED_LAYOUT_CONTIGUOUS)
         launch_layout<STRIPED_LAYOUT_CONTIGUOUS>(grid, stream, gather, x, y, S, L, N, vlog, rows_per_block,
-                                                 (int)bps);
+                                                 (int)bps, seqs);
     else
-        launch_layout<STRIPED_LAYOUT_STRIPED>(grid, stream, gather, x, y, S, L, N, vlog, rows_per_block, (int)bps);
+        launch_layout<STRIPED_LAYOUT_STRIPED>(grid, stream, gather, x, y, S, L, N, vlog, rows_per_block, (int)bps,
+                                              seqs);
     return cuda_status(cudaGetLastError());
 }
 

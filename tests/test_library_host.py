@@ -118,6 +118,25 @@ def test_invalid_arguments_rejected_on_host(lib):
                                     None) == -1
     assert lib.striped_attn_bwd_gqa(fake, fake, fake, fake, fake, fake, fake, fake, fake, fake, 1 << 30, 1, 4, 8,
                                     64, 128, 4, 0, 0, 1.0, None, None) == -1
+    # packed sequences: cu_seqlens checked on the host
+    def cu(vals):
+        arr = (ctypes.c_int32 * len(vals))(*vals)
+        return arr, len(vals) - 1
+
+    def fwd_varlen(vals, N=4, layout=0, dtype=0):
+        arr, n = cu(vals)
+        return lib.striped_attn_fwd_varlen(fake, fake, fake, fake, fake, arr, n, 2, 2, 128, N, layout, dtype, 1.0,
+                                           None, None)
+
+    assert fwd_varlen([1, 512, 1024]) == -1           # does not start at 0
+    assert fwd_varlen([0, 1024, 512]) == -1           # decreasing
+    assert fwd_varlen([0, 512, 514]) == -1            # length not a multiple of N
+    assert fwd_varlen([0, 512, 516]) == -2            # multiple of N, not of N*T
+    assert fwd_varlen([0, 512, 1024], layout=2) == -2  # zig-zag: 512 is not a multiple of 2N*T
+    assert fwd_varlen([0, 512, 1028], layout=2) == -1  # zig-zag: not a multiple of 2N
+    assert fwd_varlen(list(range(0, 513 * 512 + 1, 512))) == -2  # more than 512 sequences
+    arr, n = cu([0, 6, 12])
+    assert lib.striped_varlen_permute(fake, P(1 << 24), arr, n, 1, 64, 4, 2, 0, None) == -1
 
 
 def test_workspace_size(lib):
