@@ -190,8 +190,9 @@ def _time_rounds(sp, torch, q, k, v, o_acc, lse_acc, N, layout, B, H, S, D, step
 
 def short_sequence_report(sp, torch, dev):
     """Short-sequence regime (B=1, H=8, S=8192, D=128, N=8): batched
-    fwd+bwd per placement, batched and per-round forward, each step timed
-    alone with the L2 flushed (a 256 MB write) before it; medians of 20."""
+    fwd+bwd per placement, batched and per-round forward (eager, and its
+    N*N launches replayed from one CUDA graph), each step timed alone with
+    the L2 flushed (a 256 MB write) before it; medians of 20."""
     from seeded_inputs import device_inputs
 
     B, H, S, D, N = 1, 8, 8192, 128, 8
@@ -234,9 +235,20 @@ def short_sequence_report(sp, torch, dev):
                     sp.ring_round_fwd(q, k, v, o_acc, lse_acc, d, (d - r) % N, N, layout, first_round=(r == 0))
 
         t_fb, t_f, t_r = timed(fwd_bwd), timed(fwd), timed(rounds)
+        # the same N*N launches captured once in a CUDA graph and replayed
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                rounds()
+        torch.cuda.current_stream().wait_stream(side)
+        t_g = timed(graph.replay)
+        del graph
         out[lname] = {"fwd_bwd_ms": t_fb, "fwd_bwd_tflops": _flops(B, H, S, D, 14) / (t_fb / 1e3) / 1e12,
                       "fwd_ms": t_f, "fwd_tflops": _flops(B, H, S, D, 4) / (t_f / 1e3) / 1e12,
                       "per_round_fwd_ms": t_r, "per_round_launches": N * N,
+                      "per_round_fwd_graph_ms": t_g,
                       "critical_path_tiles": sp.critical_path(S, N, 128, 128, layout),
                       "total_tiles": int(sum(t.sum() for t in sp.tile_counts(S, N, 128, 128, layout)))}
     return out

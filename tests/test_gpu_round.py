@@ -85,3 +85,47 @@ def test_single_round_partial_matches_oracle_keyset():
         fin = np.isfinite(lse_ref)
         assert np.array_equal(np.isfinite(got_l), fin)
         assert maxerr(got_l[fin], lse_ref[fin]) <= 1e-3
+
+
+def test_rounds_captured_in_a_cuda_graph():
+    """The per-round path is launch-bound at short sequences; its N x N
+    ring_round_fwd launches can be captured in one CUDA graph (the library
+    launches only on the caller's stream and its one-time set-up runs on the
+    first, eager call).  Replaying the graph reproduces the eager result
+    exactly, including on new inputs copied into the captured buffers."""
+    B, H, S, D, N = 1, 4, 8192, 128, 8
+    x = inputs(B, H, S, D, torch.bfloat16, seed=9, with_do=False)
+    q, k, v = (to_layout(x[n], N, sp.STRIPED, DEV) for n in ("q", "k", "v"))
+    o_acc = torch.empty(B, H, S, D, dtype=torch.float32, device=DEV)
+    lse_acc = torch.empty(B, H, S, dtype=torch.float32, device=DEV)
+
+    def rounds():
+        for r in range(N):
+            for d in range(N):
+                sp.ring_round_fwd(q, k, v, o_acc, lse_acc, d, (d - r) % N, N, sp.STRIPED, first_round=(r == 0))
+
+    rounds()  # eager: one-time set-up, reference result
+    torch.cuda.synchronize()
+    o_ref, l_ref = o_acc.clone(), lse_acc.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            rounds()
+    torch.cuda.current_stream().wait_stream(s)
+    o_acc.zero_()
+    lse_acc.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert sp.check_error() == 0
+    assert torch.equal(o_acc, o_ref) and torch.equal(lse_acc, l_ref)
+    # new inputs through the same captured buffers
+    y = inputs(B, H, S, D, torch.bfloat16, seed=10, with_do=False)
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        t.copy_(to_layout(y[n], N, sp.STRIPED, DEV))
+    graph.replay()
+    rounds_out = (o_acc.clone(), lse_acc.clone())
+    rounds()
+    torch.cuda.synchronize()
+    assert torch.equal(rounds_out[0], o_acc) and torch.equal(rounds_out[1], lse_acc)
