@@ -9,11 +9,15 @@
 // abstract) -- here by an online softmax with a log-sum-exp accumulator.
 //
 // One CTA = one 128-row query tile of one (b, h, stripe):
-//   warp 0      TMA producer: Q once, then K/V tiles into a 3-stage ring
+//   warp 0      TMA producer: K/V tiles into a 3-stage ring
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
 //   warps 2..5  softmax + epilogue; thread t owns query row t (TMEM lane t)
-// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O [256,384).
-//   S_j = Q K_j^T            (SS MMA, both K-major, M=N=128, K=16 x 8)
+//               and first stores that row of Q into TMEM
+// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O [256,384),
+// Q [384,448) as bf16 pairs.
+//   S_j = Q K_j^T            (TS MMA: A = Q from TMEM, B = K K-major;
+//                             M=N=128, K=16 x 8), so the tensor core reads
+//                             only K from shared memory for it
 //   P_j = exp2(S_j*c - m) written back over S_j as bf16 (64 columns)
 //   O  += P_j V_j            (TS MMA: A = P from TMEM, B = V MN-major)
 // S is double-buffered so S_{j+1} runs on the tensor core while the softmax
@@ -33,8 +37,7 @@ constexpr int BM = 128, BN = 128, HD = 128;
 constexpr int NS = 3;                       // K/V stages
 constexpr uint32_t kBoxBytes = 128 * 128;   // 128 rows x 64 bf16
 constexpr uint32_t kTileBytes = 2 * kBoxBytes;  // 128 x 128 bf16 = 32 KB
-constexpr uint32_t kQOff = 0;
-constexpr uint32_t kKVOff = kTileBytes;
+constexpr uint32_t kKVOff = 0;
 constexpr uint32_t kStageBytes = 2 * kTileBytes;  // K + V
 constexpr uint32_t kBarOff = kKVOff + NS * kStageBytes;
 constexpr size_t kSmemBytes = 1024 + kBarOff + 256;
@@ -44,6 +47,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct FwdParams {
     AttnGeom g;
+    const __nv_bfloat16 *q;       // queries (batched: full tensor; round mode: the stripe slice)
     int d_fixed, e_fixed, first;  // single-round mode only
     __nv_bfloat16 *o;             // batched: output
     float *lse;                   // batched: output
@@ -72,8 +76,8 @@ __device__ __forceinline__ int tile_rows(int64_t L, int t) {
 // consulted); the dense instantiation compiles the span as {0, nq}.
 template <bool kRound, bool kPacked>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+    tc_fwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const FwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
@@ -123,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (threadIdx.x == 0) {
-        mbar_init(smem_u32(&bars->q_full), 1);
+        mbar_init(smem_u32(&bars->q_full), 4);  // the four softmax warps stored Q in TMEM
         for (int s = 0; s < NS; ++s) {
             mbar_init(smem_u32(&bars->kv_full[s]), 1);
             mbar_init(smem_u32(&bars->kv_empty[s]), 1);
@@ -153,19 +157,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_slot;
-    const uint32_t tS0 = tmem, tS1 = tmem + 128, tO = tmem + 256;
+    const uint32_t tS0 = tmem, tS1 = tmem + 128, tO = tmem + 256, tQ = tmem + 384;
 
     const int qstripe = kRound ? 0 : d;
     const int kvh = (int)(bh / g.G);  // key/value head read by query head bh
     if (warp == 0 && lane == 0 && nt > 0) {
         // ---------------- TMA producer
-        tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
-        const uint32_t qb = smem_u32(&bars->q_full);
-        mbar_arrive_expect_tx(qb, kTileBytes);
-        tma_load_4d(sbase + kQOff, &tmQ, qb, 0, ag * BM, qstripe, (int)bh);
-        tma_load_4d(sbase + kQOff + kBoxBytes, &tmQ, qb, 64, ag * BM, qstripe, (int)bh);
         int j = 0;
         bool ok = true;
         for (int r = 0; r < nrounds && ok; ++r) {
@@ -205,8 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk) {
                 const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-                mma_ss(dS, sdesc_sw128(sbase + kQOff + off, 16, 1024), sdesc_sw128(kaddr + off, 16, 1024),
-                       idesc_qk, kk > 0 ? 1u : 0u);
+                mma_ts(dS, tQ + kk * 8, sdesc_sw128(kaddr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
             }
             mma_commit(smem_u32(&bars->s_full[t & 1]));
             return true;
@@ -235,6 +233,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ri = quarter * 32 + lane;  // query row of the tile
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const float cl2 = g.scale * 1.4426950408889634f;  // scores -> log2 units
+        if (nt > 0) {
+            // Q row ri -> TMEM columns [tQ, tQ + 64) as bf16 pairs: the A
+            // operand of every S = Q K^T, so the tensor core reads only K
+            // from shared memory for it
+            const int64_t qrow = (int64_t)ag * BM + ri;
+            uint32_t qa[32], qb[32];
+            if (qrow < g.L) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    p.q + bh * g.stride_bh + (int64_t)qstripe * g.stripe_stride + qrow * HD);
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    const uint4 w0 = __ldg(src + v), w1 = __ldg(src + 8 + v);
+                    qa[4 * v] = w0.x, qa[4 * v + 1] = w0.y, qa[4 * v + 2] = w0.z, qa[4 * v + 3] = w0.w;
+                    qb[4 * v] = w1.x, qb[4 * v + 1] = w1.y, qb[4 * v + 2] = w1.z, qb[4 * v + 3] = w1.w;
+                }
+            } else {
+#pragma unroll
+                for (int u = 0; u < 32; ++u) qa[u] = qb[u] = 0u;
+            }
+            tmem_st32(tQ + lane_off, qa);
+            tmem_st32(tQ + lane_off + 32, qb);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->q_full));
+        }
         float m_ref = -INFINITY, l = 0.f;
         int j = 0;
         bool ok = true;
@@ -453,14 +477,14 @@ int launch_tc_fwd(const void *q, const void *k, const void *v, void *o, float *l
                   const AttnGeom &g, int64_t *tile_stats, cudaStream_t stream) {
     int st = set_smem_once();
     if (st != STRIPED_OK) return st;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mk, mv;
     const int64_t bh_kv = g.BH / g.G;
-    if ((st = make_bf16_map(&mq, q, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 128)) ||
-        (st = make_bf16_map(&mk, k, g.D, g.L, g.N, bh_kv, g.stripe_stride, g.stride_bh, 128)) ||
+    if ((st = make_bf16_map(&mk, k, g.D, g.L, g.N, bh_kv, g.stripe_stride, g.stride_bh, 128)) ||
         (st = make_bf16_map(&mv, v, g.D, g.L, g.N, bh_kv, g.stripe_stride, g.stride_bh, 128)))
         return st;
     FwdParams p{};
     p.g = g;
+    p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
     p.o = reinterpret_cast<__nv_bfloat16 *>(o);
     p.lse = lse;
     p.tile_stats = tile_stats;
@@ -469,9 +493,9 @@ int launch_tc_fwd(const void *q, const void *k, const void *v, void *o, float *l
     const int64_t nblocks = nq * g.N * g.BH;
     if (nblocks > 0x7fffffffll) return STRIPED_ERR_UNSUPPORTED;
     if (g.seqs.n > 0)
-        tc_fwd_kernel<false, true><<<(unsigned)nblocks, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+        tc_fwd_kernel<false, true><<<(unsigned)nblocks, kThreads, kSmemBytes, stream>>>(mk, mv, p);
     else
-        tc_fwd_kernel<false, false><<<(unsigned)nblocks, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+        tc_fwd_kernel<false, false><<<(unsigned)nblocks, kThreads, kSmemBytes, stream>>>(mk, mv, p);
     return cuda_status(cudaGetLastError());
 }
 
@@ -480,14 +504,14 @@ int launch_tc_round(const void *q_d, const void *k_e, const void *v_e, float *o_
                     cudaStream_t stream) {
     int st = set_smem_once();
     if (st != STRIPED_OK) return st;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mk, mv;
     // the slices are single stripes: a stripe dimension of extent 1
-    if ((st = make_bf16_map(&mq, q_d, g.D, g.L, 1, g.BH, g.L * g.D, g.stride_bh, 128)) ||
-        (st = make_bf16_map(&mk, k_e, g.D, g.L, 1, g.BH, g.L * g.D, g.stride_bh, 128)) ||
+    if ((st = make_bf16_map(&mk, k_e, g.D, g.L, 1, g.BH, g.L * g.D, g.stride_bh, 128)) ||
         (st = make_bf16_map(&mv, v_e, g.D, g.L, 1, g.BH, g.L * g.D, g.stride_bh, 128)))
         return st;
     FwdParams p{};
     p.g = g;
+    p.q = reinterpret_cast<const __nv_bfloat16 *>(q_d);
     p.g.G = 1;
     p.g.stripe_stride = 0;
     p.g.lse_stripe_stride = 0;
@@ -502,7 +526,7 @@ int launch_tc_round(const void *q_d, const void *k_e, const void *v_e, float *o_
     const int64_t nq = (g.L + BM - 1) / BM;
     if (g.BH > 65535) return STRIPED_ERR_UNSUPPORTED;
     dim3 grid((unsigned)nq, (unsigned)g.BH);
-    tc_fwd_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+    tc_fwd_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(mk, mv, p);
     return cuda_status(cudaGetLastError());
 }
 
