@@ -254,6 +254,55 @@ def short_sequence_report(sp, torch, dev):
     return out
 
 
+def variants_report(sp, torch, dev, x, B, H, S, D, N):
+    """Grouped-query attention (Hkv = H/4) and a packed batch (8 sequences
+    of S/8 tokens in one head dimension) at the benchmark size, striped:
+    fwd+bwd time of 2 steps each after one warm-up, unmasked FLOPs only."""
+    out = {}
+
+    def timed(fn, n=2):
+        fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(n):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    Hkv = max(H // 4, 1)
+    q, do = (sp.striped_permute(x[n], N) for n in ("q", "do"))
+    k, v = (sp.striped_permute(x[n][:, :Hkv].contiguous(), N) for n in ("k", "v"))
+    o, lse = sp.striped_attn_fwd_gqa(q, k, v, N)
+    ws = sp.new_workspace(B, H, S, D, N, torch.bfloat16, dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def gqa_step():
+        sp.striped_attn_fwd_gqa(q, k, v, N, out=o, lse_out=lse)
+        sp.striped_attn_bwd_gqa(q, k, v, o, lse, do, N, workspace=ws, dq=dq, dk=dk, dv=dv)
+
+    ms = timed(gqa_step)
+    out["gqa"] = {"H": H, "Hkv": Hkv, "ms": ms, "tflops": _flops(B, H, S, D, 14) / (ms / 1e3) / 1e12}
+    del k, v, dk, dv
+    nseq = 8
+    cu = [i * (S // nseq) for i in range(nseq + 1)]
+    qp, kp, vp, dop = (sp.striped_varlen_permute(x[n][0], cu, N) for n in ("q", "k", "v", "do"))
+    op, lp = sp.striped_attn_fwd_varlen(qp, kp, vp, cu, N)
+    ws1 = sp.new_workspace(1, H, S, D, N, torch.bfloat16, dev)
+    g3 = [torch.empty_like(qp) for _ in range(3)]
+
+    def varlen_step():
+        sp.striped_attn_fwd_varlen(qp, kp, vp, cu, N, out=op, lse_out=lp)
+        sp.striped_attn_bwd_varlen(qp, kp, vp, op, lp, dop, cu, N, workspace=ws1, dq=g3[0], dk=g3[1], dv=g3[2])
+
+    ms = timed(varlen_step)
+    fl = 14 * D * H * sum((b_ - a_) * (b_ - a_ + 1) / 2 for a_, b_ in zip(cu, cu[1:]))
+    out["varlen"] = {"H": H, "sequences": nseq, "seq_len": S // nseq, "ms": ms, "tflops": fl / (ms / 1e3) / 1e12}
+    return out
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
 
@@ -520,6 +569,8 @@ def run_gpu(args, rank, world, local_rank):
         line["per_round_fwd"] = per_round
     if args.compare and args.short:
         line["short_sequence"] = short_sequence_report(sp, torch, dev)
+    if args.compare and B == 1:
+        line["variants"] = variants_report(sp, torch, dev, x, B, H, S, D, N)
     if e2e is not None:
         line["e2e"] = e2e
     line["clocks"] = clk.summary()
