@@ -475,42 +475,49 @@ def run_gpu(args, rank, world, local_rank):
         ev_in = [torch.cuda.Event() for _ in range(2)]
         ev_done = [torch.cuda.Event() for _ in range(2)]
         ev_out = [torch.cuda.Event() for _ in range(2)]
-        torch.cuda.synchronize()
-        h0 = torch.cuda.Event(enable_timing=True)
-        h1 = torch.cuda.Event(enable_timing=True)
-        h0.record(s_comp)
-        s_h2d.wait_stream(s_comp)
-        s_d2h.wait_stream(s_comp)
-        K = args.e2e_steps
+        def pipeline(K):
+            """K end-to-end steps; returns the device time from the first
+            input copy to the last result copy."""
+            torch.cuda.synchronize()
+            h0 = torch.cuda.Event(enable_timing=True)
+            h1 = torch.cuda.Event(enable_timing=True)
+            h0.record(s_comp)
+            s_h2d.wait_stream(s_comp)
+            s_d2h.wait_stream(s_comp)
 
-        def load(kk):
-            bb = kk % 2
-            with torch.cuda.stream(s_h2d):
+            def load(kk):
+                bb = kk % 2
+                with torch.cuda.stream(s_h2d):
+                    if kk >= 2:
+                        s_h2d.wait_event(ev_done[bb])  # step kk-2 no longer reads this buffer
+                    for k_ in names:
+                        dev_in[bb][k_].copy_(host_in[k_], non_blocking=True)
+                    ev_in[bb].record(s_h2d)
+
+            load(0)
+            for kk in range(K):
+                bb = kk % 2
+                if kk + 1 < K:
+                    load(kk + 1)
+                s_comp.wait_event(ev_in[bb])
                 if kk >= 2:
-                    s_h2d.wait_event(ev_done[bb])  # step kk-2 no longer reads this buffer
-                for k_ in names:
-                    dev_in[bb][k_].copy_(host_in[k_], non_blocking=True)
-                ev_in[bb].record(s_h2d)
+                    s_comp.wait_event(ev_out[bb])  # step kk-2's results have left this buffer
+                step(src=dev_in[bb], dst=dev_out[bb])
+                ev_done[bb].record(s_comp)
+                with torch.cuda.stream(s_d2h):
+                    s_d2h.wait_event(ev_done[bb])
+                    for t, h in zip(dev_out[bb], host_out[bb]):
+                        h.copy_(t, non_blocking=True)
+                    ev_out[bb].record(s_d2h)
+            s_comp.wait_stream(s_d2h)
+            h1.record(s_comp)
+            torch.cuda.synchronize()
+            return h0.elapsed_time(h1)
 
-        load(0)
-        for kk in range(K):
-            bb = kk % 2
-            if kk + 1 < K:
-                load(kk + 1)
-            s_comp.wait_event(ev_in[bb])
-            if kk >= 2:
-                s_comp.wait_event(ev_out[bb])  # step kk-2's results have left this buffer
-            step(src=dev_in[bb], dst=dev_out[bb])
-            ev_done[bb].record(s_comp)
-            with torch.cuda.stream(s_d2h):
-                s_d2h.wait_event(ev_done[bb])
-                for t, h in zip(dev_out[bb], host_out[bb]):
-                    h.copy_(t, non_blocking=True)
-                ev_out[bb].record(s_d2h)
-        s_comp.wait_stream(s_d2h)
-        h1.record(s_comp)
-        torch.cuda.synchronize()
-        e_ms = max_over_ranks(h0.elapsed_time(h1), dist, dev) / K
+        pipeline(2)  # untimed warm-up of the copy pipeline (first touches of the buffers)
+        K = args.e2e_steps
+        t_e2e = pipeline(K)
+        e_ms = max_over_ranks(t_e2e, dist, dev) / K
         # the copied-out results of the last step match the device results
         last = host_out[(K - 1) % 2]
         for t, h in zip((o, dq, dk, dv), last):
@@ -520,7 +527,8 @@ def run_gpu(args, rank, world, local_rank):
         bo = sum(t.numel() * t.element_size() for t in host_out[0])
         e2e = {"value": job_tflops(fl_step, e_ms, world), "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": bo, "ms_per_step": e_ms, "steps": K,
-               "copies": "pinned host buffers, own streams, double-buffered (overlapped with compute)"}
+               "copies": "pinned host buffers, own streams, double-buffered (overlapped with compute); "
+                         "one untimed 2-step pass of the pipeline first"}
         del host_in, host_out, dev_in, dev_out
 
     if rank != 0:
@@ -590,7 +598,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-sample", type=int, default=24576,
                     help="causal-prefix length of the timed CPU-oracle sample (0 disables)")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-compare", dest="compare", action="store_false")
     ap.add_argument("--no-short", dest="short", action="store_false",
                     help="skip the short-sequence (S=8192) comparison")
