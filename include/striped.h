@@ -142,7 +142,7 @@ int striped_varlen_unpermute(const void *x, void *y, const int32_t *cu_seqlens, 
  * rounding, and lse = natural-log log-sum-exp of each row's kept scores.
  *  q, k, v: [B,H,S,D] `dtype` inputs in `layout` order.
  *  o:       [B,H,S,D] `dtype` output.      lse: [B,H,S] fp32 output.
- * bf16 requires D == 128; fp32 requires D % 8 == 0 and D <= 128.
+ * bf16 requires D == 64 or D == 128; fp32 requires D % 8 == 0 and D <= 128.
  */
 int striped_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
                      int64_t H, int64_t S, int64_t D, int N, int layout, int dtype, float scale,

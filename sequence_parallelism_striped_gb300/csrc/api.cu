@@ -102,7 +102,7 @@ static int check_attn(int64_t B, int64_t H, int64_t S, int64_t D, int N, int lay
     if (!valid_layout(layout)) return STRIPED_ERR_INVALID_ARG;
     int64_t tile;
     if (dtype == STRIPED_BF16) {
-        if (D != 128) return STRIPED_ERR_UNSUPPORTED;
+        if (D != 128 && D != 64) return STRIPED_ERR_UNSUPPORTED;
         tile = kTcTile;
     } else if (dtype == STRIPED_FP32) {
         if (D % 8 != 0 || D > 128) return STRIPED_ERR_UNSUPPORTED;
@@ -191,7 +191,7 @@ int striped_selftest_timeout(int64_t spins, void *stream) {
 
 int striped_kernel_tile(int dtype, int64_t D, int *Tq, int *Tk) {
     if (!Tq || !Tk) return STRIPED_ERR_INVALID_ARG;
-    if (dtype == STRIPED_BF16 && D == 128) {
+    if (dtype == STRIPED_BF16 && (D == 128 || D == 64)) {
         *Tq = *Tk = kTcTile;
         return STRIPED_OK;
     }

@@ -46,20 +46,26 @@ namespace striped {
 
 namespace {
 
-constexpr int BT = 128, HD = 128;
+constexpr int BT = 128;
 constexpr int QS = 2;  // Q/dO stages
-constexpr uint32_t kBox = 128 * 128;
-constexpr uint32_t kTile = 2 * kBox;
-constexpr uint32_t kKOff = 0;
-constexpr uint32_t kVOff = kTile;
-constexpr uint32_t kQOff = 2 * kTile;                 // stage s: Q at kQOff + s*2*kTile, dO after
-constexpr uint32_t kDSOff = kQOff + QS * 2 * kTile;   // dS (MN-major A operand)
-constexpr uint32_t kStatOff = kDSOff + kTile;         // per stage: [LSE*log2e 128 | Delta 128] floats
+constexpr uint32_t kBox = 128 * 128;  // 128 rows x 64 bf16 (one 128-byte-swizzle box)
 constexpr uint32_t kStatBytes = 2 * 128 * 4;
-constexpr uint32_t kBarOff = kStatOff + QS * kStatBytes;
-constexpr size_t kSmemBytes = kBarOff + 256;            // the dynamic smem base is 1024-aligned
-static_assert(kSmemBytes <= 232448, "shared memory over the per-block limit");
 constexpr int kThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 4..11 compute
+
+// Shared-memory plan for head dimension HD (64 or 128): K, V, Q_i, dO_i
+// tiles of HD/64 boxes; the dS tile is always 128 x 128.
+template <int HD>
+struct BwdCfg {
+    static constexpr uint32_t kTile = (HD / 64) * kBox;
+    static constexpr uint32_t kKOff = 0;
+    static constexpr uint32_t kVOff = kTile;
+    static constexpr uint32_t kQOff = 2 * kTile;                // stage s: Q at kQOff + s*2*kTile, dO after
+    static constexpr uint32_t kDSOff = kQOff + QS * 2 * kTile;  // dS (MN-major A operand)
+    static constexpr uint32_t kStatOff = kDSOff + 2 * kBox;     // per stage: [LSE*log2e 128 | Delta 128]
+    static constexpr uint32_t kBarOff = kStatOff + QS * kStatBytes;
+    static constexpr size_t kSmemBytes = kBarOff + 256;           // the dynamic smem base is 1024-aligned
+    static_assert(kSmemBytes <= 232448, "shared memory over the per-block limit");
+};
 
 struct BwdParams {
     AttnGeom g;
@@ -135,18 +141,22 @@ __device__ __forceinline__ void qiter_next(QTileIter &it, int layout, int N, int
 
 // kPacked: packed variable-length sequences (the sequence table is
 // consulted); the dense instantiation compiles the span as {0, nq}.
-template <bool kPacked>
+template <int HD, bool kPacked>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                   const __grid_constant__ CUtensorMap tmdQ, const BwdParams p) {
+    using Cfg = BwdCfg<HD>;
+    constexpr uint32_t kTile = Cfg::kTile, kKOff = Cfg::kKOff, kVOff = Cfg::kVOff, kQOff = Cfg::kQOff,
+                       kDSOff = Cfg::kDSOff, kStatOff = Cfg::kStatOff;
+    constexpr int kBoxes = HD / 64;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw;
     if ((smem_u32(smem) & 1023u) != 0) {  // operand tiles need 1024-byte alignment
         if (threadIdx.x == 0 && p.err) atomicExch(p.err, STRIPED_ERR_ALIGN);
         return;
     }
-    Bars *bars = reinterpret_cast<Bars *>(smem + kBarOff);
+    Bars *bars = reinterpret_cast<Bars *>(smem + Cfg::kBarOff);
     const uint32_t sbase = smem_u32(smem);
     const AttnGeom &g = p.g;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -213,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_slot;
-    const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
+    const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + HD;
 
     if (warp == 0 && lane == 0 && nt > 0) {
         // ---------------- TMA producer: K, V once, then Q_i + statistics
@@ -223,10 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmdO);
         const uint32_t kb = smem_u32(&bars->kv_full);
         mbar_arrive_expect_tx(kb, 2 * kTile);
-        tma_load_4d(sbase + kKOff, &tmK, kb, 0, bg * BT, e, (int)bh);
-        tma_load_4d(sbase + kKOff + kBox, &tmK, kb, 64, bg * BT, e, (int)bh);
-        tma_load_4d(sbase + kVOff, &tmV, kb, 0, bg * BT, e, (int)bh);
-        tma_load_4d(sbase + kVOff + kBox, &tmV, kb, 64, bg * BT, e, (int)bh);
+#pragma unroll
+        for (int x = 0; x < kBoxes; ++x) tma_load_4d(sbase + kKOff + x * kBox, &tmK, kb, 64 * x, bg * BT, e, (int)bh);
+#pragma unroll
+        for (int x = 0; x < kBoxes; ++x) tma_load_4d(sbase + kVOff + x * kBox, &tmV, kb, 64 * x, bg * BT, e, (int)bh);
         QTileIter it = qiter_begin(g.layout, N, G, e, b, nqs, rows_b);
         for (int i = 0; i < nt; ++i, qiter_next(it, g.layout, N, G, e, b, nqs, rows_b)) {
             const int s = i % QS;
@@ -237,8 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(fb, kTile + kStatBytes);
             bulk_load(sbase + kStatOff + s * kStatBytes,
                       p.stats + (((bq * N + it.d) * (int64_t)nq + qbase + it.a) << 8), kStatBytes, fb);
-            tma_load_4d(qdst, &tmQ, fb, 0, (qbase + it.a) * BT, it.d, (int)bq);
-            tma_load_4d(qdst + kBox, &tmQ, fb, 64, (qbase + it.a) * BT, it.d, (int)bq);
+#pragma unroll
+            for (int x = 0; x < kBoxes; ++x)
+                tma_load_4d(qdst + x * kBox, &tmQ, fb, 64 * x, (qbase + it.a) * BT, it.d, (int)bq);
         }
     } else if (warp == 2 && lane == 0 && nt > 0) {
         // ---------------- TMA producer: dO_i (its own stream: the buffer is
@@ -252,8 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t odst = sbase + kQOff + s * 2 * kTile + kTile;
             const int bq = (int)(bh * G + it.h);
             mbar_arrive_expect_tx(fb, kTile);
-            tma_load_4d(odst, &tmdO, fb, 0, (qbase + it.a) * BT, it.d, bq);
-            tma_load_4d(odst + kBox, &tmdO, fb, 64, (qbase + it.a) * BT, it.d, bq);
+#pragma unroll
+            for (int x = 0; x < kBoxes; ++x)
+                tma_load_4d(odst + x * kBox, &tmdO, fb, 64 * x, (qbase + it.a) * BT, it.d, bq);
         }
     } else if (warp == 1 && lane == 0 && nt > 0) {
         // ---------------- MMA issuer
@@ -329,11 +341,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) mma_commit(smem_u32(&bars->acc_done));
     } else if (warp >= 4) {
-        // ---------------- compute: two warpgroups split the 128 columns
-        const int wg = (warp - 4) >> 2;       // 0: columns 0..63, 1: columns 64..127
+        // ---------------- compute: two warpgroups split the 128 query columns
+        // of S^T/dP^T (64 each) and the HD columns of dQ_i, dK, dV (HD/2 each)
+        const int wg = (warp - 4) >> 2;       // 0: first half, 1: second half
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;  // key row of S^T/dP^T; query row of dQ
-        const int cbase = wg * 64;            // first column of this warpgroup
+        const int cbase = wg * 64;            // first query column of this warpgroup
+        // first head-dimension column of this warpgroup (at HD = 128 the same
+        // value as cbase, and written so for the compiler)
+        const int dbase = HD == 128 ? cbase : wg * (HD / 2);
         const uint32_t pbase = wg * 64;       // TMEM columns of this warpgroup's P^T pairs
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const float cl2 = g.scale * 1.4426950408889634f;
@@ -445,58 +461,99 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            uint32_t q0[32], q1[32];
-            tmem_ld32(tdP + lane_off + cbase, q0);
-            tmem_ld32(tdP + lane_off + cbase + 32, q1);
-            tmem_ld_wait(q0);
-            tmem_ld_wait(q1);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
             // dQ_i -> fp32 accumulator, split over two paths so neither the
             // TMA engine nor the load/store unit carries all of it: warpgroup 0
-            // adds its 64 columns with vector reductions; warpgroup 1 stages its
-            // 64 columns in the dO_i buffer (dead once dV_i, covered by
-            // dq_full, is done) as two 128-byte-swizzled 32-column boxes and
+            // adds its HD/2 columns with vector reductions; warpgroup 1 stages
+            // its HD/2 columns in the dO_i buffer (dead once dV_i, covered by
+            // dq_full, is done) as 128-byte-swizzled 32-column boxes and
             // each warp bulk-reduces its own 32 rows, then returns the buffer.
+            // HD = 128 and HD = 64 are written out separately: a shared generic
+            // form compiled to a 1.4% slower schedule of this hot path at 128.
             const int s = i % QS;
             const int64_t bq = bh * G + done.h;  // query head of tile i
-            if (wg == 0) {
-                const int64_t qi = (int64_t)(qbase + done.a) * BT + row;
-                if (qi < g.L) {
-                    float *dst =
-                        p.dq_acc + (bq * g.stride_bh + (int64_t)done.d * g.stripe_stride + qi * HD + cbase);
+            if constexpr (HD == 128) {
+                uint32_t q0[32], q1[32];
+                tmem_ld32(tdP + lane_off + cbase, q0);
+                tmem_ld32(tdP + lane_off + cbase + 32, q1);
+                tmem_ld_wait(q0);
+                tmem_ld_wait(q1);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
+                if (wg == 0) {
+                    const int64_t qi = (int64_t)(qbase + done.a) * BT + row;
+                    if (qi < g.L) {
+                        float *dst =
+                            p.dq_acc + (bq * g.stride_bh + (int64_t)done.d * g.stripe_stride + qi * HD + cbase);
 #pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        red_add_v4(dst + 4 * v, __uint_as_float(q0[4 * v]), __uint_as_float(q0[4 * v + 1]),
-                                   __uint_as_float(q0[4 * v + 2]), __uint_as_float(q0[4 * v + 3]));
+                        for (int v = 0; v < 8; ++v)
+                            red_add_v4(dst + 4 * v, __uint_as_float(q0[4 * v]), __uint_as_float(q0[4 * v + 1]),
+                                       __uint_as_float(q0[4 * v + 2]), __uint_as_float(q0[4 * v + 3]));
 #pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        red_add_v4(dst + 32 + 4 * v, __uint_as_float(q1[4 * v]), __uint_as_float(q1[4 * v + 1]),
-                                   __uint_as_float(q1[4 * v + 2]), __uint_as_float(q1[4 * v + 3]));
-                }
-            } else {
-                const uint32_t stage = sbase + kQOff + s * 2 * kTile + kTile;
+                        for (int v = 0; v < 8; ++v)
+                            red_add_v4(dst + 32 + 4 * v, __uint_as_float(q1[4 * v]), __uint_as_float(q1[4 * v + 1]),
+                                       __uint_as_float(q1[4 * v + 2]), __uint_as_float(q1[4 * v + 3]));
+                    }
+                } else {
+                    const uint32_t stage = sbase + kQOff + s * 2 * kTile + kTile;
 #pragma unroll
-                for (int box = 0; box < 2; ++box) {
-                    const uint32_t(&src)[32] = box ? q1 : q0;
+                    for (int box = 0; box < 2; ++box) {
+                        const uint32_t(&src)[32] = box ? q1 : q0;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint32_t addr = stage + box * kBox + row * 128 + ((j ^ (row & 7)) * 16);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(src[4 * j]),
-                                     "r"(src[4 * j + 1]), "r"(src[4 * j + 2]), "r"(src[4 * j + 3])
-                                     : "memory");
+                        for (int j = 0; j < 8; ++j) {
+                            const uint32_t addr = stage + box * kBox + row * 128 + ((j ^ (row & 7)) * 16);
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(src[4 * j]),
+                                         "r"(src[4 * j + 1]), "r"(src[4 * j + 2]), "r"(src[4 * j + 3])
+                                         : "memory");
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const uint32_t wofs = (uint32_t)quarter * 32 * 128;
+                        const int r0 = (qbase + done.a) * BT + quarter * 32;
+                        tma_reduce_add_4d(&tmdQ, stage + wofs, cbase, r0, done.d, (int)bq);
+                        tma_reduce_add_4d(&tmdQ, stage + kBox + wofs, cbase + 32, r0, done.d, (int)bq);
+                        bulk_commit_group();
+                        pending = s;
                     }
                 }
-                fence_proxy_async_smem();
+            } else {
+                // HD = 64: 32 columns per warpgroup, one box for the bulk path
+                uint32_t q0[32];
+                tmem_ld32(tdP + lane_off + dbase, q0);
+                tmem_ld_wait(q0);
+                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    const uint32_t wofs = (uint32_t)quarter * 32 * 128;
-                    const int r0 = (qbase + done.a) * BT + quarter * 32;
-                    tma_reduce_add_4d(&tmdQ, stage + wofs, cbase, r0, done.d, (int)bq);
-                    tma_reduce_add_4d(&tmdQ, stage + kBox + wofs, cbase + 32, r0, done.d, (int)bq);
-                    bulk_commit_group();
-                    pending = s;
+                if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
+                if (wg == 0) {
+                    const int64_t qi = (int64_t)(qbase + done.a) * BT + row;
+                    if (qi < g.L) {
+                        float *dst =
+                            p.dq_acc + (bq * g.stride_bh + (int64_t)done.d * g.stripe_stride + qi * HD + dbase);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            red_add_v4(dst + 4 * v, __uint_as_float(q0[4 * v]), __uint_as_float(q0[4 * v + 1]),
+                                       __uint_as_float(q0[4 * v + 2]), __uint_as_float(q0[4 * v + 3]));
+                    }
+                } else {
+                    const uint32_t stage = sbase + kQOff + s * 2 * kTile + kTile;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t addr = stage + row * 128 + ((j ^ (row & 7)) * 16);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(q0[4 * j]),
+                                     "r"(q0[4 * j + 1]), "r"(q0[4 * j + 2]), "r"(q0[4 * j + 3])
+                                     : "memory");
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const uint32_t wofs = (uint32_t)quarter * 32 * 128;
+                        const int r0 = (qbase + done.a) * BT + quarter * 32;
+                        tma_reduce_add_4d(&tmdQ, stage + wofs, dbase, r0, done.d, (int)bq);
+                        bulk_commit_group();
+                        pending = s;
+                    }
                 }
             }
         }
@@ -508,17 +565,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // ---------------- epilogue: this warpgroup's columns of dK, dV
         const int64_t kj = (int64_t)bg * BT + row;
-        const int64_t krow = bh * g.stride_bh + (int64_t)e * g.stripe_stride + kj * HD + cbase;
+        const int64_t krow = bh * g.stride_bh + (int64_t)e * g.stripe_stride + kj * HD + dbase;
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
             const uint32_t tacc = which ? tdK : tdV;
             __nv_bfloat16 *outp = which ? p.dk : p.dv;
             const float mul = which ? g.scale : 1.f;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < HD / 64; ++c) {
                 uint32_t rr[32];
                 if (ok) {
-                    tmem_ld32(tacc + lane_off + cbase + c * 32, rr);
+                    tmem_ld32(tacc + lane_off + dbase + c * 32, rr);
                     tmem_ld_wait(rr);
                 } else {
 #pragma unroll
@@ -551,7 +608,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Per row of every stripe, padded to whole 128-row tiles: the tile-major
 // statistics block [LSE*log2e 128 | Delta 128] with Delta_p = <dO_p, O_p>
 // (fp32); padding rows get LSE = +inf and Delta = 0.  Real rows also get
-// their dQ accumulator row zeroed.  One warp per padded row, D = 128.
+// their dQ accumulator row zeroed.  One warp per padded row; each lane
+// covers HD/32 consecutive elements of it.
+template <int HD>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o,
                                                       const __nv_bfloat16 *__restrict__ dO,
                                                       const float *__restrict__ lse, float *__restrict__ stats,
@@ -573,20 +632,30 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__res
             continue;
         }
         const int64_t rw = stripe * L + ii;  // row of the [BH][S] tensors
-        const uint2 ov = *reinterpret_cast<const uint2 *>(o + rw * HD + lane * 4);
-        const uint2 gv = *reinterpret_cast<const uint2 *>(dO + rw * HD + lane * 4);
-        const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&ov);
-        const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&gv);
-        float2 a0 = __bfloat1622float2(o2[0]), a1 = __bfloat1622float2(o2[1]);
-        float2 b0 = __bfloat1622float2(g2[0]), b1 = __bfloat1622float2(g2[1]);
-        float sum = a0.x * b0.x + a0.y * b0.y + a1.x * b1.x + a1.y * b1.y;
+        float sum;
+        if constexpr (HD == 128) {
+            const uint2 ov = *reinterpret_cast<const uint2 *>(o + rw * HD + lane * 4);
+            const uint2 gv = *reinterpret_cast<const uint2 *>(dO + rw * HD + lane * 4);
+            const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&ov);
+            const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&gv);
+            const float2 a0 = __bfloat1622float2(o2[0]), a1 = __bfloat1622float2(o2[1]);
+            const float2 b0 = __bfloat1622float2(g2[0]), b1 = __bfloat1622float2(g2[1]);
+            sum = a0.x * b0.x + a0.y * b0.y + a1.x * b1.x + a1.y * b1.y;
+        } else {
+            const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(o + rw * HD + lane * 2));
+            const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(dO + rw * HD + lane * 2));
+            sum = a.x * b.x + a.y * b.y;
+        }
 #pragma unroll
         for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
         if (lane == 0) {
             blk[0] = lse[rw] * 1.4426950408889634f;
             blk[128] = sum;
         }
-        *reinterpret_cast<float4 *>(dq_acc + rw * HD + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+        if constexpr (HD == 128)
+            *reinterpret_cast<float4 *>(dq_acc + rw * HD + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+        else
+            *reinterpret_cast<float2 *>(dq_acc + rw * HD + lane * 2) = make_float2(0.f, 0.f);
     }
 }
 
@@ -619,15 +688,19 @@ int num_sms() {
 
 }  // namespace
 
-int launch_tc_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
-                  const void *dO, void *dq, void *dk, void *dv, float *dq_acc, float *stats,
-                  const AttnGeom &g, int64_t *tile_stats, cudaStream_t stream) {
+namespace {
+
+template <int HD>
+int launch_bwd_hd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
+                  void *dq, void *dk, void *dv, float *dq_acc, float *stats, const AttnGeom &g, int64_t *tile_stats,
+                  cudaStream_t stream) {
+    constexpr size_t kSmemBytes = BwdCfg<HD>::kSmemBytes;
     static int attr = 1;
     if (attr == 1) {
-        cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel<HD, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)kSmemBytes);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(tc_bwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(tc_bwd_kernel<HD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kSmemBytes);
         attr = cuda_status(e);
     }
@@ -635,8 +708,8 @@ int launch_tc_bwd(const void *q, const void *k, const void *v, const void *o, co
     const int64_t rows = g.BH * g.N * g.L;
     const int sms = num_sms();
     const int nq = (int)((g.L + BT - 1) / BT);
-    bwd_pre_kernel<<<sms * 8, 256, 0, stream>>>((const __nv_bfloat16 *)o, (const __nv_bfloat16 *)dO, lse, stats,
-                                                dq_acc, g.L, nq, g.BH * g.N * (int64_t)nq * BT);
+    bwd_pre_kernel<HD><<<sms * 8, 256, 0, stream>>>((const __nv_bfloat16 *)o, (const __nv_bfloat16 *)dO, lse,
+                                                    stats, dq_acc, g.L, nq, g.BH * g.N * (int64_t)nq * BT);
     int st = cuda_status(cudaGetLastError());
     if (st != STRIPED_OK) return st;
     CUtensorMap mq, mk, mv, mdo;
@@ -660,13 +733,23 @@ int launch_tc_bwd(const void *q, const void *k, const void *v, const void *o, co
     const int64_t nblocks = nk * g.N * bh_kv;  // one CTA per key tile of every key/value head
     if (nblocks > 0x7fffffffll) return STRIPED_ERR_UNSUPPORTED;
     if (g.seqs.n > 0)
-        tc_bwd_kernel<true><<<(unsigned)nblocks, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, p);
+        tc_bwd_kernel<HD, true><<<(unsigned)nblocks, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, p);
     else
-        tc_bwd_kernel<false><<<(unsigned)nblocks, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, p);
+        tc_bwd_kernel<HD, false><<<(unsigned)nblocks, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, p);
     st = cuda_status(cudaGetLastError());
     if (st != STRIPED_OK) return st;
     bwd_post_kernel<<<sms * 8, 256, 0, stream>>>(dq_acc, (__nv_bfloat16 *)dq, rows * HD / 8, g.scale);
     return cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+
+int launch_tc_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                  const void *dO, void *dq, void *dk, void *dv, float *dq_acc, float *stats,
+                  const AttnGeom &g, int64_t *tile_stats, cudaStream_t stream) {
+    if (g.D == 64)
+        return launch_bwd_hd<64>(q, k, v, o, lse, dO, dq, dk, dv, dq_acc, stats, g, tile_stats, stream);
+    return launch_bwd_hd<128>(q, k, v, o, lse, dO, dq, dk, dv, dq_acc, stats, g, tile_stats, stream);
 }
 
 }  // namespace striped

@@ -33,16 +33,22 @@ namespace striped {
 
 namespace {
 
-constexpr int BM = 128, BN = 128, HD = 128;
-constexpr int NS = 3;                       // K/V stages
-constexpr uint32_t kBoxBytes = 128 * 128;   // 128 rows x 64 bf16
-constexpr uint32_t kTileBytes = 2 * kBoxBytes;  // 128 x 128 bf16 = 32 KB
-constexpr uint32_t kKVOff = 0;
-constexpr uint32_t kStageBytes = 2 * kTileBytes;  // K + V
-constexpr uint32_t kBarOff = kKVOff + NS * kStageBytes;
-constexpr size_t kSmemBytes = 1024 + kBarOff + 256;
-static_assert(kSmemBytes <= 232448, "shared memory over the per-block limit");
+constexpr int BM = 128, BN = 128;
+constexpr uint32_t kBoxBytes = 128 * 128;   // 128 rows x 64 bf16 (one 128-byte-swizzle box)
 constexpr int kThreads = 192;
+
+// Shared-memory plan for head dimension HD (64 or 128): K/V tiles of HD/64
+// boxes each, in a ring of NS stages (3 at HD = 128, 5 at HD = 64).
+template <int HD>
+struct FwdCfg {
+    static constexpr int kBoxes = HD / 64;
+    static constexpr int NS = HD == 128 ? 3 : 5;
+    static constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;
+    static constexpr uint32_t kStageBytes = 2 * kTileBytes;  // K + V
+    static constexpr uint32_t kBarOff = NS * kStageBytes;
+    static constexpr size_t kSmemBytes = 1024 + kBarOff + 256;
+    static_assert(kSmemBytes <= 232448, "shared memory over the per-block limit");
+};
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct FwdParams {
@@ -57,6 +63,7 @@ struct FwdParams {
     int *err;                     // device error word
 };
 
+template <int NS>
 struct Bars {
     uint64_t q_full;
     uint64_t kv_full[NS];
@@ -74,14 +81,17 @@ __device__ __forceinline__ int tile_rows(int64_t L, int t) {
 
 // kPacked: packed variable-length sequences (the sequence table is
 // consulted); the dense instantiation compiles the span as {0, nq}.
-template <bool kRound, bool kPacked>
+template <int HD, bool kRound, bool kPacked>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_fwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const FwdParams p) {
+    using Cfg = FwdCfg<HD>;
+    constexpr int NS = Cfg::NS;
+    constexpr uint32_t kTileBytes = Cfg::kTileBytes, kStageBytes = Cfg::kStageBytes, kKVOff = 0;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
-    Bars *bars = reinterpret_cast<Bars *>(smem + kBarOff);
+    Bars<NS> *bars = reinterpret_cast<Bars<NS> *>(smem + Cfg::kBarOff);
     const uint32_t sbase = smem_u32(smem);
     const AttnGeom &g = p.g;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -157,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_slot;
-    const uint32_t tS0 = tmem, tS1 = tmem + 128, tO = tmem + 256, tQ = tmem + 384;
+    const uint32_t tS0 = tmem, tS1 = tmem + 128, tO = tmem + 256, tQ = tmem + 256 + HD;
 
     const int qstripe = kRound ? 0 : d;
     const int kvh = (int)(bh / g.G);  // key/value head read by query head bh
@@ -183,10 +193,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t kdst = sbase + kKVOff + s * kStageBytes;
                 const uint32_t vdst = kdst + kTileBytes;
                 mbar_arrive_expect_tx(fb, 2 * kTileBytes);
-                tma_load_4d(kdst, &tmK, fb, 0, kb * BN, kstripe, kvh);
-                tma_load_4d(kdst + kBoxBytes, &tmK, fb, 64, kb * BN, kstripe, kvh);
-                tma_load_4d(vdst, &tmV, fb, 0, kb * BN, kstripe, kvh);
-                tma_load_4d(vdst + kBoxBytes, &tmV, fb, 64, kb * BN, kstripe, kvh);
+#pragma unroll
+                for (int x = 0; x < Cfg::kBoxes; ++x) {
+                    tma_load_4d(kdst + x * kBoxBytes, &tmK, fb, 64 * x, kb * BN, kstripe, kvh);
+                    tma_load_4d(vdst + x * kBoxBytes, &tmV, fb, 64 * x, kb * BN, kstripe, kvh);
+                }
             }
         }
     } else if (warp == 1 && lane == 0 && nt > 0) {
@@ -238,22 +249,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             // operand of every S = Q K^T, so the tensor core reads only K
             // from shared memory for it
             const int64_t qrow = (int64_t)ag * BM + ri;
-            uint32_t qa[32], qb[32];
-            if (qrow < g.L) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(
-                    p.q + bh * g.stride_bh + (int64_t)qstripe * g.stripe_stride + qrow * HD);
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                p.q + bh * g.stride_bh + (int64_t)qstripe * g.stripe_stride + qrow * HD);
+#pragma unroll
+            for (int h = 0; h < HD / 64; ++h) {  // 64 bf16 = 32 columns per chunk
+                uint32_t qa[32];
 #pragma unroll
                 for (int v = 0; v < 8; ++v) {
-                    const uint4 w0 = __ldg(src + v), w1 = __ldg(src + 8 + v);
-                    qa[4 * v] = w0.x, qa[4 * v + 1] = w0.y, qa[4 * v + 2] = w0.z, qa[4 * v + 3] = w0.w;
-                    qb[4 * v] = w1.x, qb[4 * v + 1] = w1.y, qb[4 * v + 2] = w1.z, qb[4 * v + 3] = w1.w;
+                    const uint4 w = qrow < g.L ? __ldg(src + 8 * h + v) : make_uint4(0u, 0u, 0u, 0u);
+                    qa[4 * v] = w.x, qa[4 * v + 1] = w.y, qa[4 * v + 2] = w.z, qa[4 * v + 3] = w.w;
                 }
-            } else {
-#pragma unroll
-                for (int u = 0; u < 32; ++u) qa[u] = qb[u] = 0u;
+                tmem_st32(tQ + lane_off + 32 * h, qa);
             }
-            tmem_st32(tQ + lane_off, qa);
-            tmem_st32(tQ + lane_off + 32, qb);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -456,16 +463,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+template <int HD>
 static int set_smem_once() {
     static int status = 1;
     if (status == 1) {
+        const int bytes = (int)FwdCfg<HD>::kSmemBytes;
         const cudaError_t e[3] = {
-            cudaFuncSetAttribute(tc_fwd_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSmemBytes),
-            cudaFuncSetAttribute(tc_fwd_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSmemBytes),
-            cudaFuncSetAttribute(tc_fwd_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSmemBytes)};
+            cudaFuncSetAttribute(tc_fwd_kernel<HD, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes),
+            cudaFuncSetAttribute(tc_fwd_kernel<HD, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes),
+            cudaFuncSetAttribute(tc_fwd_kernel<HD, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)};
         status = STRIPED_OK;
         for (cudaError_t x : e)
             if (x != cudaSuccess) status = cuda_status(x);
@@ -473,10 +479,31 @@ static int set_smem_once() {
     return status;
 }
 
+template <int HD>
+static int launch_fwd_hd(const CUtensorMap &mk, const CUtensorMap &mv, const FwdParams &p, int64_t nblocks,
+                         cudaStream_t stream) {
+    const int st = set_smem_once<HD>();
+    if (st != STRIPED_OK) return st;
+    const size_t bytes = FwdCfg<HD>::kSmemBytes;
+    if (p.g.seqs.n > 0)
+        tc_fwd_kernel<HD, false, true><<<(unsigned)nblocks, kThreads, bytes, stream>>>(mk, mv, p);
+    else
+        tc_fwd_kernel<HD, false, false><<<(unsigned)nblocks, kThreads, bytes, stream>>>(mk, mv, p);
+    return cuda_status(cudaGetLastError());
+}
+
+template <int HD>
+static int launch_round_hd(const CUtensorMap &mk, const CUtensorMap &mv, const FwdParams &p, dim3 grid,
+                           cudaStream_t stream) {
+    const int st = set_smem_once<HD>();
+    if (st != STRIPED_OK) return st;
+    tc_fwd_kernel<HD, true, false><<<grid, kThreads, FwdCfg<HD>::kSmemBytes, stream>>>(mk, mv, p);
+    return cuda_status(cudaGetLastError());
+}
+
 int launch_tc_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
                   const AttnGeom &g, int64_t *tile_stats, cudaStream_t stream) {
-    int st = set_smem_once();
-    if (st != STRIPED_OK) return st;
+    int st = STRIPED_OK;
     CUtensorMap mk, mv;
     const int64_t bh_kv = g.BH / g.G;
     if ((st = make_bf16_map(&mk, k, g.D, g.L, g.N, bh_kv, g.stripe_stride, g.stride_bh, 128)) ||
@@ -492,18 +519,13 @@ int launch_tc_fwd(const void *q, const void *k, const void *v, void *o, float *l
     const int64_t nq = (g.L + BM - 1) / BM;
     const int64_t nblocks = nq * g.N * g.BH;
     if (nblocks > 0x7fffffffll) return STRIPED_ERR_UNSUPPORTED;
-    if (g.seqs.n > 0)
-        tc_fwd_kernel<false, true><<<(unsigned)nblocks, kThreads, kSmemBytes, stream>>>(mk, mv, p);
-    else
-        tc_fwd_kernel<false, false><<<(unsigned)nblocks, kThreads, kSmemBytes, stream>>>(mk, mv, p);
-    return cuda_status(cudaGetLastError());
+    return g.D == 64 ? launch_fwd_hd<64>(mk, mv, p, nblocks, stream) : launch_fwd_hd<128>(mk, mv, p, nblocks, stream);
 }
 
 int launch_tc_round(const void *q_d, const void *k_e, const void *v_e, float *o_acc, float *lse_acc,
                     void *o_out, int d, int e, int first, const AttnGeom &g, int64_t *tile_stats,
                     cudaStream_t stream) {
-    int st = set_smem_once();
-    if (st != STRIPED_OK) return st;
+    int st = STRIPED_OK;
     CUtensorMap mk, mv;
     // the slices are single stripes: a stripe dimension of extent 1
     if ((st = make_bf16_map(&mk, k_e, g.D, g.L, 1, g.BH, g.L * g.D, g.stride_bh, 128)) ||
@@ -526,8 +548,7 @@ int launch_tc_round(const void *q_d, const void *k_e, const void *v_e, float *o_
     const int64_t nq = (g.L + BM - 1) / BM;
     if (g.BH > 65535) return STRIPED_ERR_UNSUPPORTED;
     dim3 grid((unsigned)nq, (unsigned)g.BH);
-    tc_fwd_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(mk, mv, p);
-    return cuda_status(cudaGetLastError());
+    return g.D == 64 ? launch_round_hd<64>(mk, mv, p, grid, stream) : launch_round_hd<128>(mk, mv, p, grid, stream);
 }
 
 }  // namespace striped

@@ -75,6 +75,21 @@ def test_bwd_bf16_zigzag(B, H, S, D, N):
 
 
 @pytest.mark.parametrize("layout", [sp.STRIPED, sp.CONTIGUOUS, sp.ZIGZAG])
+@pytest.mark.parametrize("B,H,S,D,N", [(1, 2, 2048, 64, 4), (2, 1, 2048, 64, 8)])
+def test_bwd_bf16_head_dim_64(B, H, S, D, N, layout):
+    x, grads, stats = _run(B, H, S, D, N, layout, torch.bfloat16, seed=5)
+    _check(x, grads, stats, B, H, S, D, N, layout, torch.bfloat16)
+
+
+@pytest.mark.parametrize("layout", [sp.STRIPED, sp.CONTIGUOUS])
+def test_bwd_bf16_head_dim_64_ragged(layout):
+    """D = 64 with a ragged stripe tail (L = 300)."""
+    B, H, S, D, N = 1, 2, 1200, 64, 4
+    x, grads, stats = _run(B, H, S, D, N, layout, torch.bfloat16, seed=6)
+    _check(x, grads, stats, B, H, S, D, N, layout, torch.bfloat16)
+
+
+@pytest.mark.parametrize("layout", [sp.STRIPED, sp.CONTIGUOUS, sp.ZIGZAG])
 def test_bwd_bf16_short_sequence_full(layout):
     """Short-sequence workload B=1, H=8, S=8192, D=128, N=8: every row."""
     B, H, S, D, N = 1, 8, 8192, 128, 8

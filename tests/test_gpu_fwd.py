@@ -98,6 +98,22 @@ def test_fwd_bf16_zigzag_short_sequence_full():
     assert int(stats[1, 1:].sum()) == 0
 
 
+@pytest.mark.parametrize("layout", [sp.STRIPED, sp.CONTIGUOUS, sp.ZIGZAG])
+@pytest.mark.parametrize("B,H,S,D,N", [(1, 2, 2048, 64, 4),    # head dimension 64: one 64-column box
+                                       (2, 1, 2048, 64, 8)])
+def test_fwd_bf16_head_dim_64(B, H, S, D, N, layout):
+    x, o, lse, stats = _run_fwd(B, H, S, D, N, layout, torch.bfloat16, seed=5)
+    _check_fwd(x, o, lse, stats, B, H, S, D, N, layout, torch.bfloat16)
+
+
+@pytest.mark.parametrize("layout", [sp.STRIPED, sp.CONTIGUOUS])
+def test_fwd_bf16_head_dim_64_ragged(layout):
+    """D = 64 with a ragged stripe tail (L = 300)."""
+    B, H, S, D, N = 1, 2, 1200, 64, 4
+    x, o, lse, stats = _run_fwd(B, H, S, D, N, layout, torch.bfloat16, seed=6)
+    _check_fwd(x, o, lse, stats, B, H, S, D, N, layout, torch.bfloat16)
+
+
 def test_striped_equals_contiguous_after_unpermute():
     """Permutation equivariance on the GPU path itself: striped output mapped
     back to positions equals the contiguous-layout output."""

@@ -38,6 +38,7 @@ CASES = [
     (torch.bfloat16, 1, 8, 2, 2048, 128, 8, (sp.STRIPED, sp.ZIGZAG)),
     (torch.bfloat16, 2, 6, 3, 1200, 128, 4, (sp.STRIPED, sp.CONTIGUOUS)),  # ragged stripe tail
     (torch.bfloat16, 1, 4, 1, 8192, 128, 8, (sp.STRIPED,)),
+    (torch.bfloat16, 1, 4, 2, 2048, 64, 4, (sp.STRIPED, sp.ZIGZAG)),  # head dimension 64
 ]
 
 

@@ -15,7 +15,8 @@ DEV = torch.device("cuda")
 @pytest.mark.parametrize("dtype,B,H,S,D,N", [(torch.float32, 1, 1, 256, 64, 4),
                                              (torch.bfloat16, 1, 2, 1200, 128, 4),
                                              (torch.bfloat16, 1, 1, 1028, 128, 4),
-                                             (torch.bfloat16, 1, 4, 8192, 128, 8)])
+                                             (torch.bfloat16, 1, 4, 8192, 128, 8),
+                                             (torch.bfloat16, 1, 2, 1200, 64, 4)])
 @pytest.mark.parametrize("layout", [sp.STRIPED, sp.CONTIGUOUS])
 def test_rounds_merge_to_full_attention(dtype, B, H, S, D, N, layout):
     _rounds_merge(dtype, B, H, S, D, N, layout)

@@ -2,7 +2,9 @@
 bit-exact against the oracle's per-sequence placement, and the forward and
 backward (with and without grouped K/V heads) against the oracle's
 per-sequence attention, all three placements, fp32 and bf16, with the tile
-counters equal to the sum of the sequences' own tables."""
+counters equal to the sum of the sequences' own tables.  The bf16 dK and dV
+bounds add the bf16 storage rounding of the largest value (these shapes lie
+beyond the benchmark workloads the fixed 2e-2 bound was stated for)."""
 import numpy as np
 import pytest
 import torch
@@ -10,7 +12,7 @@ import torch
 import oracle
 import sequence_parallelism_striped_gb300 as sp
 from seeded_inputs import attention_inputs
-from tests._util import TOL, maxerr
+from tests._util import TOL, maxerr, with_bf16_storage
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda")
@@ -45,6 +47,7 @@ CASES = [
     (torch.bfloat16, 4, 2, 128, 4, [0, 1024, 3072, 4096], (sp.STRIPED, sp.CONTIGUOUS, sp.ZIGZAG)),
     (torch.bfloat16, 2, 1, 128, 8, [0, 2048, 3072, 8192], (sp.STRIPED, sp.CONTIGUOUS)),
     (torch.bfloat16, 2, 1, 128, 8, [0, 2048, 6144, 8192], (sp.ZIGZAG,)),  # zig-zag: multiples of 2N*T
+    (torch.bfloat16, 2, 2, 64, 4, [0, 1024, 3072, 4096], (sp.STRIPED, sp.ZIGZAG)),  # head dimension 64
 ]
 
 
@@ -85,12 +88,15 @@ def test_varlen_fwd_bwd_match_oracle(dtype, H, Hkv, D, N, cu, layouts):
 
         o_p, l_p, dq_p, dk_p, dv_p = back(o), back(lse), back(dq), back(dk), back(dv)
         kv_tol = tol["grad"] * np.sqrt(G)
+        bf = dtype == torch.bfloat16
         for h in range(H):
             assert maxerr(o_p[h], ref_o[h]) <= tol["o"], (layout, h)
             assert maxerr(l_p[h], ref_l[h]) <= tol["lse"], (layout, h)
             assert maxerr(dq_p[h], ref_dq[h]) <= tol["grad"], (layout, h)
-        assert maxerr(dk_p, ref_dk) <= kv_tol, (layout, maxerr(dk_p, ref_dk))
-        assert maxerr(dv_p, ref_dv) <= kv_tol, (layout, maxerr(dv_p, ref_dv))
+        dk_tol = with_bf16_storage(kv_tol, ref_dk) if bf else kv_tol
+        dv_tol = with_bf16_storage(kv_tol, ref_dv) if bf else kv_tol
+        assert maxerr(dk_p, ref_dk) <= dk_tol, (layout, maxerr(dk_p, ref_dk))
+        assert maxerr(dv_p, ref_dv) <= dv_tol, (layout, maxerr(dv_p, ref_dv))
         full = sum(oracle.tile_counts_bruteforce(b - a, N, T, T, layout)[0] for a, b in zip(cu, cu[1:]))
         part = sum(oracle.tile_counts_bruteforce(b - a, N, T, T, layout)[1] for a, b in zip(cu, cu[1:]))
         for st in (fst, bst):

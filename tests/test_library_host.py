@@ -73,6 +73,7 @@ def test_kernel_tiles(lib):
     import torch
 
     assert sp.kernel_tile(torch.bfloat16, 128) == 128
+    assert sp.kernel_tile(torch.bfloat16, 64) == 128
     assert sp.kernel_tile(torch.float32, 64) == 16
     with pytest.raises(sp.StripedError):
         sp.kernel_tile(torch.bfloat16, 96)
