@@ -282,6 +282,17 @@ int striped_tile_counts(int64_t S, int N, int Tq, int Tk, int layout, int64_t *f
  * device, §Summary).  Returns < 0 (a status code) on invalid arguments. */
 int64_t striped_critical_path(int64_t S, int N, int Tq, int Tk, int layout);
 
+/* Host-only: striped_tile_counts for a packed batch (cu_seqlens a HOST
+ * int32 array of nseq + 1 entries, as for striped_attn_fwd_varlen): each
+ * sequence is placed and tiled on its own, so the table is the sum of the
+ * sequences' tables; per packed head. */
+int striped_tile_counts_varlen(const int32_t *cu_seqlens, int nseq, int N, int Tq, int Tk, int layout,
+                               int64_t *full, int64_t *partial);
+
+/* Host-only: modelled ring critical path of a packed batch (each round runs
+ * at the pace of the device with the most tiles over all its sequences). */
+int64_t striped_critical_path_varlen(const int32_t *cu_seqlens, int nseq, int N, int Tq, int Tk, int layout);
+
 /* Synchronises `stream`, then reads and clears the device error word.
  * Returns STRIPED_OK, STRIPED_ERR_TIMEOUT or STRIPED_ERR_CUDA. */
 int striped_check_error(void *stream);

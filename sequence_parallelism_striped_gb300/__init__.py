@@ -82,6 +82,9 @@ def load(build_if_missing: bool = True):
         lib.striped_tile_counts.argtypes = [I64, I, I, I, I, P, P]
         lib.striped_critical_path.argtypes = [I64, I, I, I, I]
         lib.striped_critical_path.restype = I64
+        lib.striped_tile_counts_varlen.argtypes = [P, I, I, I, I, I, P, P]
+        lib.striped_critical_path_varlen.argtypes = [P, I, I, I, I, I]
+        lib.striped_critical_path_varlen.restype = I64
         lib.striped_check_error.argtypes = [P]
         lib.striped_status_string.argtypes = [I]
         lib.striped_status_string.restype = ctypes.c_char_p
@@ -355,6 +358,26 @@ def critical_path(S: int, N: int, Tq: int, Tk: int, layout: int = STRIPED) -> in
     r = int(load().striped_critical_path(S, N, Tq, Tk, layout))
     if r < 0:
         raise StripedError(r, "striped_critical_path")
+    return r
+
+
+def tile_counts_varlen(cu_seqlens, N: int, Tq: int, Tk: int, layout: int = STRIPED):
+    """(full, partial) tables [N rounds, N devices] of a packed batch."""
+    import numpy as np
+
+    full = np.zeros(N * N, dtype=np.int64)
+    part = np.zeros(N * N, dtype=np.int64)
+    cu, cp, n = _cu_host(cu_seqlens)
+    _check(load().striped_tile_counts_varlen(cp, n, N, Tq, Tk, layout, full.ctypes.data_as(ctypes.c_void_p),
+                                             part.ctypes.data_as(ctypes.c_void_p)), "striped_tile_counts_varlen")
+    return full.reshape(N, N), part.reshape(N, N)
+
+
+def critical_path_varlen(cu_seqlens, N: int, Tq: int, Tk: int, layout: int = STRIPED) -> int:
+    cu, cp, n = _cu_host(cu_seqlens)
+    r = int(load().striped_critical_path_varlen(cp, n, N, Tq, Tk, layout))
+    if r < 0:
+        raise StripedError(r, "striped_critical_path_varlen")
     return r
 
 

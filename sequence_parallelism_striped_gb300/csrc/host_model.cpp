@@ -86,6 +86,67 @@ int striped_tile_counts(int64_t S, int N, int Tq, int Tk, int layout, int64_t *f
     return STRIPED_OK;
 }
 
+// Packed sequences: each sequence is placed and tiled on its own, so a
+// device's work in round r is the sum of the sequences' tables.
+int striped_tile_counts_varlen(const int32_t *cu_seqlens, int nseq, int N, int Tq, int Tk, int layout,
+                               int64_t *full, int64_t *partial) {
+    if (!cu_seqlens || nseq < 1 || N < 1 || N > 4096 || cu_seqlens[0] != 0) return STRIPED_ERR_INVALID_ARG;
+    const size_t nn = (size_t)N * N;
+    int64_t *f = (int64_t *)malloc(sizeof(int64_t) * nn);
+    int64_t *p = (int64_t *)malloc(sizeof(int64_t) * nn);
+    if (!f || !p) {
+        free(f);
+        free(p);
+        return STRIPED_ERR_INVALID_ARG;
+    }
+    for (size_t x = 0; x < nn; ++x) {
+        if (full) full[x] = 0;
+        if (partial) partial[x] = 0;
+    }
+    int st = STRIPED_OK;
+    for (int i = 0; i < nseq && st == STRIPED_OK; ++i) {
+        const int64_t len = (int64_t)cu_seqlens[i + 1] - cu_seqlens[i];
+        if (len <= 0) {
+            st = STRIPED_ERR_INVALID_ARG;
+            break;
+        }
+        st = striped_tile_counts(len, N, Tq, Tk, layout, f, p);
+        for (size_t x = 0; x < nn && st == STRIPED_OK; ++x) {
+            if (full) full[x] += f[x];
+            if (partial) partial[x] += p[x];
+        }
+    }
+    free(f);
+    free(p);
+    return st;
+}
+
+int64_t striped_critical_path_varlen(const int32_t *cu_seqlens, int nseq, int N, int Tq, int Tk, int layout) {
+    if (N < 1 || N > 4096) return STRIPED_ERR_INVALID_ARG;
+    const size_t nn = (size_t)N * N;
+    int64_t *f = (int64_t *)malloc(sizeof(int64_t) * nn);
+    int64_t *p = (int64_t *)malloc(sizeof(int64_t) * nn);
+    if (!f || !p) {
+        free(f);
+        free(p);
+        return STRIPED_ERR_INVALID_ARG;
+    }
+    int64_t total = striped_tile_counts_varlen(cu_seqlens, nseq, N, Tq, Tk, layout, f, p);
+    if (total == STRIPED_OK) {
+        for (int r = 0; r < N; ++r) {
+            int64_t mx = 0;
+            for (int d = 0; d < N; ++d) {
+                const int64_t c = f[r * N + d] + p[r * N + d];
+                if (c > mx) mx = c;
+            }
+            total += mx;
+        }
+    }
+    free(f);
+    free(p);
+    return total;
+}
+
 int64_t striped_critical_path(int64_t S, int N, int Tq, int Tk, int layout) {
     if (N < 1 || N > 4096) return STRIPED_ERR_INVALID_ARG;
     int64_t *f = (int64_t *)malloc(sizeof(int64_t) * (size_t)N * N);

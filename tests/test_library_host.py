@@ -58,6 +58,32 @@ def test_zigzag_tile_counts_match_oracle_bruteforce(lib, S, N, Tq, Tk):
     assert sp.critical_path(S, N, Tq, Tk, sp.ZIGZAG) == oracle.critical_path(bf, bp)
 
 
+@pytest.mark.parametrize("layout", [sp.STRIPED, sp.CONTIGUOUS, sp.ZIGZAG])
+@pytest.mark.parametrize("N,cu,T", [(4, [0, 64, 192, 256], 16), (8, [0, 1024, 3072, 8192], 128),
+                                    (4, [0, 40, 48, 88], 4), (2, [0, 8, 12, 20, 32], 3)])
+def test_varlen_tile_counts_match_oracle(lib, N, cu, T, layout):
+    """Packed batch: the sum of the oracle's brute-force tables of the
+    sequences; the critical path takes the busiest device of that sum (not
+    the sum of the sequences' critical paths)."""
+    if layout == sp.ZIGZAG and any((b - a) % (2 * N) for a, b in zip(cu, cu[1:])):
+        pytest.skip("zig-zag needs every length a multiple of 2N")
+    full, part = sp.tile_counts_varlen(cu, N, T, T, layout)
+    bf = sum(oracle.tile_counts_bruteforce(b - a, N, T, T, layout)[0] for a, b in zip(cu, cu[1:]))
+    bp = sum(oracle.tile_counts_bruteforce(b - a, N, T, T, layout)[1] for a, b in zip(cu, cu[1:]))
+    assert np.array_equal(full, bf) and np.array_equal(part, bp)
+    assert sp.critical_path_varlen(cu, N, T, T, layout) == oracle.critical_path(bf, bp)
+
+
+def test_varlen_contiguous_critical_path_exceeds_striped(lib):
+    """Packing does not fix Ring Attention's imbalance: with several long
+    sequences the contiguous placement's critical path stays far above the
+    striped one."""
+    cu, N, T = [0, 8192, 16384, 24576, 32768], 8, 128
+    cs = sp.critical_path_varlen(cu, N, T, T, sp.STRIPED)
+    cc = sp.critical_path_varlen(cu, N, T, T, sp.CONTIGUOUS)
+    assert cc > 1.6 * cs
+
+
 def test_golden_tables(lib):
     gold = json.load(open(os.path.join(ROOT, "tests", "golden", "tile_counts.json")))
     for w in gold["workloads"]:
