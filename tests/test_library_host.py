@@ -164,6 +164,25 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert fwd_varlen(list(range(0, 513 * 512 + 1, 512))) == -2  # more than 512 sequences
     arr, n = cu([0, 6, 12])
     assert lib.striped_varlen_permute(fake, P(1 << 24), arr, n, 1, 64, 4, 2, 0, None) == -1
+    # NULL table, NULL tensors, misaligned tensors, bad head dimension
+    assert lib.striped_attn_fwd_varlen(fake, fake, fake, fake, fake, None, 2, 2, 2, 128, 4, 0, 0, 1.0, None,
+                                       None) == -1
+    arr, n = cu([0, 512, 1024])
+    assert lib.striped_attn_fwd_varlen(None, fake, fake, fake, fake, arr, n, 2, 2, 128, 4, 0, 0, 1.0, None,
+                                       None) == -1
+    assert lib.striped_attn_fwd_varlen(P((1 << 20) + 8), fake, fake, fake, fake, arr, n, 2, 2, 128, 4, 0, 0,
+                                       1.0, None, None) == -3
+    assert lib.striped_attn_fwd_varlen(fake, fake, fake, fake, fake, arr, n, 2, 2, 96, 4, 0, 0, 1.0, None,
+                                       None) == -2
+    assert lib.striped_attn_bwd_varlen(fake, fake, fake, fake, fake, fake, fake, fake, fake, fake, 16, arr, n, 2,
+                                       2, 128, 4, 0, 0, 1.0, None, None) == -6  # workspace too small
+    assert lib.striped_tile_counts_varlen(None, 2, 4, 16, 16, 0, None, None) == -1
+    assert lib.striped_critical_path_varlen(arr, n, 0, 16, 16, 0) < 0
+    # grouped-query: misaligned key/value tensor
+    assert lib.striped_attn_fwd_gqa(fake, P((1 << 20) + 4), fake, fake, fake, 1, 4, 2, 64, 128, 4, 0, 0, 1.0,
+                                    None, None) == -3
+    # bf16 head dimension 64 accepted by validation (fails later only on a NULL output)
+    assert lib.striped_attn_fwd(fake, fake, fake, None, fake, 1, 1, 64, 64, 4, 0, 0, 1.0, None, None) == -1
 
 
 def test_workspace_size(lib):
