@@ -13,14 +13,18 @@
 // Three kernels:
 //   bwd_pre    Delta_p = <dO_p, O_p> (fp32) and zero the fp32 dQ accumulator
 //   bwd_main   one CTA per 128-key tile; loops over the query tiles that see
-//              it.  warp 0 = TMA producer (K, V once; then Q_i with its
-//              statistics, 2 stages), warp 2 = TMA producer of dO_i (own
-//              2-stage stream), warp 1 = TMEM allocator + MMA issuer, warps
-//              4..11 = two compute warpgroups; thread t of a warpgroup owns
-//              key row t of S^T/dP^T (query row t of dQ), warpgroup 0 columns
-//              0..63 and warpgroup 1 columns 64..127.
+//              it (of every query head that reads its key/value head, with
+//              grouped-query attention, and of its own sequence only, with
+//              packed sequences).  warp 0 = TMA producer (K, V once; then
+//              Q_i with its statistics, 2 stages), warp 2 = TMA producer of
+//              dO_i (own 2-stage stream), warp 1 = TMEM allocator + MMA
+//              issuer, warps 4..11 = two compute warpgroups; thread t of a
+//              warpgroup owns key row t of S^T/dP^T (query row t of dQ),
+//              warpgroup 0 query columns 0..63 and head-dimension columns
+//              0..HD/2-1, warpgroup 1 the rest.  HD = 128 or 64.
 //              TMEM: S^T [0,128) (P^T bf16 pairs over it), dP^T [128,256)
-//              (dQ_i over it once dS_i is formed), dV [256,384), dK [384,512).
+//              (dQ_i over it once dS_i is formed), dV [256,256+HD),
+//              dK [256+HD,256+2HD).
 //                S^T  = K Q_i^T      SS, both K-major
 //                dP^T = V dO_i^T     SS, both K-major
 //                dV  += P^T dO_i     TS, A = P^T in TMEM, B = dO_i MN-major

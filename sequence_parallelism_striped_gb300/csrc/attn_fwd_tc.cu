@@ -8,13 +8,15 @@
 // per-round partial results are merged exactly (pith.science paper page,
 // abstract) -- here by an online softmax with a log-sum-exp accumulator.
 //
-// One CTA = one 128-row query tile of one (b, h, stripe):
-//   warp 0      TMA producer: K/V tiles into a 3-stage ring
+// One CTA = one 128-row query tile of one (b, h, stripe); K/V come from the
+// key/value head of h (grouped-query attention) and, with packed sequences,
+// only from the tiles of the query tile's own sequence.  HD = 128 or 64.
+//   warp 0      TMA producer: K/V tiles into a ring of stages (3 at HD = 128)
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
 //   warps 2..5  softmax + epilogue; thread t owns query row t (TMEM lane t)
 //               and first stores that row of Q into TMEM
-// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O [256,384),
-// Q [384,448) as bf16 pairs.
+// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O [256,256+HD),
+// Q [256+HD,256+3HD/2) as bf16 pairs.
 //   S_j = Q K_j^T            (TS MMA: A = Q from TMEM, B = K K-major;
 //                             M=N=128, K=16 x 8), so the tensor core reads
 //                             only K from shared memory for it
