@@ -67,6 +67,11 @@ int launch_simt_bwd(const float *q, const float *k, const float *v, const float 
 constexpr int kTcTile = 128;
 int launch_tc_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
                   const AttnGeom &g, int64_t *tile_stats, cudaStream_t stream);
+// attn_fwd_pair.cu: the batched forward with two query tiles (stripes d and
+// d+1) per CTA; STRIPED_ERR_UNSUPPORTED unless fwd_pair_eligible(g).
+bool fwd_pair_eligible(const AttnGeom &g);
+int launch_tc_fwd_pair(const void *q, const void *k, const void *v, void *o, float *lse,
+                       const AttnGeom &g, int64_t *tile_stats, cudaStream_t stream);
 int launch_tc_round(const void *q_d, const void *k_e, const void *v_e, float *o_acc, float *lse_acc,
                     void *o_out, int d, int e, int first, const AttnGeom &g, int64_t *tile_stats,
                     cudaStream_t stream);

@@ -72,6 +72,17 @@ def test_fwd_bf16_short_sequence_full(layout):
     _check_fwd(x, o, lse, stats, B, H, S, D, N, layout, torch.bfloat16)
 
 
+@pytest.mark.parametrize("B,H,S,D,N", [(2, 3, 4096, 128, 8),   # stripes of 4 whole tiles, 4 stripe pairs
+                                       (1, 2, 1024, 128, 2),   # one stripe pair
+                                       (1, 1, 3072, 128, 6),   # N = 6
+                                       (1, 2, 1536, 128, 3)])  # odd N: one query tile per CTA
+def test_fwd_bf16_stripe_pairs(B, H, S, D, N):
+    """Whole-tile stripes and an even N: the forward runs the query tiles
+    of stripes d and d + 1 in one CTA on one K/V stream."""
+    x, o, lse, stats = _run_fwd(B, H, S, D, N, sp.STRIPED, torch.bfloat16, seed=4)
+    _check_fwd(x, o, lse, stats, B, H, S, D, N, sp.STRIPED, torch.bfloat16)
+
+
 @pytest.mark.parametrize("B,H,S,D,N", [(1, 1, 256, 64, 4), (1, 2, 128, 32, 4), (2, 1, 256, 128, 8),
                                        (1, 1, 64, 64, 1), (1, 1, 512, 64, 16)])
 def test_fwd_fp32_zigzag(B, H, S, D, N):
