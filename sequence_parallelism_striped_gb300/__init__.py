@@ -79,6 +79,7 @@ def load(build_if_missing: bool = True):
         lib.striped_attn_bwd_varlen.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, P, I, I64, I64, I64, I, I, I,
                                                 F, P, P]
         lib.striped_kernel_tile.argtypes = [I, I64, P, P]
+        lib.striped_fwd_query_tiles_per_cta.argtypes = [I64, I64, I64, I64, I, I, I, I]
         lib.striped_tile_counts.argtypes = [I64, I, I, I, I, P, P]
         lib.striped_critical_path.argtypes = [I64, I, I, I, I]
         lib.striped_critical_path.restype = I64
@@ -167,6 +168,20 @@ def kernel_tile(dtype: torch.dtype, D: int) -> int:
     code = BF16 if dtype == torch.bfloat16 else FP32
     _check(load().striped_kernel_tile(code, D, ctypes.byref(tq), ctypes.byref(tk)), "striped_kernel_tile")
     return tq.value
+
+
+def fwd_query_tiles_per_cta(B: int, H: int, S: int, D: int, N: int, layout: int = STRIPED,
+                            dtype: torch.dtype = torch.bfloat16, num_sms: int | None = None) -> int:
+    """Query tiles one forward CTA runs (1, or 2 for the stripe-pair
+    schedule) on a GPU with num_sms multiprocessors (default: the current
+    CUDA device's)."""
+    if num_sms is None:
+        num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    code = BF16 if dtype == torch.bfloat16 else FP32
+    r = load().striped_fwd_query_tiles_per_cta(B, H, S, D, N, layout, code, num_sms)
+    if r < 0:
+        raise StripedError(r, "striped_fwd_query_tiles_per_cta")
+    return r
 
 
 def new_tile_stats(N: int, device) -> torch.Tensor:

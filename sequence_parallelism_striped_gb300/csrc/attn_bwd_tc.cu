@@ -679,7 +679,9 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const float *__restrict__
     }
 }
 
-int num_sms() {
+}  // namespace
+
+int device_sm_count() {
     static int n = 0;
     if (!n) {
         int dev = 0;
@@ -689,8 +691,6 @@ int num_sms() {
     }
     return n;
 }
-
-}  // namespace
 
 namespace {
 
@@ -710,7 +710,7 @@ int launch_bwd_hd(const void *q, const void *k, const void *v, const void *o, co
     }
     if (attr != STRIPED_OK) return attr;
     const int64_t rows = g.BH * g.N * g.L;
-    const int sms = num_sms();
+    const int sms = device_sm_count();
     const int nq = (int)((g.L + BT - 1) / BT);
     bwd_pre_kernel<HD><<<sms * 8, 256, 0, stream>>>((const __nv_bfloat16 *)o, (const __nv_bfloat16 *)dO, lse,
                                                     stats, dq_acc, g.L, nq, g.BH * g.N * (int64_t)nq * BT);

@@ -11,8 +11,9 @@
 //     PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
 // so that while one group turns S into P the tensor core works for the
 // other group.  Used for the batched striped forward when every stripe is a
-// whole number of tiles, N is even and the head dimension is 128; the
-// one-tile kernel serves every other case.
+// whole number of tiles, N is even, the head dimension is 128 and the grid
+// stays balanced (fwd_pair_eligible); the one-tile kernel serves every other
+// case.
 //
 //   warp 0      TMA producer: Q_A, Q_B once, then K/V tiles (2 stages)
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
@@ -328,14 +329,28 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
 }  // namespace
 
-bool fwd_pair_eligible(const AttnGeom &g) {
-    return g.layout == STRIPED_LAYOUT_STRIPED && g.D == PHD && g.seqs.n == 0 && g.N % 2 == 0 && g.L > 0 &&
-           g.L % PB == 0;
+// Shape rule, then balance: a pair CTA carries twice the key tiles of a
+// one-tile CTA and the grid has half as many CTAs, so short sequences (few
+// query tiles per multiprocessor) leave SMs idle behind the heaviest CTAs.
+// The pair schedule is taken when twice the heaviest CTA's key tiles,
+// 2 * nq * N, fit into the average key tiles per multiprocessor,
+// BH * N^2 * nq (nq + 1) / 2 / num_sms (measured on GB300: at B=1, H=8,
+// N=8 the pair forward is 16% slower at S = 8192, where the rule declines
+// it, and 4.5% faster at S = 65536).
+bool fwd_pair_eligible(const AttnGeom &g, int num_sms) {
+    if (!(g.layout == STRIPED_LAYOUT_STRIPED && g.D == PHD && g.seqs.n == 0 && g.N % 2 == 0 && g.L > 0 &&
+          g.L % PB == 0) ||
+        num_sms < 1)
+        return false;
+    const double nq = (double)(g.L / PB);
+    const double total = (double)g.BH * g.N * g.N * nq * (nq + 1.0) / 2.0;
+    const double heaviest = 2.0 * nq * g.N;
+    return 2.0 * heaviest * num_sms <= total;
 }
 
 int launch_tc_fwd_pair(const void *q, const void *k, const void *v, void *o, float *lse, const AttnGeom &g,
                        int64_t *tile_stats, cudaStream_t stream) {
-    if (!fwd_pair_eligible(g)) return STRIPED_ERR_UNSUPPORTED;
+    if (!fwd_pair_eligible(g, device_sm_count())) return STRIPED_ERR_UNSUPPORTED;
     static int attr = 1;
     if (attr == 1)
         attr = cuda_status(cudaFuncSetAttribute(tc_fwd_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

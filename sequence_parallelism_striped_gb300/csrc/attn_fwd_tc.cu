@@ -505,7 +505,7 @@ static int launch_round_hd(const CUtensorMap &mk, const CUtensorMap &mv, const F
 
 int launch_tc_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
                   const AttnGeom &g, int64_t *tile_stats, cudaStream_t stream) {
-    if (fwd_pair_eligible(g)) return launch_tc_fwd_pair(q, k, v, o, lse, g, tile_stats, stream);
+    if (fwd_pair_eligible(g, device_sm_count())) return launch_tc_fwd_pair(q, k, v, o, lse, g, tile_stats, stream);
     int st = STRIPED_OK;
     CUtensorMap mk, mv;
     const int64_t bh_kv = g.BH / g.G;

@@ -68,8 +68,12 @@ constexpr int kTcTile = 128;
 int launch_tc_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
                   const AttnGeom &g, int64_t *tile_stats, cudaStream_t stream);
 // attn_fwd_pair.cu: the batched forward with two query tiles (stripes d and
-// d+1) per CTA; STRIPED_ERR_UNSUPPORTED unless fwd_pair_eligible(g).
-bool fwd_pair_eligible(const AttnGeom &g);
+// d+1) per CTA; STRIPED_ERR_UNSUPPORTED unless fwd_pair_eligible(g, sms)
+// with the current device's multiprocessor count.
+bool fwd_pair_eligible(const AttnGeom &g, int num_sms);
+// Multiprocessor count of the current device (queried once; 152 if the
+// query fails).
+int device_sm_count();
 int launch_tc_fwd_pair(const void *q, const void *k, const void *v, void *o, float *lse,
                        const AttnGeom &g, int64_t *tile_stats, cudaStream_t stream);
 int launch_tc_round(const void *q_d, const void *k_e, const void *v_e, float *o_acc, float *lse_acc,

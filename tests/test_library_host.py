@@ -105,6 +105,49 @@ def test_kernel_tiles(lib):
         sp.kernel_tile(torch.bfloat16, 96)
 
 
+def test_forward_schedule_rule(lib):
+    """Stripe-pair forward (2 query tiles per CTA) only for bf16, D = 128,
+    striped, whole-tile stripes, even N, and a balanced grid: twice the
+    heaviest pair CTA's key tiles (2 * nq * N) at most the average key
+    tiles per multiprocessor, the total taken from the oracle's table."""
+    import torch
+
+    sms = 152
+    cases = [(1, 32, 262144, 8), (1, 8, 65536, 8), (1, 8, 8192, 8), (1, 24, 8192, 8), (2, 24, 4096, 2),
+             (1, 24, 6144, 6), (1, 8, 16384, 8), (1, 8, 32768, 8), (4, 32, 2048, 8), (1, 2, 1536, 3),
+             (1, 2, 1200, 4), (1, 64, 1024, 4)]
+    seen = set()
+    for B, H, S, N in cases:
+        L = S // N
+        full, part = oracle.tile_counts_closed(S, N, 128, sp.STRIPED) if L % 128 == 0 else (None, None)
+        if L % 128 == 0 and N % 2 == 0:
+            total = B * H * int(full.sum() + part.sum())
+            heaviest = 2 * (L // 128) * N
+            want = 2 if 2 * heaviest * sms <= total else 1
+        else:
+            want = 1
+        got = sp.fwd_query_tiles_per_cta(B, H, S, 128, N, sp.STRIPED, torch.bfloat16, num_sms=sms)
+        assert got == want, (B, H, S, N)
+        seen.add(got)
+    assert seen == {1, 2}
+    # the benchmark sizes take the pair schedule, the short-sequence one does not
+    assert sp.fwd_query_tiles_per_cta(1, 32, 262144, 128, 8, num_sms=sms) == 2
+    assert sp.fwd_query_tiles_per_cta(1, 8, 8192, 128, 8, num_sms=sms) == 1
+    # every other kernel configuration: one query tile per CTA
+    for layout in (sp.CONTIGUOUS, sp.ZIGZAG):
+        assert sp.fwd_query_tiles_per_cta(1, 32, 262144, 128, 8, layout, num_sms=sms) == 1
+    assert sp.fwd_query_tiles_per_cta(1, 32, 262144, 64, 8, num_sms=sms) == 1
+    assert sp.fwd_query_tiles_per_cta(1, 4, 4096, 64, 8, dtype=torch.float32, num_sms=sms) == 1
+    # more multiprocessors need more work per head before pairs pay
+    assert sp.fwd_query_tiles_per_cta(1, 24, 8192, 128, 8, num_sms=1000) == 1
+    for bad in ((1, 32, 262144, 96, 8, sp.STRIPED, torch.bfloat16, sms),
+                (1, 32, 262144, 128, 8, sp.STRIPED, torch.bfloat16, 0),
+                (1, 32, 262144, 128, 8, 7, torch.bfloat16, sms),
+                (1, 32, 262143, 128, 8, sp.STRIPED, torch.bfloat16, sms)):
+        with pytest.raises(sp.StripedError):
+            sp.fwd_query_tiles_per_cta(*bad[:5], bad[5], bad[6], num_sms=bad[7])
+
+
 def test_invalid_arguments_rejected_on_host(lib):
     P = ctypes.c_void_p
     fake = P(1 << 20)  # never dereferenced: validation fails first
