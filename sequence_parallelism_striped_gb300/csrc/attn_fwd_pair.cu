@@ -272,7 +272,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     }
                     tc_fence_after();
                     if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
+                        // rare (lazy rescale): one 32-column chunk at a time
+                        // keeps the softmax thread within its registers
+#pragma unroll 1
                         for (int c = 0; c < PHD / 32; ++c) {
                             uint32_t rr[32];
                             tmem_ld32(tO + c * 32, rr);
