@@ -80,8 +80,19 @@ def test_fwd_bf16_short_sequence_full(layout):
 def test_fwd_bf16_stripe_pairs(B, H, S, D, N, pairs):
     """Whole-tile stripes, an even N and enough work per multiprocessor: the
     forward runs the query tiles of stripes d and d + 1 in one CTA on one
-    K/V stream (checked against the oracle on a few heads of each batch)."""
-    assert sp.fwd_query_tiles_per_cta(B, H, S, D, N, sp.STRIPED) == pairs
+    K/V stream (checked against the oracle on a few heads of each batch).
+    `pairs` is the schedule on a 152-SM GB300; the balance rule is
+    re-derived here for the device the test runs on."""
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    L = S // N
+    nq = L // 128
+    if N % 2 == 0 and L % 128 == 0:
+        want = 2 if 2 * (2 * nq * N) * sms <= B * H * N * N * nq * (nq + 1) // 2 else 1
+    else:
+        want = 1
+    if sms == 152:
+        assert want == pairs
+    assert sp.fwd_query_tiles_per_cta(B, H, S, D, N, sp.STRIPED) == want
     x, o, lse, stats = _run_fwd(B, H, S, D, N, sp.STRIPED, torch.bfloat16, seed=4)
     heads = sorted({0, H // 2, H - 1})
     _check_fwd(x, o, lse, stats, B, H, S, D, N, sp.STRIPED, torch.bfloat16, heads=heads)
