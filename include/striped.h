@@ -40,8 +40,15 @@
  *  - Every call returns an int status (STRIPED_OK or a negative code) and
  *    never throws.  Launch failures return STRIPED_ERR_CUDA (the CUDA error
  *    code is kept in striped_last_cuda_error()).  A device-side bounded wait
- *    that expires records STRIPED_ERR_TIMEOUT in a device error word that
- *    striped_check_error() reads back.
+ *    that expires (2 s by default) records STRIPED_ERR_TIMEOUT in a device
+ *    error word that striped_check_error() reads back.  There is ONE error
+ *    word per device, shared by every stream and every caller on it: a
+ *    timeout is reported to whichever caller next calls
+ *    striped_check_error() on that device.
+ *  - The library caches per-device addresses (its status block, the
+ *    no-allocation scratch array) and kernel attributes the first time it
+ *    runs on a device; after cudaDeviceReset() on a device, do not use the
+ *    library on that device again in the same process.
  *  - `scale` multiplies the scores q.k (pass 1/sqrt(D) for the usual scaled
  *    dot product).
  *  - `tile_stats`, when not NULL, is an int64 [2][N][N] DEVICE array that
@@ -305,8 +312,10 @@ int striped_tile_counts_varlen(const int32_t *cu_seqlens, int nseq, int N, int T
  * at the pace of the device with the most tiles over all its sequences). */
 int64_t striped_critical_path_varlen(const int32_t *cu_seqlens, int nseq, int N, int Tq, int Tk, int layout);
 
-/* Synchronises `stream`, then reads and clears the device error word.
- * Returns STRIPED_OK, STRIPED_ERR_TIMEOUT or STRIPED_ERR_CUDA. */
+/* Synchronises `stream`, then reads and clears the error word of the
+ * current device (one per device, not per stream; see the conventions).
+ * Returns STRIPED_OK, STRIPED_ERR_TIMEOUT, STRIPED_ERR_ALIGN or
+ * STRIPED_ERR_CUDA. */
 int striped_check_error(void *stream);
 
 /* Human-readable name of a status code (static string). */
@@ -323,6 +332,30 @@ int striped_last_cuda_error(void);
  * trap or hang is involved.
  */
 int striped_selftest_timeout(int64_t spins, void *stream);
+
+/*
+ * TEST HOOK (not for production use): checks that the attention kernels'
+ * own bounded waits end, report STRIPED_ERR_TIMEOUT and leave the device
+ * usable.  Synchronises the current device, then sets for every later launch
+ * on it:
+ *  - wait_limit_ns: the bound of every device-side wait (<= 0 restores the
+ *    default 2 s);
+ *  - fault: STRIPED_FAULT_NONE, or STRIPED_FAULT_FWD_SKIP_KV (the forward
+ *    kernels' TMA producer never loads its first K/V tile) or
+ *    STRIPED_FAULT_BWD_SKIP_Q (the tensor-core backward's producer never
+ *    loads its first Q tile).  Every wait on the missing tile runs out; each
+ *    CTA then records the timeout, waits (bounded) for its own copies and
+ *    tensor-core operations in flight, frees its tensor memory and returns.
+ *    No fault, trap or hang is involved; results of such a launch are
+ *    garbage.
+ * Restore with striped_test_inject(STRIPED_FAULT_NONE, 0).  Returns
+ * STRIPED_ERR_INVALID_ARG for an unknown fault, else STRIPED_OK or
+ * STRIPED_ERR_CUDA.
+ */
+#define STRIPED_FAULT_NONE 0
+#define STRIPED_FAULT_FWD_SKIP_KV 1
+#define STRIPED_FAULT_BWD_SKIP_Q 2
+int striped_test_inject(int fault, int64_t wait_limit_ns);
 
 #ifdef __cplusplus
 }

@@ -23,6 +23,9 @@ CONTIGUOUS = 1
 ZIGZAG = 2
 BF16 = 0
 FP32 = 1
+FAULT_NONE = 0
+FAULT_FWD_SKIP_KV = 1
+FAULT_BWD_SKIP_Q = 2
 
 _STATUS = {
     0: "ok", -1: "invalid argument", -2: "unsupported configuration", -3: "misaligned",
@@ -91,6 +94,7 @@ def load(build_if_missing: bool = True):
         lib.striped_status_string.restype = ctypes.c_char_p
         lib.striped_last_cuda_error.argtypes = []
         lib.striped_selftest_timeout.argtypes = [I64, P]
+        lib.striped_test_inject.argtypes = [I, I64]
         _lib = lib
         return lib
 
@@ -403,6 +407,13 @@ def check_error(stream=None) -> int:
 
 def selftest_timeout(spins: int, stream=None):
     _check(load().striped_selftest_timeout(int(spins), _stream(stream)), "striped_selftest_timeout")
+
+
+def test_inject(fault: int, wait_limit_ns: int = 0):
+    """TEST HOOK: make the kernels skip one of their loads (FAULT_*) and/or
+    bound every device-side wait by wait_limit_ns (<= 0: the 2 s default)
+    for every later launch on the current device; (FAULT_NONE, 0) restores."""
+    _check(load().striped_test_inject(int(fault), int(wait_limit_ns)), "striped_test_inject")
 
 
 def status_string(status: int) -> str:

@@ -1,24 +1,33 @@
 // api.cu -- the C entry points of libstriped (declared in include/striped.h):
 // argument validation, status codes, tensor-map construction, the host-side
-// tile/critical-path model and the device error word.
+// tile/critical-path model and the device status block.
+#include <stddef.h>
 #include <stdio.h>
 #include <string.h>
+
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
 
 namespace striped {
 
-__device__ int g_error_word = 0;
+// The library's status block on every device that loads it (see
+// DeviceStatus): the error word striped_check_error() reads, the bound of
+// every device-side wait, and the test hook.  One block per device, shared
+// by every stream and caller on that device.
+__device__ DeviceStatus g_status = {0, kInjectNone, kDefaultWaitLimitNs};
 
-int *device_error_word() {
-    static int *cache[256] = {nullptr};
+DeviceStatus *device_status() {
+    static std::mutex mu;
+    static DeviceStatus *cache[256] = {nullptr};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
     if (!cache[dev]) {
         void *ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_error_word) != cudaSuccess) return nullptr;
-        cache[dev] = static_cast<int *>(ptr);
+        if (cudaGetSymbolAddress(&ptr, g_status) != cudaSuccess) return nullptr;
+        cache[dev] = static_cast<DeviceStatus *>(ptr);
     }
     return cache[dev];
 }
@@ -42,17 +51,20 @@ typedef CUresult (*EncodeTiledFnT)(CUtensorMap *, CUtensorMapDataType, cuuint32_
 static int make_map(CUtensorMap *map, CUtensorMapDataType dt, int64_t esize, const void *base, int64_t D,
                     int64_t L, int64_t N, int64_t BH, int64_t stripe_stride, int64_t stride_bh, int box_x,
                     int box_rows) {
+    // the driver entry point is process-wide: resolved once, under a lock
+    static std::mutex mu;
     static EncodeTiledFnT fn = nullptr;
-    static int resolved = 0;
-    if (!resolved) {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                                         cudaEnableDefault, &q);
-        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !ptr)
-            return cuda_status(e != cudaSuccess ? e : cudaErrorNotSupported);
-        fn = reinterpret_cast<EncodeTiledFnT>(ptr);
-        resolved = 1;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!fn) {
+            void *ptr = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                                             cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !ptr)
+                return cuda_status(e != cudaSuccess ? e : cudaErrorNotSupported);
+            fn = reinterpret_cast<EncodeTiledFnT>(ptr);
+        }
     }
     cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)N, (cuuint64_t)BH};
     cuuint64_t strides[3] = {(cuuint64_t)(D * esize), (cuuint64_t)(stripe_stride * esize),
@@ -145,7 +157,7 @@ __global__ void selftest_wait_kernel(int64_t spins) {
     const volatile int *flag = &g_selftest_flag;
     for (int64_t it = 0; it < spins; ++it)
         if (*flag != 0) return;
-    atomicExch(&g_error_word, STRIPED_ERR_TIMEOUT);
+    atomicExch(&g_status.error, STRIPED_ERR_TIMEOUT);
 }
 
 }  // namespace striped
@@ -173,14 +185,24 @@ int striped_check_error(void *stream) {
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_status(e);
     int word = 0, zero = 0;
-    e = cudaMemcpyFromSymbol(&word, g_error_word, sizeof(int));
+    e = cudaMemcpyFromSymbol(&word, g_status, sizeof(int), offsetof(DeviceStatus, error));
     if (e != cudaSuccess) return cuda_status(e);
     if (word != 0) {
-        e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int));
+        e = cudaMemcpyToSymbol(g_status, &zero, sizeof(int), offsetof(DeviceStatus, error));
         if (e != cudaSuccess) return cuda_status(e);
         return word;
     }
     return STRIPED_OK;
+}
+
+int striped_test_inject(int fault, int64_t wait_limit_ns) {
+    if (fault < kInjectNone || fault > kInjectBwdSkipQ) return STRIPED_ERR_INVALID_ARG;
+    const unsigned long long limit = wait_limit_ns > 0 ? (unsigned long long)wait_limit_ns : kDefaultWaitLimitNs;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_status, &fault, sizeof(int), offsetof(DeviceStatus, inject));
+    if (e == cudaSuccess)
+        e = cudaMemcpyToSymbol(g_status, &limit, sizeof(limit), offsetof(DeviceStatus, wait_limit_ns));
+    return cuda_status(e);
 }
 
 int striped_selftest_timeout(int64_t spins, void *stream) {

@@ -28,8 +28,11 @@ constexpr size_t kNoAllocScratchBytes = size_t(48) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Device address of the scratch array on the current device, looked up once
-// per device (the host-side symbol is only a stand-in, never a device
-// address).  Returns a status code.
+// per device with that device current (the host-side symbol is only a
+// stand-in, never a device address).  The address belongs to the device's
+// context: after cudaDeviceReset() it would be stale, and the library is
+// not to be used on a reset device again (see striped.h).  Returns a
+// status code.
 static int noalloc_scratch(void **out) {
     static std::mutex mu;
     static void *cache[256] = {nullptr};

@@ -77,7 +77,7 @@ struct BwdParams {
     float *dq_acc;       // [BH][S][D] fp32
     __nv_bfloat16 *dk, *dv;
     int64_t *tile_stats;
-    int *err;
+    DeviceStatus *err;
 };
 
 struct Bars {
@@ -85,6 +85,7 @@ struct Bars {
     uint64_t q_full[QS], q_empty[QS];    // Q_i + statistics of tile i
     uint64_t do_full[QS], do_empty[QS];  // dO_i (its buffer also stages half of dQ_i)
     uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, dq_free, acc_done;
+    uint64_t drain;  // every MMA of the issuer has completed (before TMEM is freed)
     uint32_t tmem_slot;
 };
 
@@ -157,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw;
     if ((smem_u32(smem) & 1023u) != 0) {  // operand tiles need 1024-byte alignment
-        if (threadIdx.x == 0 && p.err) atomicExch(p.err, STRIPED_ERR_ALIGN);
+        if (threadIdx.x == 0) record_error(p.err, STRIPED_ERR_ALIGN);
         return;
     }
     Bars *bars = reinterpret_cast<Bars *>(smem + Cfg::kBarOff);
@@ -205,19 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&bars->dq_full), 1);
         mbar_init(smem_u32(&bars->dq_free), 8);
         mbar_init(smem_u32(&bars->acc_done), 1);
+        mbar_init(smem_u32(&bars->drain), 1);
         fence_barrier_init();
-        if (p.tile_stats) {
-            for (int d = 0; d < N; ++d) {
-                const QuerySpan sp = query_span(g.layout, d, e, b, nqs, rows_b);
-                const int cnt = nqs - sp.a_lo;
-                if (cnt == 0) continue;
-                const int rr = ring_round_of(d, e, N);
-                atomicAdd((unsigned long long *)&p.tile_stats[rr * N + d],
-                          (unsigned long long)(G * (cnt - sp.has_diag)));
-                atomicAdd((unsigned long long *)&p.tile_stats[N * N + rr * N + d],
-                          (unsigned long long)(G * sp.has_diag));
-            }
-        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&bars->tmem_slot), 512);
@@ -241,10 +231,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int x = 0; x < kBoxes; ++x) tma_load_4d(sbase + kKOff + x * kBox, &tmK, kb, 64 * x, bg * BT, e, (int)bh);
 #pragma unroll
         for (int x = 0; x < kBoxes; ++x) tma_load_4d(sbase + kVOff + x * kBox, &tmV, kb, 64 * x, bg * BT, e, (int)bh);
+        // test hook: the first Q tile is never loaded, so every wait on it
+        // runs out (the kernel must then record the timeout and return)
+        const bool skip_first = injected_fault(p.err) == kInjectBwdSkipQ;
         QTileIter it = qiter_begin(g.layout, N, G, e, b, nqs, rows_b);
-        for (int i = 0; i < nt; ++i, qiter_next(it, g.layout, N, G, e, b, nqs, rows_b)) {
+        int i = 0;
+        for (; i < nt; ++i, qiter_next(it, g.layout, N, G, e, b, nqs, rows_b)) {
             const int s = i % QS;
             if (i >= QS && !mbar_wait(smem_u32(&bars->q_empty[s]), ((i / QS) + 1) & 1, p.err)) break;
+            if (skip_first && i == 0) continue;
             const uint32_t fb = smem_u32(&bars->q_full[s]);
             const uint32_t qdst = sbase + kQOff + s * 2 * kTile;
             const int64_t bq = bh * G + it.h;  // query head
@@ -255,12 +250,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int x = 0; x < kBoxes; ++x)
                 tma_load_4d(qdst + x * kBox, &tmQ, fb, 64 * x, (qbase + it.a) * BT, it.d, (int)bq);
         }
+        // K, V and loads [0, i) were issued: wait (bounded) for the last of
+        // each stage, so that on an error path none lands after the CTA exits
+        mbar_wait(kb, 0, p.err);
+        for (int t = i > QS ? i - QS : 0; t < i; ++t)
+            if (!(skip_first && t == 0)) mbar_wait(smem_u32(&bars->q_full[t % QS]), (t / QS) & 1, p.err);
     } else if (warp == 2 && lane == 0 && nt > 0) {
         // ---------------- TMA producer: dO_i (its own stream: the buffer is
         // released later than Q_i's, after the dQ_i half staged in it is read)
         tma_prefetch_desc(&tmdO);
         QTileIter it = qiter_begin(g.layout, N, G, e, b, nqs, rows_b);
-        for (int i = 0; i < nt; ++i, qiter_next(it, g.layout, N, G, e, b, nqs, rows_b)) {
+        int i = 0;
+        for (; i < nt; ++i, qiter_next(it, g.layout, N, G, e, b, nqs, rows_b)) {
             const int s = i % QS;
             if (i >= QS && !mbar_wait(smem_u32(&bars->do_empty[s]), ((i / QS) + 1) & 1, p.err)) break;
             const uint32_t fb = smem_u32(&bars->do_full[s]);
@@ -271,6 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int x = 0; x < kBoxes; ++x)
                 tma_load_4d(odst + x * kBox, &tmdO, fb, 64 * x, (qbase + it.a) * BT, it.d, bq);
         }
+        for (int t = i > QS ? i - QS : 0; t < i; ++t)  // in-flight loads, as above
+            mbar_wait(smem_u32(&bars->do_full[t % QS]), (t / QS) & 1, p.err);
     } else if (warp == 1 && lane == 0 && nt > 0) {
         // ---------------- MMA issuer
         // Per query tile i (TMEM: S = S^T then P^T; DP = dP^T then dQ_i):
@@ -344,6 +347,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (ok) mma_commit(smem_u32(&bars->acc_done));
+        // every MMA issued above completes before TMEM is freed (error paths)
+        mma_commit(smem_u32(&bars->drain));
+        mbar_wait(smem_u32(&bars->drain), 0, p.err);
     } else if (warp >= 4) {
         // ---------------- compute: two warpgroups split the 128 query columns
         // of S^T/dP^T (64 each) and the HD columns of dQ_i, dK, dV (HD/2 each)
@@ -413,6 +419,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pending = -1;
             }
         };
+        // tiles that ran, per query stripe: counted by one thread as their dS
+        // is formed and added to the (round, device) counter when the stripe
+        // changes
+        int cnt_d = -1, n_full = 0, n_part = 0;
+        auto flush_counts = [&]() {
+            if (p.tile_stats && cnt_d >= 0 && (n_full | n_part)) {
+                const int rr = ring_round_of(cnt_d, e, N);
+                atomicAdd((unsigned long long *)&p.tile_stats[rr * N + cnt_d], (unsigned long long)n_full);
+                atomicAdd((unsigned long long *)&p.tile_stats[N * N + rr * N + cnt_d], (unsigned long long)n_part);
+            }
+            n_full = n_part = 0;
+        };
+        const bool counter = warp == 4 && lane == 0;
         if (ok) ok = compute_p(cur, 0);
         for (int i = 0; i < nt && ok; ++i) {
             // ---- dS = P * (dP - Delta) -> smem (A operand of dQ and dK)
@@ -447,6 +466,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready));
+            if (counter) {
+                if (cur.d != cnt_d) {
+                    flush_counts();
+                    cnt_d = cur.d;
+                }
+                if (cur.has_diag && cur.a == cur.a_lo) ++n_part;
+                else ++n_full;
+            }
             // the previous tile's dQ reduce has had dS_i's time to read its
             // staging: return that dO buffer to the producer now
             if (wg == 1 && lane == 0) release_pending();
@@ -561,6 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        if (counter) flush_counts();
         if (wg == 1 && lane == 0) release_pending();
         if (lane == 0) bulk_wait_group0();
         if (ok) {
@@ -682,14 +710,14 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const float *__restrict__
 }  // namespace
 
 int device_sm_count() {
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0) n = 152;
-    }
-    return n;
+    static PerDeviceOnce once;
+    return once.get([] {
+        int dev = 0, n = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 152;
+        return n;
+    });
 }
 
 namespace {
@@ -699,15 +727,15 @@ int launch_bwd_hd(const void *q, const void *k, const void *v, const void *o, co
                   void *dq, void *dk, void *dv, float *dq_acc, float *stats, const AttnGeom &g, int64_t *tile_stats,
                   cudaStream_t stream) {
     constexpr size_t kSmemBytes = BwdCfg<HD>::kSmemBytes;
-    static int attr = 1;
-    if (attr == 1) {
+    static PerDeviceOnce attr_once;
+    const int attr = attr_once.get([] {
         cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel<HD, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)kSmemBytes);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(tc_bwd_kernel<HD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kSmemBytes);
-        attr = cuda_status(e);
-    }
+        return cuda_status(e);
+    });
     if (attr != STRIPED_OK) return attr;
     const int64_t rows = g.BH * g.N * g.L;
     const int sms = device_sm_count();
@@ -732,7 +760,7 @@ int launch_bwd_hd(const void *q, const void *k, const void *v, const void *o, co
     p.dk = (__nv_bfloat16 *)dk;
     p.dv = (__nv_bfloat16 *)dv;
     p.tile_stats = tile_stats;
-    p.err = device_error_word();
+    p.err = device_status();
     const int64_t nk = (g.L + BT - 1) / BT;
     const int64_t nblocks = nk * g.N * bh_kv;  // one CTA per key tile of every key/value head
     if (nblocks > 0x7fffffffll) return STRIPED_ERR_UNSUPPORTED;

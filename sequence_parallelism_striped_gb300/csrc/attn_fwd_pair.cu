@@ -48,6 +48,7 @@ struct PairBars {
     uint64_t q_full;
     uint64_t kv_full[PNS], kv_empty[PNS];
     uint64_t s_full[2], p_ready[2], o_done[2];  // per softmax group
+    uint64_t drain;                             // every MMA of the issuer has completed
     uint32_t tmem_slot;
 };
 
@@ -56,7 +57,7 @@ struct PairParams {
     __nv_bfloat16 *o;
     float *lse;
     int64_t *tile_stats;
-    int *err;
+    DeviceStatus *err;
 };
 
 __global__ void __launch_bounds__(kPThreads, 1)
@@ -95,17 +96,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
             mbar_init(smem_u32(&bars->p_ready[x]), 4);
             mbar_init(smem_u32(&bars->o_done[x]), 1);
         }
+        mbar_init(smem_u32(&bars->drain), 1);
         fence_barrier_init();
-        if (p.tile_stats) {
-            for (int x = 0; x < 2; ++x) {
-                const int d = d0 + x;
-                for (int e = 0; e < N; ++e) {
-                    const int rr = ring_round_of(d, e, N);
-                    atomicAdd((unsigned long long *)&p.tile_stats[rr * N + d], (unsigned long long)a);
-                    atomicAdd((unsigned long long *)&p.tile_stats[N * N + rr * N + d], 1ull);
-                }
-            }
-        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&bars->tmem_slot), 512);
@@ -127,6 +119,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
             tma_load_4d(sbase + kPQOff + x * kPTile, &tmQ, qb, 0, a * PB, d0 + x, (int)bh);
             tma_load_4d(sbase + kPQOff + x * kPTile + kPBox, &tmQ, qb, 64, a * PB, d0 + x, (int)bh);
         }
+        // test hook: the first K/V tile is never loaded, so every wait on it
+        // runs out (the kernel must then record the timeout and return)
+        const bool skip_first = injected_fault(p.err) == kInjectFwdSkipKV;
         int j = 0;
         for (int e = 0; e < N; ++e) {
             bool ok = true;
@@ -136,6 +131,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     ok = false;
                     break;
                 }
+                if (skip_first && j == 0) continue;
                 const uint32_t fb = smem_u32(&bars->kv_full[s]);
                 const uint32_t kdst = sbase + kPKVOff + s * kPStage;
                 const uint32_t vdst = kdst + kPTile;
@@ -147,6 +143,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             if (!ok) break;
         }
+        // loads [0, j) and Q were issued: wait (bounded) for the last of each
+        // stage, so that on an error path none lands after the CTA has exited
+        mbar_wait(qb, 0, p.err);
+        for (int t = j > PNS ? j - PNS : 0; t < j; ++t)
+            if (!(skip_first && t == 0)) mbar_wait(smem_u32(&bars->kv_full[t % PNS]), (t / PNS) & 1, p.err);
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
         constexpr uint32_t idesc_qk = idesc_bf16_f32(PB, PB, false, false);
@@ -188,6 +189,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (j + PNS < nt) mma_commit(smem_u32(&bars->kv_empty[j % PNS]));
             if (j + 1 < nt && !issue_s(1, j + 1)) break;
         }
+        // every MMA issued above completes before TMEM is freed (error paths)
+        mma_commit(smem_u32(&bars->drain));
+        mbar_wait(smem_u32(&bars->drain), 0, p.err);
     } else if (warp >= 2) {
         // ---------------- softmax + epilogue of one query tile
         const int x = (warp - 2) >> 2;       // group: 0 (stripe d0) or 1 (stripe d0 + 1)
@@ -201,7 +205,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
         int j = 0;
         bool ok = true;
         for (int e = 0; e < N && ok; ++e) {
-            const int lim_diag = ri + ((e <= d) ? 0 : -1);  // keep key column <= lim on the diagonal tile
+            // key tiles 0 .. nfull-1 in full, tile nfull (= a) under the
+            // striped diagonal mask: keep key column <= row + diag_off
+            const RoundSpan sp = round_span(STRIPED_LAYOUT_STRIPED, d, e, a, nq, PB);
+            const int lim_diag = ri + sp.diag_off;
+            int n_full = 0, n_part = 0;  // tiles of this round turned into P below
             for (int b = 0; b < ntr; ++b, ++j) {
                 if (!mbar_wait(smem_u32(&bars->s_full[x]), j & 1, p.err)) {
                     ok = false;
@@ -227,7 +235,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         sv[96 + u] = __uint_as_float(r3[u]);
                     }
                 }
-                if (b == a) {
+                const bool diag = b == sp.nfull;
+                if (diag) {
 #pragma unroll
                     for (int c = 0; c < PB; ++c)
                         if (c > lim_diag) sv[c] = -INFINITY;
@@ -290,6 +299,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&bars->p_ready[x]));
+                if (diag) ++n_part;
+                else ++n_full;
+            }
+            // the round's counters get the tiles that ran (one thread a group)
+            if (p.tile_stats && quarter == 2 && lane == 0 && (n_full | n_part)) {
+                const int rr = ring_round_of(d, e, N);
+                atomicAdd((unsigned long long *)&p.tile_stats[rr * N + d], (unsigned long long)n_full);
+                atomicAdd((unsigned long long *)&p.tile_stats[N * N + rr * N + d], (unsigned long long)n_part);
             }
         }
         // ---------------- epilogue
@@ -353,10 +370,11 @@ bool fwd_pair_eligible(const AttnGeom &g, int num_sms) {
 int launch_tc_fwd_pair(const void *q, const void *k, const void *v, void *o, float *lse, const AttnGeom &g,
                        int64_t *tile_stats, cudaStream_t stream) {
     if (!fwd_pair_eligible(g, device_sm_count())) return STRIPED_ERR_UNSUPPORTED;
-    static int attr = 1;
-    if (attr == 1)
-        attr = cuda_status(cudaFuncSetAttribute(tc_fwd_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                (int)kPSmemBytes));
+    static PerDeviceOnce attr_once;
+    const int attr = attr_once.get([] {
+        return cuda_status(
+            cudaFuncSetAttribute(tc_fwd_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmemBytes));
+    });
     if (attr != STRIPED_OK) return attr;
     CUtensorMap mq, mk, mv;
     const int64_t bh_kv = g.BH / g.G;
@@ -370,7 +388,7 @@ int launch_tc_fwd_pair(const void *q, const void *k, const void *v, void *o, flo
     p.o = reinterpret_cast<__nv_bfloat16 *>(o);
     p.lse = lse;
     p.tile_stats = tile_stats;
-    p.err = device_error_word();
+    p.err = device_status();
     const int64_t nblocks = (g.L / PB) * (g.N / 2) * g.BH;
     if (nblocks > 0x7fffffffll) return STRIPED_ERR_UNSUPPORTED;
     tc_fwd_pair_kernel<<<(unsigned)nblocks, kPThreads, kPSmemBytes, stream>>>(mq, mk, mv, p);

@@ -62,7 +62,7 @@ struct FwdParams {
     float *o_acc, *lse_acc;       // round mode: accumulator
     __nv_bfloat16 *o_out;         // round mode: optional copy
     int64_t *tile_stats;
-    int *err;                     // device error word
+    DeviceStatus *err;                     // device error word
 };
 
 template <int NS>
@@ -73,6 +73,7 @@ struct Bars {
     uint64_t s_full[2];
     uint64_t p_ready;
     uint64_t o_done;
+    uint64_t drain;  // every MMA of the issuer has completed (before TMEM is freed)
     uint32_t tmem_slot;
 };
 
@@ -148,18 +149,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&bars->s_full[1]), 1);
         mbar_init(smem_u32(&bars->p_ready), 4);
         mbar_init(smem_u32(&bars->o_done), 1);
+        mbar_init(smem_u32(&bars->drain), 1);
         fence_barrier_init();
-        if (p.tile_stats) {
-            for (int r = 0; r < nrounds; ++r) {
-                const int e = stripe_of(r);
-                const RoundSpan sp = round_span(g.layout, d, e, a, nqs, rows_a);
-                if (sp.nfull + sp.has_diag == 0) continue;
-                const int rr = ring_round_of(d, e, g.N);
-                atomicAdd((unsigned long long *)&p.tile_stats[rr * g.N + d], (unsigned long long)sp.nfull);
-                atomicAdd((unsigned long long *)&p.tile_stats[g.N * g.N + rr * g.N + d],
-                          (unsigned long long)sp.has_diag);
-            }
-        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&bars->tmem_slot), 512);
@@ -177,6 +168,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- TMA producer
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        // test hook: the first K/V tile is never loaded, so every wait on it
+        // runs out (the kernel must then record the timeout and return)
+        const bool skip_first = injected_fault(p.err) == kInjectFwdSkipKV;
         int j = 0;
         bool ok = true;
         for (int r = 0; r < nrounds && ok; ++r) {
@@ -191,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
+                if (skip_first && j == 0) continue;
                 const uint32_t fb = smem_u32(&bars->kv_full[s]);
                 const uint32_t kdst = sbase + kKVOff + s * kStageBytes;
                 const uint32_t vdst = kdst + kTileBytes;
@@ -202,6 +197,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        // loads [0, j) were issued: wait (bounded) for the last of each stage,
+        // so that on an error path none lands after the CTA has exited
+        for (int t = j > NS ? j - NS : 0; t < j; ++t)
+            if (!(skip_first && t == 0)) mbar_wait(smem_u32(&bars->kv_full[t % NS]), (t / NS) & 1, p.err);
     } else if (warp == 1 && lane == 0 && nt > 0) {
         // ---------------- MMA issuer
         constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
@@ -240,6 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(smem_u32(&bars->o_done));
             if (j + 2 < nt) ok = issue_s(j + 2);
         }
+        // every MMA issued above completes before TMEM is freed (error paths)
+        mma_commit(smem_u32(&bars->drain));
+        mbar_wait(smem_u32(&bars->drain), 0, p.err);
     } else if (warp >= 2) {
         // ---------------- softmax + epilogue
         const int quarter = warp & 3;
@@ -275,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int e = stripe_of(r);
             const RoundSpan sp = round_span(g.layout, d, e, a, nqs, rows_a);
             const int ntr = sp.nfull + sp.has_diag;
+            int n_full = 0, n_part = 0;  // tiles of this round turned into P below
             for (int b = 0; b < ntr; ++b, ++j) {
                 const uint32_t tS = ((j & 1) ? tS1 : tS0) + lane_off;
                 if (!mbar_wait(smem_u32(&bars->s_full[j & 1]), (j >> 1) & 1, p.err)) {
@@ -369,6 +372,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&bars->p_ready));
+                if (diag) ++n_part;
+                else ++n_full;
+            }
+            // the round's counters get the tiles that ran (one thread)
+            if (p.tile_stats && warp == 2 && lane == 0 && (n_full | n_part)) {
+                const int rr = ring_round_of(d, e, g.N);
+                atomicAdd((unsigned long long *)&p.tile_stats[rr * g.N + d], (unsigned long long)n_full);
+                atomicAdd((unsigned long long *)&p.tile_stats[g.N * g.N + rr * g.N + d], (unsigned long long)n_part);
             }
         }
         // ---------------- epilogue
@@ -467,18 +478,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int HD>
 static int set_smem_once() {
-    static int status = 1;
-    if (status == 1) {
+    static PerDeviceOnce once;
+    return once.get([] {
         const int bytes = (int)FwdCfg<HD>::kSmemBytes;
         const cudaError_t e[3] = {
             cudaFuncSetAttribute(tc_fwd_kernel<HD, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes),
             cudaFuncSetAttribute(tc_fwd_kernel<HD, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes),
             cudaFuncSetAttribute(tc_fwd_kernel<HD, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)};
-        status = STRIPED_OK;
+        int status = STRIPED_OK;
         for (cudaError_t x : e)
             if (x != cudaSuccess) status = cuda_status(x);
-    }
-    return status;
+        return status;
+    });
 }
 
 template <int HD>
@@ -518,7 +529,7 @@ int launch_tc_fwd(const void *q, const void *k, const void *v, void *o, float *l
     p.o = reinterpret_cast<__nv_bfloat16 *>(o);
     p.lse = lse;
     p.tile_stats = tile_stats;
-    p.err = device_error_word();
+    p.err = device_status();
     const int64_t nq = (g.L + BM - 1) / BM;
     const int64_t nblocks = nq * g.N * g.BH;
     if (nblocks > 0x7fffffffll) return STRIPED_ERR_UNSUPPORTED;
@@ -547,7 +558,7 @@ int launch_tc_round(const void *q_d, const void *k_e, const void *v_e, float *o_
     p.lse_acc = lse_acc;
     p.o_out = reinterpret_cast<__nv_bfloat16 *>(o_out);
     p.tile_stats = tile_stats;
-    p.err = device_error_word();
+    p.err = device_status();
     const int64_t nq = (g.L + BM - 1) / BM;
     if (g.BH > 65535) return STRIPED_ERR_UNSUPPORTED;
     dim3 grid((unsigned)nq, (unsigned)g.BH);

@@ -81,12 +81,9 @@ __device__ void fwd_tile(const float *__restrict__ q_stripe, const float *__rest
         const int e = e_fixed >= 0 ? e_fixed : (d - r + g.N) % g.N;
         const RoundSpan sp = round_span(g.layout, d, e, a, nqs, rows_a);
         const int ntiles = sp.nfull + sp.has_diag;
-        if (tile_stats && threadIdx.x == 0 && ntiles > 0) {
-            const int rr = ring_round_of(d, e, g.N);
-            atomicAdd((unsigned long long *)&tile_stats[rr * g.N + d], (unsigned long long)sp.nfull);
-            atomicAdd((unsigned long long *)&tile_stats[g.N * g.N + rr * g.N + d],
-                      (unsigned long long)sp.has_diag);
-        }
+        // tiles of this round processed below (full / partial), counted as
+        // they run and added to the round's counters once
+        int n_full = 0, n_part = 0;
         const float *k_stripe = k_head + (int64_t)e * g.stripe_stride;
         const float *v_stripe = v_head + (int64_t)e * g.stripe_stride;
         for (int b = 0; b < ntiles; ++b) {
@@ -113,6 +110,13 @@ __device__ void fwd_tile(const float *__restrict__ q_stripe, const float *__rest
                     if (u < dpt) st.acc[u] = st.acc[u] * alpha + p * sV[c * D + sub * dpt + u];
                 st.m = m_new;
             }
+            if (diag) ++n_part;
+            else ++n_full;
+        }
+        if (tile_stats && threadIdx.x == 0 && (n_full | n_part)) {
+            const int rr = ring_round_of(d, e, g.N);
+            atomicAdd((unsigned long long *)&tile_stats[rr * g.N + d], (unsigned long long)n_full);
+            atomicAdd((unsigned long long *)&tile_stats[g.N * g.N + rr * g.N + d], (unsigned long long)n_part);
         }
     }
 }
@@ -237,11 +241,7 @@ __global__ void __launch_bounds__(kThreads) simt_dq_kernel(
         const int e = (d - r + g.N) % g.N;
         const RoundSpan sp = round_span(g.layout, d, e, a, nqs, rows_a);
         const int ntiles = sp.nfull + sp.has_diag;
-        if (tile_stats && threadIdx.x == 0 && ntiles > 0) {
-            atomicAdd((unsigned long long *)&tile_stats[r * g.N + d], (unsigned long long)sp.nfull);
-            atomicAdd((unsigned long long *)&tile_stats[g.N * g.N + r * g.N + d],
-                      (unsigned long long)sp.has_diag);
-        }
+        int n_full = 0, n_part = 0;  // tiles processed below, counted as they run
         const float *k_stripe = k + (bh / g.G) * g.stride_bh + (int64_t)e * g.stripe_stride;
         const float *v_stripe = v + (bh / g.G) * g.stride_bh + (int64_t)e * g.stripe_stride;
         for (int b = 0; b < ntiles; ++b) {
@@ -269,6 +269,12 @@ __global__ void __launch_bounds__(kThreads) simt_dq_kernel(
                 for (int u = 0; u < kMaxDPT; ++u)
                     if (u < dpt) acc[u] += dS * sK[c * D + sub * dpt + u];
             }
+            if (diag) ++n_part;
+            else ++n_full;
+        }
+        if (tile_stats && threadIdx.x == 0 && (n_full | n_part)) {
+            atomicAdd((unsigned long long *)&tile_stats[r * g.N + d], (unsigned long long)n_full);
+            atomicAdd((unsigned long long *)&tile_stats[g.N * g.N + r * g.N + d], (unsigned long long)n_part);
         }
     }
     if (!valid) return;

@@ -2,8 +2,8 @@
 //
 //  * the per-round tile schedule of the ring (which key tiles a query tile
 //    visits in round r, and which of them need a mask);
-//  * bounded waits that record a timeout in the device error word instead of
-//    hanging;
+//  * bounded waits that record a timeout in the device status block instead
+//    of hanging;
 //  * thin inline-PTX wrappers for mbarrier, TMA (cp.async.bulk.tensor) and the
 //    5th-generation tensor core (tcgen05: TMEM alloc, mma, commit, ld, st).
 #pragma once
@@ -18,12 +18,25 @@
 namespace striped {
 
 // --------------------------------------------------------------------------
-// bounded waits; a timeout is recorded in the library's device error word
+// bounded waits; a timeout is recorded in the library's device status block
 // (owned by api.cu, passed to every kernel as a pointer)
 // --------------------------------------------------------------------------
-// A wait gives up after this many nanoseconds of wall-clock time (read from
-// %globaltimer).  Every legitimate wait in these kernels is microseconds.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// Per-device control block of the library.  `error` is the status the next
+// striped_check_error() returns (one word per device, shared by every stream
+// and caller on it).  `wait_limit_ns` bounds every mbarrier wait of the
+// kernels (wall-clock time read from %globaltimer; every legitimate wait is
+// microseconds).  `inject` is a test hook that makes one kind of kernel skip
+// one of its own loads, so that the waits on it run out (kInject* below);
+// it is 0 outside tests.
+struct DeviceStatus {
+    int error;
+    int inject;
+    unsigned long long wait_limit_ns;
+};
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
+constexpr int kInjectNone = STRIPED_FAULT_NONE;
+constexpr int kInjectFwdSkipKV = STRIPED_FAULT_FWD_SKIP_KV;  // forward TMA producers skip their first K/V tile
+constexpr int kInjectBwdSkipQ = STRIPED_FAULT_BWD_SKIP_Q;    // backward TMA producers skip their first Q tile
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
@@ -31,8 +44,17 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
-__device__ __forceinline__ void record_timeout(int *err) {
-    if (err) atomicExch(err, STRIPED_ERR_TIMEOUT);
+__device__ __forceinline__ void record_timeout(DeviceStatus *st) {
+    if (st) atomicExch(&st->error, STRIPED_ERR_TIMEOUT);
+}
+
+__device__ __forceinline__ void record_error(DeviceStatus *st, int code) {
+    if (st) atomicExch(&st->error, code);
+}
+
+// The test hook of this launch (read once per CTA by the producers).
+__device__ __forceinline__ int injected_fault(const DeviceStatus *st) {
+    return st ? *reinterpret_cast<const volatile int *>(&st->inject) : kInjectNone;
 }
 
 // --------------------------------------------------------------------------
@@ -207,16 +229,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase of parity `parity` to complete; false (and the device
-// error word set) if the bound ran out.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *err) {
+// status set to STRIPED_ERR_TIMEOUT) if the bound runs out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, DeviceStatus *st) {
     for (int it = 0; it < 64; ++it)
         if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t limit =
+        st ? *reinterpret_cast<const volatile unsigned long long *>(&st->wait_limit_ns) : kDefaultWaitLimitNs;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 255u && global_timer_ns() - t0 > kWaitLimitNs) break;
+        if ((it & 255u) == 255u && global_timer_ns() - t0 > limit) break;
     }
-    record_timeout(err);
+    record_timeout(st);
     return false;
 }
 

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "striped.h"
 
 namespace striped {
@@ -14,9 +16,37 @@ namespace striped {
 // maps it to a status code.
 int cuda_status(cudaError_t err);
 
-// Device address of the library's error word on the current device (where
-// bounded waits record STRIPED_ERR_TIMEOUT), or nullptr on failure.
-int *device_error_word();
+// A status computed once per device, under a lock: kernel attributes (the
+// dynamic shared-memory opt-in) are per device, so a process that launches
+// on several GPUs sets them on each.
+constexpr int kMaxDevices = 256;
+class PerDeviceOnce {
+  public:
+    template <typename F>
+    int get(F &&fn) {
+        int dev = 0;
+        const cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return cuda_status(e);
+        if (dev < 0 || dev >= kMaxDevices) return STRIPED_ERR_UNSUPPORTED;
+        std::lock_guard<std::mutex> lock(mu_);
+        if (!done_[dev]) {
+            status_[dev] = fn();
+            done_[dev] = true;
+        }
+        return status_[dev];
+    }
+
+  private:
+    std::mutex mu_;
+    bool done_[kMaxDevices] = {};
+    int status_[kMaxDevices] = {};
+};
+
+// Device address of the library's status block on the current device (where
+// bounded waits record STRIPED_ERR_TIMEOUT; see DeviceStatus in common.cuh),
+// or nullptr on failure.  Looked up once per device under a lock.
+struct DeviceStatus;
+DeviceStatus *device_status();
 
 // Geometry of one attention launch.  Every tensor is addressed as
 // [BH][N stripes][L rows][D] with stripe e of head bh starting at element
@@ -71,8 +101,8 @@ int launch_tc_fwd(const void *q, const void *k, const void *v, void *o, float *l
 // d+1) per CTA; STRIPED_ERR_UNSUPPORTED unless fwd_pair_eligible(g, sms)
 // with the current device's multiprocessor count.
 bool fwd_pair_eligible(const AttnGeom &g, int num_sms);
-// Multiprocessor count of the current device (queried once; 152 if the
-// query fails).
+// Multiprocessor count of the current device (queried once per device; 152
+// if the query fails).
 int device_sm_count();
 int launch_tc_fwd_pair(const void *q, const void *k, const void *v, void *o, float *lse,
                        const AttnGeom &g, int64_t *tile_stats, cudaStream_t stream);

@@ -243,3 +243,11 @@ def test_workspace_size(lib):
 def test_status_strings(lib):
     assert sp.status_string(0) == "ok"
     assert "timed out" in sp.status_string(-5)
+
+
+def test_test_hook_rejects_unknown_faults(lib):
+    """The fault-injection test hook validates its selector before it
+    touches the device."""
+    assert lib.striped_test_inject(3, 0) == -1
+    assert lib.striped_test_inject(-1, 1000) == -1
+    assert "striped_test_inject" in _declared_functions()
