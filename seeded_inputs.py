@@ -70,6 +70,27 @@ def sample_tail_keys(n: int, S: int, window: int, seed: int = 0) -> torch.Tensor
     return torch.sort(S - w + perm).values
 
 
+def sample_keys(n: int, S: int, seed: int = 0) -> torch.Tensor:
+    """n distinct key positions drawn uniformly over [0, S) (row seed), sorted."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed + 4) * 104729 + 3)
+    m = min(n, S)
+    if S <= 4 * m:
+        pick = torch.randperm(S, generator=g)[:m]
+    else:  # rejection of repeats keeps memory O(n) for long sequences
+        seen = set()
+        out = []
+        while len(out) < m:
+            for x in torch.randint(0, S, (2 * m,), generator=g).tolist():
+                if x not in seen:
+                    seen.add(x)
+                    out.append(x)
+                    if len(out) == m:
+                        break
+        pick = torch.as_tensor(out, dtype=torch.int64)
+    return torch.sort(pick).values
+
+
 def sample_head(B: int, H: int, seed: int = 0) -> tuple[int, int]:
     """One (b, h) chosen with the row seed, for per-head key-row checks."""
     g = torch.Generator(device="cpu")

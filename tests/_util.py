@@ -52,9 +52,64 @@ def maxerr(a, b):
     return float(np.max(np.abs(a - b))) if a.size else 0.0
 
 
-def with_bf16_storage(tol, ref):
-    """Bound for a bf16-stored output in cases beyond the benchmark
-    workloads: the arithmetic bound `tol` plus the bf16 storage rounding of
-    the largest value, 2^-8 of its magnitude (half the 2^-7 relative spacing
-    of bf16 numbers).  At |ref| ~ 5 the storage alone can cost 0.016."""
-    return tol + 2.0 ** -8 * float(np.max(np.abs(ref)))
+def bf16_storage_excess(got, ref):
+    """Largest |got - ref| left after allowing each element the bf16 rounding
+    of its own stored value.  A bf16 output holds round(v) of the kernel's
+    fp32 result v, at most half a bf16 ulp of the element away from it; so
+    |got - ref| - halfulp(got) <= |v - ref|, the arithmetic error that the
+    tolerance is about.  (Comparing against round(ref) instead would count a
+    whole ulp whenever v and ref fall on opposite sides of a rounding
+    boundary, which at |x| in [4, 8) is 2^-5 = 0.031 for any tiny error.)"""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    mag = np.maximum(np.abs(got), np.abs(ref))
+    with np.errstate(divide="ignore"):
+        expo = np.floor(np.log2(np.where(mag > 0, mag, 1.0)))
+    half_ulp = np.where(mag > 0, np.exp2(expo - 8.0), 0.0)  # bf16: 8 significant bits
+    return float(np.max(np.abs(got - ref) - half_ulp)) if got.size else 0.0
+
+
+def grad_sum_errors(dv, dk, do_pos, q_pos, G: int = 1):
+    """Worst ratio (error / bound) over every (b, h, column) of the two
+    gradient invariants of causal softmax attention, on full GPU tensors:
+        sum_t dV_t = sum_p dO_p   (every row of P sums to 1)
+        sum_t dK_t = 0            (every row of dS sums to 0).
+    dv, dk: [B, Hkv, S, D] device tensors in any row order (sums ignore it);
+    do_pos, q_pos: [B, H, S, D] inputs in POSITION order (device tensors);
+    G = H / Hkv query heads share a key/value head (their sums add up).
+    Bound per column c (fp64 sums, so the sums add no error of their own):
+      4 * 2^-9 * ( sqrt(sum_t x_tc^2) + sqrt(sum_p y_pc^2 * w_p) ) + 1e-3
+    * first term: each stored bf16 value is off by at most half an ulp
+      (<= 2^-8 relative, unbiased), so the sum of S of them has a standard
+      deviation below 2^-9 sqrt(sum x^2); 4 of those.
+    * second term: P (and dS) are rounded to bf16 as tensor-core operands,
+      so row p's weights sum to 1 only up to about 2^-9 sqrt(sum_t P_pt^2);
+      for these inputs (N(0,1) q, k at scale 1/sqrt(D): scores ~ N(0,1)) a
+      row of p+1 kept keys has sum_t P_pt^2 ~ e/(p+1) =: w_p.  The row
+      errors enter the dV sum weighted by dO_p and the dK sum by
+      scale * |dP| * q_p ~ q_p (|dP| ~ sqrt(D) for unit dO, v).
+    The bound grows like sqrt(log S), where sqrt(S) * 2^-9 * max|x| grows
+    like sqrt(S) and would accept a head with many wrong rows at S = 262,144.
+    Returns {"dv"|"dk": (max error, smallest bound, max error/bound)}."""
+    import torch
+
+    B, Hkv, S, D = dv.shape
+    pos = torch.arange(S, device=do_pos.device, dtype=torch.float64)
+    w = torch.clamp(np.e / (pos + 1.0), max=1.0).view(S, 1)
+    out = {}
+    for name, x, y, has_target in (("dv", dv, do_pos, True), ("dk", dk, q_pos, False)):
+        sx = x.double().sum(2)
+        if has_target:
+            want = y.double().sum(2).reshape(B, Hkv, G, D).sum(2)
+        else:
+            want = torch.zeros_like(sx)
+        err = (sx - want).abs()
+        x2 = torch.zeros_like(sx)
+        y2 = torch.zeros_like(sx)
+        for h in range(Hkv):  # per head keeps the fp64 temporaries small
+            x2[:, h] = x[:, h].double().square().sum(1)
+            for g in range(G):
+                y2[:, h] += (y[:, h * G + g].double().square() * w).sum(1)
+        bound = 4.0 * 2.0 ** -9 * (x2.sqrt() + y2.sqrt()) + 1e-3
+        out[name] = (float(err.max()), float(bound.min()), float((err / bound).max()))
+    return out

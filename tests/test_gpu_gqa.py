@@ -16,7 +16,7 @@ import torch
 import oracle
 import sequence_parallelism_striped_gb300 as sp
 from seeded_inputs import attention_inputs, sample_rows, sample_tail_keys
-from tests._util import TOL, maxerr, to_layout, to_positions
+from tests._util import TOL, grad_sum_errors, maxerr, to_layout, to_positions
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda")
@@ -139,6 +139,6 @@ def test_gqa_mid_size_sampled():
     ev = float(np.abs(dv[0, kvh, kidx].double().cpu().numpy() - dv_r).max())
     print("gqa mid tail-key max errors dk dv", ek, ev)
     assert ek <= 2e-2 * np.sqrt(G) and ev <= 2e-2 * np.sqrt(G)
-    sdv = dv.double().sum(2)
-    sdo = x["do"].to(DEV).double().sum(2).reshape(B, Hkv, G, D).sum(2)
-    assert float((sdv - sdo).abs().max()) <= np.sqrt(G * S) * 2.0 ** -9 * float(dv.abs().max()) + 2e-2
+    inv = grad_sum_errors(dv, dk, x["do"].to(DEV), x["q"].to(DEV), G=G)
+    print("gqa mid gradient invariants", inv)
+    assert inv["dv"][2] <= 1.0 and inv["dk"][2] <= 1.0, inv

@@ -1,10 +1,15 @@
 """Full-size parity on the benchmark workloads (the launch configuration the
 bench times): 4096 seed-sampled (b, h, position) query rows for O, LSE and
-dQ against the fp64 oracle; dK and dV for key positions sampled from the
-tail of one seed-chosen head (the oracle needs LSE and the Jacobian sums of
-every query at or after a key, which is cheap only near the end); the
-per-round tile counters against the oracle's closed forms; and the gradient
-invariants sum_t dV_t = sum_p dO_p and sum_t dK_t = 0 on every head."""
+dQ against the fp64 oracle; dK and dV for 4096 key positions drawn
+uniformly over the whole sequence of one seed-chosen head (the oracle first
+runs a full-head fp64 pass for the LSE and Jacobian sum of every query,
+about 2 D S^2 flops: seconds at S = 65,536, minutes at 262,144), so the
+early key tiles, which accumulate dK/dV over every later query tile of all
+N stripes, are compared element by element; at S = 786,432 that pass would
+take about an hour, so there the keys come from the last 1,024 positions;
+the per-round tile counters against the oracle's closed forms; and the
+gradient invariants sum_t dV_t = sum_p dO_p and sum_t dK_t = 0 on every
+head and column, under an error bound that grows like sqrt(log S)."""
 import time
 
 import numpy as np
@@ -13,7 +18,8 @@ import torch
 
 import oracle
 import sequence_parallelism_striped_gb300 as sp
-from seeded_inputs import attention_inputs, sample_head, sample_rows, sample_tail_keys
+from seeded_inputs import attention_inputs, sample_head, sample_keys, sample_rows, sample_tail_keys
+from tests._util import grad_sum_errors
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 DEV = torch.device("cuda")
@@ -49,13 +55,10 @@ def test_full_size_sampled_parity(name):
     st = stats.cpu().numpy()
     assert np.array_equal(st[0], B * H * full) and np.array_equal(st[1], B * H * part)
 
-    # invariants on every head (fp64 sums of the GPU tensors)
-    sdv = dv.double().sum(2)
-    sdo = x["do"].to(DEV).double().sum(2)
-    bound_v = np.sqrt(S) * 2.0 ** -9 * float(dv.abs().max()) + 2e-2
-    assert float((sdv - sdo).abs().max()) <= bound_v
-    bound_k = np.sqrt(S) * 2.0 ** -9 * float(dk.abs().max()) + 2e-2
-    assert float(dk.double().sum(2).abs().max()) <= bound_k
+    # invariants on every head and column (fp64 sums of the GPU tensors)
+    inv = grad_sum_errors(dv, dk, x["do"].to(DEV), x["q"].to(DEV))
+    print(name, "gradient invariants (max error, smallest bound, max error/bound):", inv)
+    assert inv["dv"][2] <= 1.0 and inv["dk"][2] <= 1.0, inv
 
     # 4096 sampled query rows: O, LSE, dQ
     rows = sample_rows(4096, B, H, S, seed=0).numpy()
@@ -82,9 +85,16 @@ def test_full_size_sampled_parity(name):
           f"{oracle.default_threads()} threads)")
     assert worst["o"] <= 2e-2 and worst["dq"] <= 2e-2 and worst["lse"] <= 1e-3, worst
 
-    # dK, dV for 256 key positions from the last 1024 positions of one head
+    # dK, dV of one seed-chosen head: 4096 keys uniform over [0, S) (the
+    # oracle's full-head pass), or 256 of the last 1024 at the largest size
     b, h = sample_head(B, H, seed=0)
-    keys = sample_tail_keys(256, S, 1024, seed=0).numpy()
+    if name == "vlong":
+        keys = sample_tail_keys(256, S, 1024, seed=0).numpy()
+        what = "256 tail keys"
+    else:
+        keys = sample_keys(4096, S, seed=0).numpy()
+        assert keys.min() < S // 64 and keys.max() > S - S // 64
+        what = "4096 uniform keys (full-head pass)"
     kidx = torch.as_tensor(_row_of_position(keys, S, N), device=DEV)
     dk_s = dk[b, h, kidx].double().cpu().numpy()
     dv_s = dv[b, h, kidx].double().cpu().numpy()
@@ -93,7 +103,12 @@ def test_full_size_sampled_parity(name):
     dk_ref, dv_ref = oracle.bwd_keys(*args, scale, keys)
     t_keys = time.perf_counter() - t_keys
     ek, ev = float(np.abs(dk_s - dk_ref).max()), float(np.abs(dv_s - dv_ref).max())
-    print(name, "tail-key max errors dk dv", ek, ev, f"(oracle: 256 key rows in {t_keys:.1f} s)")
+    early = keys < S // 8  # keys whose tiles see (almost) every query tile
+    ek0 = float(np.abs(dk_s[early] - dk_ref[early]).max()) if early.any() else 0.0
+    ev0 = float(np.abs(dv_s[early] - dv_ref[early]).max()) if early.any() else 0.0
+    print(name, what, "max errors dk dv", ek, ev, "(first eighth:", ek0, ev0, ")",
+          f"max |dk| {np.abs(dk_ref).max():.3f} |dv| {np.abs(dv_ref).max():.3f}",
+          f"(oracle: {t_keys:.1f} s on {oracle.default_threads()} threads)")
     assert ek <= 2e-2 and ev <= 2e-2
 
 
@@ -148,9 +163,9 @@ def test_mid_contiguous_and_per_round_sampled():
     assert worst["o"] <= 2e-2 and worst["dq"] <= 2e-2 and worst["o_round"] <= 2e-2
     assert worst["lse"] <= 1e-3 and worst["lse_round"] <= 1e-3
     # gradient invariants of the contiguous backward on every head
-    assert float((dv.double().sum(2) - do.double().sum(2)).abs().max()) <= \
-        np.sqrt(S) * 2.0 ** -9 * float(dv.abs().max()) + 2e-2
-    assert float(dk.double().sum(2).abs().max()) <= np.sqrt(S) * 2.0 ** -9 * float(dk.abs().max()) + 2e-2
+    inv = grad_sum_errors(dv, dk, do, q)
+    print("mid contiguous gradient invariants", inv)
+    assert inv["dv"][2] <= 1.0 and inv["dk"][2] <= 1.0, inv
 
 
 def test_mid_zigzag_sampled():
@@ -188,6 +203,6 @@ def test_mid_zigzag_sampled():
             worst[key] = max(worst[key], float(np.abs(got[key][sel] - ref).max()))
     print("mid zig-zag max errors", worst)
     assert worst["o"] <= 2e-2 and worst["dq"] <= 2e-2 and worst["lse"] <= 1e-3
-    assert float((dv.double().sum(2) - do.double().sum(2)).abs().max()) <= \
-        np.sqrt(S) * 2.0 ** -9 * float(dv.abs().max()) + 2e-2
-    assert float(dk.double().sum(2).abs().max()) <= np.sqrt(S) * 2.0 ** -9 * float(dk.abs().max()) + 2e-2
+    inv = grad_sum_errors(dv, dk, x["do"].to(DEV), x["q"].to(DEV))
+    print("mid zig-zag gradient invariants", inv)
+    assert inv["dv"][2] <= 1.0 and inv["dk"][2] <= 1.0, inv

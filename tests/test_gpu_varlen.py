@@ -2,9 +2,11 @@
 bit-exact against the oracle's per-sequence placement, and the forward and
 backward (with and without grouped K/V heads) against the oracle's
 per-sequence attention, all three placements, fp32 and bf16, with the tile
-counters equal to the sum of the sequences' own tables.  The bf16 dK and dV
-bounds add the bf16 storage rounding of the largest value (these shapes lie
-beyond the benchmark workloads the fixed 2e-2 bound was stated for)."""
+counters equal to the sum of the sequences' own tables.  bf16 dK and dV are
+compared after allowing each element the rounding of its own stored bf16
+value (half an ulp at that element), so the 2e-2 bound applies to the
+arithmetic before storage (dK/dV of a packed D = 64 head reach |dV| ~ 4.8,
+where stored bf16 values lie 2^-5 apart)."""
 import numpy as np
 import pytest
 import torch
@@ -12,7 +14,7 @@ import torch
 import oracle
 import sequence_parallelism_striped_gb300 as sp
 from seeded_inputs import attention_inputs
-from tests._util import TOL, maxerr, with_bf16_storage
+from tests._util import TOL, bf16_storage_excess, maxerr
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda")
@@ -93,10 +95,9 @@ def test_varlen_fwd_bwd_match_oracle(dtype, H, Hkv, D, N, cu, layouts):
             assert maxerr(o_p[h], ref_o[h]) <= tol["o"], (layout, h)
             assert maxerr(l_p[h], ref_l[h]) <= tol["lse"], (layout, h)
             assert maxerr(dq_p[h], ref_dq[h]) <= tol["grad"], (layout, h)
-        dk_tol = with_bf16_storage(kv_tol, ref_dk) if bf else kv_tol
-        dv_tol = with_bf16_storage(kv_tol, ref_dv) if bf else kv_tol
-        assert maxerr(dk_p, ref_dk) <= dk_tol, (layout, maxerr(dk_p, ref_dk))
-        assert maxerr(dv_p, ref_dv) <= dv_tol, (layout, maxerr(dv_p, ref_dv))
+        err = bf16_storage_excess if bf else maxerr
+        assert err(dk_p, ref_dk) <= kv_tol, (layout, err(dk_p, ref_dk), maxerr(dk_p, ref_dk))
+        assert err(dv_p, ref_dv) <= kv_tol, (layout, err(dv_p, ref_dv), maxerr(dv_p, ref_dv))
         full = sum(oracle.tile_counts_bruteforce(b - a, N, T, T, layout)[0] for a, b in zip(cu, cu[1:]))
         part = sum(oracle.tile_counts_bruteforce(b - a, N, T, T, layout)[1] for a, b in zip(cu, cu[1:]))
         for st in (fst, bst):
