@@ -433,3 +433,41 @@ def test_varlen_positions_place_each_sequence_on_its_own(oracle_lib, layout):
             assert np.array_equal(rows[off:off + Li], cu[i] + own)
             off += Li
     assert np.array_equal(oracle.varlen_positions([0, 64], N, layout), oracle.layout_positions(64, N, layout))
+
+
+@pytest.mark.parametrize("layout", [STRIPED, CONTIGUOUS, ZIGZAG])
+@pytest.mark.parametrize("N,cu", [(4, [0, 16, 24, 56, 64]), (2, [0, 4, 12, 20]), (8, [0, 16, 48, 64]),
+                                  (1, [0, 3, 10])])
+def test_varlen_positions_independent_enumeration(oracle_lib, N, cu, layout):
+    """An enumeration written from the placement rules alone, position by
+    position (no call into the oracle's placements): position p of sequence
+    i (offset t = p - cu[i], length S_i, L_i = S_i / N rows per device) sits
+    on device d at local row j of that sequence's block, which starts at row
+    d*L + cu[i]/N of the packed head --
+      striped:    every N-th token, d = t mod N, j = t div N
+      contiguous: d = t div L_i, j = t mod L_i
+      zig-zag:    chunk c = t div C_i (C_i = S_i / 2N); c < N: d = c, j = t mod C_i;
+                  else d = 2N-1-c, j = C_i + t mod C_i.
+    The oracle's pos[row] must invert it."""
+    if layout == ZIGZAG and any((b - a) % (2 * N) for a, b in zip(cu, cu[1:])):
+        pytest.skip("zig-zag needs every length a multiple of 2N")
+    S = cu[-1]
+    L = S // N
+    row_of = {}
+    for i in range(len(cu) - 1):
+        Si = cu[i + 1] - cu[i]
+        Li = Si // N
+        for t in range(Si):
+            if layout == STRIPED:
+                d, j = t % N, t // N
+            elif layout == CONTIGUOUS:
+                d, j = t // Li, t % Li
+            else:
+                Ci = Si // (2 * N)
+                c = t // Ci
+                d, j = (c, t % Ci) if c < N else (2 * N - 1 - c, Ci + t % Ci)
+            row_of[cu[i] + t] = d * L + cu[i] // N + j
+    assert sorted(row_of.values()) == list(range(S))
+    pos = oracle.varlen_positions(cu, N, layout)
+    for p, row in row_of.items():
+        assert pos[row] == p, (p, row)

@@ -4,7 +4,9 @@ extend, or they keep cudaMalloc off the hot path).  Its scratch is a fixed
 array inside the library, so this test calls it through the C ABI and
 checks it against striped_attn_bwd with a caller-owned workspace, twice in
 a row (the second call must not depend on what the first left in the
-shared array).  Collected last on purpose."""
+shared array).  Both run the same kernels: dK and dV are accumulated in a
+fixed order and must be equal bit for bit; dQ is summed with fp32 atomics,
+so only its summation order may differ.  Collected last on purpose."""
 import ctypes
 
 import pytest
@@ -53,8 +55,8 @@ def test_noalloc_matches_workspace_entry_point(dtype, B, H, S, D, N, layout):
         assert st == 0, sp.status_string(st)
         torch.cuda.synchronize()
         assert sp.check_error() == 0
-        for got, want in zip((dq, dk, dv), ref):
-            assert maxerr(got.float().cpu(), want.float().cpu()) <= tol
+        assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2])
+        assert maxerr(dq.float().cpu(), ref[0].float().cpu()) <= tol
 
 
 def test_noalloc_rejects_problems_beyond_the_array():
