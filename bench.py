@@ -254,6 +254,79 @@ def short_sequence_report(sp, torch, dev):
     return out
 
 
+def configs_report(sp, torch, dev, peaks):
+    """The other synthetic workloads on one GPU, each step the same pass as
+    the headline (permute Q, K, V, dO -> forward over all rounds -> backward
+    -> unpermute O, dQ, dK, dV; the contiguous placement needs no permute):
+    mid (B=1, H=24, S=65,536, N=8) and very long (B=1, H=16, S=786,432,
+    N=16) for the striped and contiguous placements, with the modelled ring
+    critical path of each; tiny (fp32, S=256, N=4, D=64) forward and
+    forward+backward times.  Inputs larger than L2 except tiny (256 KB)."""
+    from seeded_inputs import device_inputs
+
+    out = {}
+
+    def timed(fn, steps, warm):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    for name, (B, H, S, D, N, steps, warm) in (("mid", (1, 24, 65536, 128, 8, 5, 2)),
+                                               ("vlong", (1, 16, 786432, 128, 16, 2, 1))):
+        x = device_inputs(B, H, S, D, torch.bfloat16, seed=5, device=dev)
+        bufs = {k_: torch.empty_like(x["q"]) for k_ in ("q", "k", "v", "do", "o", "dq", "dk", "dv", "u")}
+        lse = torch.empty(B, H, S, dtype=torch.float32, device=dev)
+        ws = sp.new_workspace(B, H, S, D, N, torch.bfloat16, dev)
+        fl = _flops(B, H, S, D, 14)
+        res = {"workload": {"B": B, "H": H, "S": S, "D": D, "N": N, "dtype": "bf16"},
+               "steps": steps, "warmup": warm, "T": 128}
+        for lname, layout in (("striped", sp.STRIPED), ("contiguous", sp.CONTIGUOUS)):
+            def step():
+                if layout == sp.STRIPED:
+                    q_, k_, v_, do_ = (sp.striped_permute(x[n_], N, out=bufs[n_]) for n_ in ("q", "k", "v", "do"))
+                else:
+                    q_, k_, v_, do_ = x["q"], x["k"], x["v"], x["do"]
+                sp.striped_attn_fwd(q_, k_, v_, N, layout, out=bufs["o"], lse_out=lse)
+                sp.striped_attn_bwd(q_, k_, v_, bufs["o"], lse, do_, N, layout, workspace=ws, dq=bufs["dq"],
+                                    dk=bufs["dk"], dv=bufs["dv"])
+                if layout == sp.STRIPED:
+                    for n_ in ("o", "dq", "dk", "dv"):
+                        sp.striped_unpermute(bufs[n_], N, out=bufs["u"])
+
+            ms = timed(step, steps, warm)
+            res[lname] = {"ms_per_step": ms, "tflops": fl / (ms / 1e3) / 1e12,
+                          "pct_of_burst": fl / (ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+                          "critical_path_tiles": sp.critical_path(S, N, 128, 128, layout)}
+        out[name] = res
+        del x, bufs, lse, ws
+        torch.cuda.empty_cache()
+
+    # tiny fp32 workload (CUDA cores, tile 16): latency of one launch chain
+    B, H, S, D, N = 1, 1, 256, 64, 4
+    x = device_inputs(B, H, S, D, torch.float32, seed=6, device=dev)
+    tiny = {"workload": {"B": B, "H": H, "S": S, "D": D, "N": N, "dtype": "fp32"}, "T": 16,
+            "timing": "mean of 50 after 5 warm-up (fits in L2)"}
+    for lname, layout in (("striped", sp.STRIPED), ("contiguous", sp.CONTIGUOUS)):
+        q_, k_, v_, do_ = (sp.layout_permute(x[n_], N, layout) for n_ in ("q", "k", "v", "do"))
+        o, lse = sp.striped_attn_fwd(q_, k_, v_, N, layout)
+        ws = sp.new_workspace(B, H, S, D, N, torch.float32, dev)
+        t_f = timed(lambda: sp.striped_attn_fwd(q_, k_, v_, N, layout, out=o, lse_out=lse), 50, 5)
+        t_fb = timed(lambda: (sp.striped_attn_fwd(q_, k_, v_, N, layout, out=o, lse_out=lse),
+                              sp.striped_attn_bwd(q_, k_, v_, o, lse, do_, N, layout, workspace=ws)), 50, 5)
+        tiny[lname] = {"fwd_us": 1e3 * t_f, "fwd_bwd_us": 1e3 * t_fb,
+                       "critical_path_tiles": sp.critical_path(S, N, 16, 16, layout)}
+    out["tiny"] = tiny
+    return out
+
+
 def variants_report(sp, torch, dev, x, B, H, S, D, N):
     """Grouped-query attention (Hkv = H/4) and a packed batch (8 sequences
     of S/8 tokens in one head dimension) at the benchmark size, striped:
@@ -579,6 +652,8 @@ def run_gpu(args, rank, world, local_rank):
         line["short_sequence"] = short_sequence_report(sp, torch, dev)
     if args.compare and B == 1:
         line["variants"] = variants_report(sp, torch, dev, x, B, H, S, D, N)
+    if args.compare and args.configs:
+        line["configs"] = configs_report(sp, torch, dev, peaks)
     if e2e is not None:
         line["e2e"] = e2e
     line["clocks"] = clk.summary()
@@ -602,6 +677,8 @@ def main():
     ap.add_argument("--no-compare", dest="compare", action="store_false")
     ap.add_argument("--no-short", dest="short", action="store_false",
                     help="skip the short-sequence (S=8192) comparison")
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="skip the mid / very-long / tiny workloads")
     for key in ("B", "H", "S", "N"):
         ap.add_argument(f"--{key}", type=int, default=None, help="override the workload (profiling cases)")
     args = ap.parse_args()
