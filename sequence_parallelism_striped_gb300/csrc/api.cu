@@ -1,6 +1,6 @@
 // api.cu -- the C entry points of libstriped (declared in include/striped.h):
 // argument validation, status codes, tensor-map construction, the host-side
-// tile/critical-path model and the device status block.
+// tile/critical-path model, the device status word and the wait control.
 #include <stddef.h>
 #include <stdio.h>
 #include <string.h>
@@ -12,24 +12,41 @@
 
 namespace striped {
 
-// The library's status block on every device that loads it (see
-// DeviceStatus): the error word striped_check_error() reads, the bound of
-// every device-side wait, and the test hook.  One block per device, shared
-// by every stream and caller on that device.
-__device__ DeviceStatus g_status = {0, kInjectNone, kDefaultWaitLimitNs};
+// The library's status word on every device that loads it (one per device,
+// shared by every stream and caller on that device).
+__device__ DeviceStatus g_status = {0};
+
+// Per-device host state: the status word's address (looked up once) and the
+// wait bound and test hook that striped_test_inject sets.
+struct HostDeviceState {
+    DeviceStatus *st = nullptr;
+    unsigned long long limit_ns = kDefaultWaitLimitNs;
+    int inject = kInjectNone;
+};
+static std::mutex g_state_mu;
+static HostDeviceState g_state[kMaxDevices];
 
 DeviceStatus *device_status() {
-    static std::mutex mu;
-    static DeviceStatus *cache[256] = {nullptr};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!cache[dev]) {
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_state_mu);
+    if (!g_state[dev].st) {
         void *ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_status) != cudaSuccess) return nullptr;
-        cache[dev] = static_cast<DeviceStatus *>(ptr);
+        g_state[dev].st = static_cast<DeviceStatus *>(ptr);
     }
-    return cache[dev];
+    return g_state[dev].st;
+}
+
+WaitCtl device_wait_ctl() {
+    WaitCtl w{device_status(), kDefaultWaitLimitNs, kInjectNone};
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
+        std::lock_guard<std::mutex> lock(g_state_mu);
+        w.limit_ns = g_state[dev].limit_ns;
+        w.inject = g_state[dev].inject;
+    }
+    return w;
 }
 
 static thread_local int t_last_cuda_error = 0;
@@ -185,10 +202,10 @@ int striped_check_error(void *stream) {
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_status(e);
     int word = 0, zero = 0;
-    e = cudaMemcpyFromSymbol(&word, g_status, sizeof(int), offsetof(DeviceStatus, error));
+    e = cudaMemcpyFromSymbol(&word, g_status, sizeof(int));
     if (e != cudaSuccess) return cuda_status(e);
     if (word != 0) {
-        e = cudaMemcpyToSymbol(g_status, &zero, sizeof(int), offsetof(DeviceStatus, error));
+        e = cudaMemcpyToSymbol(g_status, &zero, sizeof(int));
         if (e != cudaSuccess) return cuda_status(e);
         return word;
     }
@@ -197,12 +214,15 @@ int striped_check_error(void *stream) {
 
 int striped_test_inject(int fault, int64_t wait_limit_ns) {
     if (fault < kInjectNone || fault > kInjectBwdSkipQ) return STRIPED_ERR_INVALID_ARG;
-    const unsigned long long limit = wait_limit_ns > 0 ? (unsigned long long)wait_limit_ns : kDefaultWaitLimitNs;
-    cudaError_t e = cudaDeviceSynchronize();
-    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_status, &fault, sizeof(int), offsetof(DeviceStatus, inject));
-    if (e == cudaSuccess)
-        e = cudaMemcpyToSymbol(g_status, &limit, sizeof(limit), offsetof(DeviceStatus, wait_limit_ns));
-    return cuda_status(e);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();  // launches already queued keep their settings
+    if (e != cudaSuccess) return cuda_status(e);
+    if (dev < 0 || dev >= kMaxDevices) return STRIPED_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_state_mu);
+    g_state[dev].limit_ns = wait_limit_ns > 0 ? (unsigned long long)wait_limit_ns : kDefaultWaitLimitNs;
+    g_state[dev].inject = fault;
+    return STRIPED_OK;
 }
 
 int striped_selftest_timeout(int64_t spins, void *stream) {

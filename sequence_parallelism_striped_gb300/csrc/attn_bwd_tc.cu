@@ -77,7 +77,7 @@ struct BwdParams {
     float *dq_acc;       // [BH][S][D] fp32
     __nv_bfloat16 *dk, *dv;
     int64_t *tile_stats;
-    DeviceStatus *err;
+    WaitCtl wc;  // status word, wait bound, test hook
 };
 
 struct Bars {
@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw;
     if ((smem_u32(smem) & 1023u) != 0) {  // operand tiles need 1024-byte alignment
-        if (threadIdx.x == 0) record_error(p.err, STRIPED_ERR_ALIGN);
+        if (threadIdx.x == 0) record_error(p.wc.st, STRIPED_ERR_ALIGN);
         return;
     }
     Bars *bars = reinterpret_cast<Bars *>(smem + Cfg::kBarOff);
@@ -233,12 +233,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int x = 0; x < kBoxes; ++x) tma_load_4d(sbase + kVOff + x * kBox, &tmV, kb, 64 * x, bg * BT, e, (int)bh);
         // test hook: the first Q tile is never loaded, so every wait on it
         // runs out (the kernel must then record the timeout and return)
-        const bool skip_first = injected_fault(p.err) == kInjectBwdSkipQ;
+        const bool skip_first = p.wc.inject == kInjectBwdSkipQ;
         QTileIter it = qiter_begin(g.layout, N, G, e, b, nqs, rows_b);
         int i = 0;
         for (; i < nt; ++i, qiter_next(it, g.layout, N, G, e, b, nqs, rows_b)) {
             const int s = i % QS;
-            if (i >= QS && !mbar_wait(smem_u32(&bars->q_empty[s]), ((i / QS) + 1) & 1, p.err)) break;
+            if (i >= QS && !mbar_wait(smem_u32(&bars->q_empty[s]), ((i / QS) + 1) & 1, p.wc)) break;
             if (skip_first && i == 0) continue;
             const uint32_t fb = smem_u32(&bars->q_full[s]);
             const uint32_t qdst = sbase + kQOff + s * 2 * kTile;
@@ -252,9 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // K, V and loads [0, i) were issued: wait (bounded) for the last of
         // each stage, so that on an error path none lands after the CTA exits
-        mbar_wait(kb, 0, p.err);
+        mbar_wait(kb, 0, p.wc);
         for (int t = i > QS ? i - QS : 0; t < i; ++t)
-            if (!(skip_first && t == 0)) mbar_wait(smem_u32(&bars->q_full[t % QS]), (t / QS) & 1, p.err);
+            if (!(skip_first && t == 0)) mbar_wait(smem_u32(&bars->q_full[t % QS]), (t / QS) & 1, p.wc);
     } else if (warp == 2 && lane == 0 && nt > 0) {
         // ---------------- TMA producer: dO_i (its own stream: the buffer is
         // released later than Q_i's, after the dQ_i half staged in it is read)
@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int i = 0;
         for (; i < nt; ++i, qiter_next(it, g.layout, N, G, e, b, nqs, rows_b)) {
             const int s = i % QS;
-            if (i >= QS && !mbar_wait(smem_u32(&bars->do_empty[s]), ((i / QS) + 1) & 1, p.err)) break;
+            if (i >= QS && !mbar_wait(smem_u32(&bars->do_empty[s]), ((i / QS) + 1) & 1, p.wc)) break;
             const uint32_t fb = smem_u32(&bars->do_full[s]);
             const uint32_t odst = sbase + kQOff + s * 2 * kTile + kTile;
             const int bq = (int)(bh * G + it.h);
@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_4d(odst + x * kBox, &tmdO, fb, 64 * x, (qbase + it.a) * BT, it.d, bq);
         }
         for (int t = i > QS ? i - QS : 0; t < i; ++t)  // in-flight loads, as above
-            mbar_wait(smem_u32(&bars->do_full[t % QS]), (t / QS) & 1, p.err);
+            mbar_wait(smem_u32(&bars->do_full[t % QS]), (t / QS) & 1, p.wc);
     } else if (warp == 1 && lane == 0 && nt > 0) {
         // ---------------- MMA issuer
         // Per query tile i (TMEM: S = S^T then P^T; DP = dP^T then dQ_i):
@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t id_mnmn = idesc_bf16_f32(BT, HD, true, true);
         auto issue_s = [&](int t) -> bool {
             const int s = t % QS;
-            if (!mbar_wait(smem_u32(&bars->q_full[s]), (t / QS) & 1, p.err)) return false;
+            if (!mbar_wait(smem_u32(&bars->q_full[s]), (t / QS) & 1, p.wc)) return false;
             tc_fence_after();
             const uint32_t qaddr = sbase + kQOff + s * 2 * kTile;
 #pragma unroll
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             return true;
         };
         auto issue_dp = [&](int t) -> bool {
-            if (!mbar_wait(smem_u32(&bars->do_full[t % QS]), (t / QS) & 1, p.err)) return false;
+            if (!mbar_wait(smem_u32(&bars->do_full[t % QS]), (t / QS) & 1, p.wc)) return false;
             tc_fence_after();
             const uint32_t oaddr = sbase + kQOff + (t % QS) * 2 * kTile + kTile;
 #pragma unroll
@@ -310,15 +310,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(smem_u32(&bars->dp_full));
             return true;
         };
-        bool ok = mbar_wait(smem_u32(&bars->kv_full), 0, p.err) && issue_s(0);
+        // tiles whose five MMAs were issued, per query stripe: added to the
+        // (round, device) counter when the stripe changes
+        QTileIter it = qiter_begin(g.layout, N, G, e, b, nqs, rows_b);
+        int cnt_d = -1, n_full = 0, n_part = 0;
+        auto flush_counts = [&]() {
+            if (p.tile_stats && cnt_d >= 0 && (n_full | n_part)) {
+                const int rr = ring_round_of(cnt_d, e, N);
+                atomicAdd((unsigned long long *)&p.tile_stats[rr * N + cnt_d], (unsigned long long)n_full);
+                atomicAdd((unsigned long long *)&p.tile_stats[N * N + rr * N + cnt_d], (unsigned long long)n_part);
+            }
+            n_full = n_part = 0;
+        };
+        bool ok = mbar_wait(smem_u32(&bars->kv_full), 0, p.wc) && issue_s(0);
         if (ok) ok = issue_dp(0);
-        for (int i = 0; i < nt && ok; ++i) {
+        for (int i = 0; i < nt && ok; ++i, qiter_next(it, g.layout, N, G, e, b, nqs, rows_b)) {
             const int s = i % QS;
             const uint32_t qaddr = sbase + kQOff + s * 2 * kTile;
             const uint32_t oaddr = qaddr + kTile;
             // dV += P^T dO: P^T (bf16 pairs) in TMEM columns [0,32) for
             // queries 0..63 and [64,96) for queries 64..127
-            if (!mbar_wait(smem_u32(&bars->p_ready), i & 1, p.err)) break;
+            if (!mbar_wait(smem_u32(&bars->p_ready), i & 1, p.wc)) break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < BT / 16; ++kk)
@@ -326,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        sdesc_sw128(oaddr + kk * 2048, kBox, 1024), id_kmn, (i > 0 || kk > 0) ? 1u : 0u);
             if (i + 1 < nt && !issue_s(i + 1)) break;
             // dQ_i = dS K (A = dS, MN-major view of the smem tile) -> DP columns
-            if (!mbar_wait(smem_u32(&bars->ds_ready), i & 1, p.err)) break;
+            if (!mbar_wait(smem_u32(&bars->ds_ready), i & 1, p.wc)) break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < BT / 16; ++kk)
@@ -340,16 +352,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                        sdesc_sw128(qaddr + kk * 2048, kBox, 1024), id_kmn, (i > 0 || kk > 0) ? 1u : 0u);
             // Q_i (and its statistics) are free once dK_i completes
             if (i + QS < nt) mma_commit(smem_u32(&bars->q_empty[s]));
+            if (it.d != cnt_d) {
+                flush_counts();
+                cnt_d = it.d;
+            }
+            if (it.has_diag && it.a == it.a_lo) ++n_part;
+            else ++n_full;
             if (i + 1 < nt) {
-                if (!mbar_wait(smem_u32(&bars->dq_free), i & 1, p.err)) break;
+                if (!mbar_wait(smem_u32(&bars->dq_free), i & 1, p.wc)) break;
                 tc_fence_after();
                 if (!issue_dp(i + 1)) break;
             }
         }
+        flush_counts();
         if (ok) mma_commit(smem_u32(&bars->acc_done));
         // every MMA issued above completes before TMEM is freed (error paths)
         mma_commit(smem_u32(&bars->drain));
-        mbar_wait(smem_u32(&bars->drain), 0, p.err);
+        mbar_wait(smem_u32(&bars->drain), 0, p.wc);
     } else if (warp >= 4) {
         // ---------------- compute: two warpgroups split the 128 query columns
         // of S^T/dP^T (64 each) and the HD columns of dQ_i, dK, dV (HD/2 each)
@@ -376,8 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // written to TMEM as the A operand of dV += P^T dO
         uint32_t pkP[32];
         auto compute_p = [&](const QTileIter &t, int i) -> bool {
-            if (!mbar_wait(smem_u32(&bars->q_full[i % QS]), (i / QS) & 1, p.err)) return false;
-            if (!mbar_wait(smem_u32(&bars->s_full), i & 1, p.err)) return false;
+            if (!mbar_wait(smem_u32(&bars->q_full[i % QS]), (i / QS) & 1, p.wc)) return false;
+            if (!mbar_wait(smem_u32(&bars->s_full), i & 1, p.wc)) return false;
             tc_fence_after();
             const float *sL = stat_ptr(i);
             const bool diag = t.has_diag && t.a == t.a_lo;
@@ -419,23 +438,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pending = -1;
             }
         };
-        // tiles that ran, per query stripe: counted by one thread as their dS
-        // is formed and added to the (round, device) counter when the stripe
-        // changes
-        int cnt_d = -1, n_full = 0, n_part = 0;
-        auto flush_counts = [&]() {
-            if (p.tile_stats && cnt_d >= 0 && (n_full | n_part)) {
-                const int rr = ring_round_of(cnt_d, e, N);
-                atomicAdd((unsigned long long *)&p.tile_stats[rr * N + cnt_d], (unsigned long long)n_full);
-                atomicAdd((unsigned long long *)&p.tile_stats[N * N + rr * N + cnt_d], (unsigned long long)n_part);
-            }
-            n_full = n_part = 0;
-        };
-        const bool counter = warp == 4 && lane == 0;
         if (ok) ok = compute_p(cur, 0);
         for (int i = 0; i < nt && ok; ++i) {
             // ---- dS = P * (dP - Delta) -> smem (A operand of dQ and dK)
-            if (!mbar_wait(smem_u32(&bars->dp_full), i & 1, p.err)) {
+            if (!mbar_wait(smem_u32(&bars->dp_full), i & 1, p.wc)) {
                 ok = false;
                 break;
             }
@@ -466,14 +472,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars->ds_ready));
-            if (counter) {
-                if (cur.d != cnt_d) {
-                    flush_counts();
-                    cnt_d = cur.d;
-                }
-                if (cur.has_diag && cur.a == cur.a_lo) ++n_part;
-                else ++n_full;
-            }
             // the previous tile's dQ reduce has had dS_i's time to read its
             // staging: return that dO buffer to the producer now
             if (wg == 1 && lane == 0) release_pending();
@@ -487,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             // ---- dQ_i readout -> fp32 accumulator
-            if (!mbar_wait(smem_u32(&bars->dq_full), i & 1, p.err)) {
+            if (!mbar_wait(smem_u32(&bars->dq_full), i & 1, p.wc)) {
                 ok = false;
                 break;
             }
@@ -588,11 +586,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        if (counter) flush_counts();
         if (wg == 1 && lane == 0) release_pending();
         if (lane == 0) bulk_wait_group0();
         if (ok) {
-            ok = mbar_wait(smem_u32(&bars->acc_done), 0, p.err);
+            ok = mbar_wait(smem_u32(&bars->acc_done), 0, p.wc);
             tc_fence_after();
         }
         // ---------------- epilogue: this warpgroup's columns of dK, dV
@@ -760,7 +757,7 @@ int launch_bwd_hd(const void *q, const void *k, const void *v, const void *o, co
     p.dk = (__nv_bfloat16 *)dk;
     p.dv = (__nv_bfloat16 *)dv;
     p.tile_stats = tile_stats;
-    p.err = device_status();
+    p.wc = device_wait_ctl();
     const int64_t nk = (g.L + BT - 1) / BT;
     const int64_t nblocks = nk * g.N * bh_kv;  // one CTA per key tile of every key/value head
     if (nblocks > 0x7fffffffll) return STRIPED_ERR_UNSUPPORTED;

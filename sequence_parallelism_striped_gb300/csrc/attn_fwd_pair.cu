@@ -57,7 +57,7 @@ struct PairParams {
     __nv_bfloat16 *o;
     float *lse;
     int64_t *tile_stats;
-    DeviceStatus *err;
+    WaitCtl wc;  // status word, wait bound, test hook
 };
 
 __global__ void __launch_bounds__(kPThreads, 1)
@@ -121,13 +121,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         // test hook: the first K/V tile is never loaded, so every wait on it
         // runs out (the kernel must then record the timeout and return)
-        const bool skip_first = injected_fault(p.err) == kInjectFwdSkipKV;
+        const bool skip_first = p.wc.inject == kInjectFwdSkipKV;
         int j = 0;
         for (int e = 0; e < N; ++e) {
             bool ok = true;
             for (int b = 0; b < ntr; ++b, ++j) {
                 const int s = j % PNS;
-                if (j >= PNS && !mbar_wait(smem_u32(&bars->kv_empty[s]), ((j / PNS) + 1) & 1, p.err)) {
+                if (j >= PNS && !mbar_wait(smem_u32(&bars->kv_empty[s]), ((j / PNS) + 1) & 1, p.wc)) {
                     ok = false;
                     break;
                 }
@@ -145,18 +145,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         // loads [0, j) and Q were issued: wait (bounded) for the last of each
         // stage, so that on an error path none lands after the CTA has exited
-        mbar_wait(qb, 0, p.err);
+        mbar_wait(qb, 0, p.wc);
         for (int t = j > PNS ? j - PNS : 0; t < j; ++t)
-            if (!(skip_first && t == 0)) mbar_wait(smem_u32(&bars->kv_full[t % PNS]), (t / PNS) & 1, p.err);
+            if (!(skip_first && t == 0)) mbar_wait(smem_u32(&bars->kv_full[t % PNS]), (t / PNS) & 1, p.wc);
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
         constexpr uint32_t idesc_qk = idesc_bf16_f32(PB, PB, false, false);
         constexpr uint32_t idesc_pv = idesc_bf16_f32(PB, PHD, false, true);
-        bool ok = mbar_wait(smem_u32(&bars->q_full), 0, p.err);
+        bool ok = mbar_wait(smem_u32(&bars->q_full), 0, p.wc);
         tc_fence_after();
         auto issue_s = [&](int x, int t) -> bool {
             const int s = t % PNS;
-            if (!mbar_wait(smem_u32(&bars->kv_full[s]), (t / PNS) & 1, p.err)) return false;
+            if (!mbar_wait(smem_u32(&bars->kv_full[s]), (t / PNS) & 1, p.wc)) return false;
             tc_fence_after();
             const uint32_t qaddr = sbase + kPQOff + x * kPTile;
             const uint32_t kaddr = sbase + kPKVOff + s * kPStage;
@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             return true;
         };
         auto issue_pv = [&](int x, int t) -> bool {
-            if (!mbar_wait(smem_u32(&bars->p_ready[x]), t & 1, p.err)) return false;
+            if (!mbar_wait(smem_u32(&bars->p_ready[x]), t & 1, p.wc)) return false;
             tc_fence_after();
             const uint32_t vaddr = sbase + kPKVOff + (t % PNS) * kPStage + kPTile;
 #pragma unroll
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         // every MMA issued above completes before TMEM is freed (error paths)
         mma_commit(smem_u32(&bars->drain));
-        mbar_wait(smem_u32(&bars->drain), 0, p.err);
+        mbar_wait(smem_u32(&bars->drain), 0, p.wc);
     } else if (warp >= 2) {
         // ---------------- softmax + epilogue of one query tile
         const int x = (warp - 2) >> 2;       // group: 0 (stripe d0) or 1 (stripe d0 + 1)
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const int lim_diag = ri + sp.diag_off;
             int n_full = 0, n_part = 0;  // tiles of this round turned into P below
             for (int b = 0; b < ntr; ++b, ++j) {
-                if (!mbar_wait(smem_u32(&bars->s_full[x]), j & 1, p.err)) {
+                if (!mbar_wait(smem_u32(&bars->s_full[x]), j & 1, p.wc)) {
                     ok = false;
                     break;
                 }
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 m_ref = m_new;
                 if (j > 0) {
                     // PV(j-1) of this group must be complete before O is touched
-                    if (!mbar_wait(smem_u32(&bars->o_done[x]), (j - 1) & 1, p.err)) {
+                    if (!mbar_wait(smem_u32(&bars->o_done[x]), (j - 1) & 1, p.wc)) {
                         ok = false;
                         break;
                     }
@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         // ---------------- epilogue
         if (ok) {
-            ok = mbar_wait(smem_u32(&bars->o_done[x]), (nt - 1) & 1, p.err);
+            ok = mbar_wait(smem_u32(&bars->o_done[x]), (nt - 1) & 1, p.wc);
             tc_fence_after();
         }
         const int64_t i = (int64_t)a * PB + ri;
@@ -388,7 +388,7 @@ int launch_tc_fwd_pair(const void *q, const void *k, const void *v, void *o, flo
     p.o = reinterpret_cast<__nv_bfloat16 *>(o);
     p.lse = lse;
     p.tile_stats = tile_stats;
-    p.err = device_status();
+    p.wc = device_wait_ctl();
     const int64_t nblocks = (g.L / PB) * (g.N / 2) * g.BH;
     if (nblocks > 0x7fffffffll) return STRIPED_ERR_UNSUPPORTED;
     tc_fwd_pair_kernel<<<(unsigned)nblocks, kPThreads, kPSmemBytes, stream>>>(mq, mk, mv, p);

@@ -62,7 +62,7 @@ struct FwdParams {
     float *o_acc, *lse_acc;       // round mode: accumulator
     __nv_bfloat16 *o_out;         // round mode: optional copy
     int64_t *tile_stats;
-    DeviceStatus *err;                     // device error word
+    WaitCtl wc;  // status word, wait bound, test hook
 };
 
 template <int NS>
@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmV);
         // test hook: the first K/V tile is never loaded, so every wait on it
         // runs out (the kernel must then record the timeout and return)
-        const bool skip_first = injected_fault(p.err) == kInjectFwdSkipKV;
+        const bool skip_first = p.wc.inject == kInjectFwdSkipKV;
         int j = 0;
         bool ok = true;
         for (int r = 0; r < nrounds && ok; ++r) {
@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int b = 0; b < ntr; ++b, ++j) {
                 const int s = j % NS;
                 const int kb = sq.start + b;  // key tile in the slice
-                if (j >= NS && !mbar_wait(smem_u32(&bars->kv_empty[s]), ((j / NS) + 1) & 1, p.err)) {
+                if (j >= NS && !mbar_wait(smem_u32(&bars->kv_empty[s]), ((j / NS) + 1) & 1, p.wc)) {
                     ok = false;
                     break;
                 }
@@ -200,16 +200,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // loads [0, j) were issued: wait (bounded) for the last of each stage,
         // so that on an error path none lands after the CTA has exited
         for (int t = j > NS ? j - NS : 0; t < j; ++t)
-            if (!(skip_first && t == 0)) mbar_wait(smem_u32(&bars->kv_full[t % NS]), (t / NS) & 1, p.err);
+            if (!(skip_first && t == 0)) mbar_wait(smem_u32(&bars->kv_full[t % NS]), (t / NS) & 1, p.wc);
     } else if (warp == 1 && lane == 0 && nt > 0) {
         // ---------------- MMA issuer
         constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
         constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, HD, false, true);
-        bool ok = mbar_wait(smem_u32(&bars->q_full), 0, p.err);
+        bool ok = mbar_wait(smem_u32(&bars->q_full), 0, p.wc);
         tc_fence_after();
         auto issue_s = [&](int t) -> bool {
             const int s = t % NS;
-            if (!mbar_wait(smem_u32(&bars->kv_full[s]), (t / NS) & 1, p.err)) return false;
+            if (!mbar_wait(smem_u32(&bars->kv_full[s]), (t / NS) & 1, p.wc)) return false;
             tc_fence_after();
             const uint32_t kaddr = sbase + kKVOff + s * kStageBytes;
             const uint32_t dS = (t & 1) ? tS1 : tS0;
@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = issue_s(0);
         if (ok && nt > 1) ok = issue_s(1);
         for (int j = 0; j < nt && ok; ++j) {
-            if (!mbar_wait(smem_u32(&bars->p_ready), j & 1, p.err)) break;
+            if (!mbar_wait(smem_u32(&bars->p_ready), j & 1, p.wc)) break;
             tc_fence_after();
             const int s = j % NS;
             const uint32_t vaddr = sbase + kKVOff + s * kStageBytes + kTileBytes;
@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // every MMA issued above completes before TMEM is freed (error paths)
         mma_commit(smem_u32(&bars->drain));
-        mbar_wait(smem_u32(&bars->drain), 0, p.err);
+        mbar_wait(smem_u32(&bars->drain), 0, p.wc);
     } else if (warp >= 2) {
         // ---------------- softmax + epilogue
         const int quarter = warp & 3;
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int n_full = 0, n_part = 0;  // tiles of this round turned into P below
             for (int b = 0; b < ntr; ++b, ++j) {
                 const uint32_t tS = ((j & 1) ? tS1 : tS0) + lane_off;
-                if (!mbar_wait(smem_u32(&bars->s_full[j & 1]), (j >> 1) & 1, p.err)) {
+                if (!mbar_wait(smem_u32(&bars->s_full[j & 1]), (j >> 1) & 1, p.wc)) {
                     ok = false;
                     break;
                 }
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_ref = m_new;
                 if (j > 0) {
                     // PV_{j-1} must be complete before O is touched or PV_j issued
-                    if (!mbar_wait(smem_u32(&bars->o_done), (j - 1) & 1, p.err)) {
+                    if (!mbar_wait(smem_u32(&bars->o_done), (j - 1) & 1, p.wc)) {
                         ok = false;
                         break;
                     }
@@ -384,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // ---------------- epilogue
         if (ok && nt > 0) {
-            ok = mbar_wait(smem_u32(&bars->o_done), (nt - 1) & 1, p.err);
+            ok = mbar_wait(smem_u32(&bars->o_done), (nt - 1) & 1, p.wc);
             tc_fence_after();
         }
         const int64_t i = (int64_t)ag * BM + ri;
@@ -529,7 +529,7 @@ int launch_tc_fwd(const void *q, const void *k, const void *v, void *o, float *l
     p.o = reinterpret_cast<__nv_bfloat16 *>(o);
     p.lse = lse;
     p.tile_stats = tile_stats;
-    p.err = device_status();
+    p.wc = device_wait_ctl();
     const int64_t nq = (g.L + BM - 1) / BM;
     const int64_t nblocks = nq * g.N * g.BH;
     if (nblocks > 0x7fffffffll) return STRIPED_ERR_UNSUPPORTED;
@@ -558,7 +558,7 @@ int launch_tc_round(const void *q_d, const void *k_e, const void *v_e, float *o_
     p.lse_acc = lse_acc;
     p.o_out = reinterpret_cast<__nv_bfloat16 *>(o_out);
     p.tile_stats = tile_stats;
-    p.err = device_status();
+    p.wc = device_wait_ctl();
     const int64_t nq = (g.L + BM - 1) / BM;
     if (g.BH > 65535) return STRIPED_ERR_UNSUPPORTED;
     dim3 grid((unsigned)nq, (unsigned)g.BH);

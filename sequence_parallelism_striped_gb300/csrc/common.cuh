@@ -21,22 +21,28 @@ namespace striped {
 // bounded waits; a timeout is recorded in the library's device status block
 // (owned by api.cu, passed to every kernel as a pointer)
 // --------------------------------------------------------------------------
-// Per-device control block of the library.  `error` is the status the next
-// striped_check_error() returns (one word per device, shared by every stream
-// and caller on it).  `wait_limit_ns` bounds every mbarrier wait of the
-// kernels (wall-clock time read from %globaltimer; every legitimate wait is
-// microseconds).  `inject` is a test hook that makes one kind of kernel skip
-// one of its own loads, so that the waits on it run out (kInject* below);
-// it is 0 outside tests.
+// The library's device-side status word: the status the next
+// striped_check_error() returns (one per device, shared by every stream and
+// caller on it).
 struct DeviceStatus {
     int error;
-    int inject;
-    unsigned long long wait_limit_ns;
 };
 constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
 constexpr int kInjectNone = STRIPED_FAULT_NONE;
 constexpr int kInjectFwdSkipKV = STRIPED_FAULT_FWD_SKIP_KV;  // forward TMA producers skip their first K/V tile
 constexpr int kInjectBwdSkipQ = STRIPED_FAULT_BWD_SKIP_Q;    // backward TMA producers skip their first Q tile
+
+// What every wait of a launch needs, passed by value in the kernel
+// parameters (so a wait reads nothing from memory): where to record a
+// failure, the bound of every mbarrier wait (wall-clock time read from
+// %globaltimer; every legitimate wait is microseconds) and the test hook
+// that makes one kind of kernel skip one of its own loads (kInject*, 0
+// outside tests).
+struct WaitCtl {
+    DeviceStatus *st;
+    unsigned long long limit_ns;
+    int inject;
+};
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
@@ -44,18 +50,11 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
-__device__ __forceinline__ void record_timeout(DeviceStatus *st) {
-    if (st) atomicExch(&st->error, STRIPED_ERR_TIMEOUT);
-}
-
 __device__ __forceinline__ void record_error(DeviceStatus *st, int code) {
     if (st) atomicExch(&st->error, code);
 }
 
-// The test hook of this launch (read once per CTA by the producers).
-__device__ __forceinline__ int injected_fault(const DeviceStatus *st) {
-    return st ? *reinterpret_cast<const volatile int *>(&st->inject) : kInjectNone;
-}
+__device__ __forceinline__ void record_timeout(const WaitCtl &w) { record_error(w.st, STRIPED_ERR_TIMEOUT); }
 
 // --------------------------------------------------------------------------
 // tile schedule
@@ -230,17 +229,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Wait for the phase of parity `parity` to complete; false (and the device
 // status set to STRIPED_ERR_TIMEOUT) if the bound runs out.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, DeviceStatus *st) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl &w) {
     for (int it = 0; it < 64; ++it)
         if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t limit =
-        st ? *reinterpret_cast<const volatile unsigned long long *>(&st->wait_limit_ns) : kDefaultWaitLimitNs;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 255u && global_timer_ns() - t0 > limit) break;
+        if ((it & 255u) == 255u && global_timer_ns() - t0 > w.limit_ns) break;
     }
-    record_timeout(st);
+    record_timeout(w);
     return false;
 }
 

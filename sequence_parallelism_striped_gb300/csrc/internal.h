@@ -42,11 +42,17 @@ class PerDeviceOnce {
     int status_[kMaxDevices] = {};
 };
 
-// Device address of the library's status block on the current device (where
-// bounded waits record STRIPED_ERR_TIMEOUT; see DeviceStatus in common.cuh),
-// or nullptr on failure.  Looked up once per device under a lock.
+// Device address of the library's status word on the current device (where
+// bounded waits record STRIPED_ERR_TIMEOUT), or nullptr on failure.  Looked
+// up once per device under a lock.
 struct DeviceStatus;
 DeviceStatus *device_status();
+
+// The wait control of a launch on the current device: its status word, the
+// wait bound and the test hook as set by striped_test_inject (defaults: 2 s,
+// none).
+struct WaitCtl;
+WaitCtl device_wait_ctl();
 
 // Geometry of one attention launch.  Every tensor is addressed as
 // [BH][N stripes][L rows][D] with stripe e of head bh starting at element

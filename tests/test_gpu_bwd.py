@@ -102,7 +102,8 @@ def test_bwd_invariants_on_device():
     full GPU tensors, under the bf16 error model of grad_sum_errors."""
     B, H, S, D, N = 1, 4, 4096, 128, 8
     x, (dq, dk, dv), _ = _run(B, H, S, D, N, sp.STRIPED, torch.bfloat16, seed=7)
-    inv = grad_sum_errors(dv, dk, x["do"].to(DEV), x["q"].to(DEV))
+    pos = torch.as_tensor(oracle.layout_positions(S, N, sp.STRIPED), device=DEV)
+    inv = grad_sum_errors(dv, dk, x["do"].to(DEV), x["q"].to(DEV), pos)
     print("gradient invariants", inv)
     assert inv["dv"][2] <= 1.0 and inv["dk"][2] <= 1.0, inv
 

@@ -139,6 +139,7 @@ def test_gqa_mid_size_sampled():
     ev = float(np.abs(dv[0, kvh, kidx].double().cpu().numpy() - dv_r).max())
     print("gqa mid tail-key max errors dk dv", ek, ev)
     assert ek <= 2e-2 * np.sqrt(G) and ev <= 2e-2 * np.sqrt(G)
-    inv = grad_sum_errors(dv, dk, x["do"].to(DEV), x["q"].to(DEV), G=G)
+    pos = torch.as_tensor(oracle.layout_positions(S, N, sp.STRIPED), device=DEV)
+    inv = grad_sum_errors(dv, dk, x["do"].to(DEV), x["q"].to(DEV), pos, G=G)
     print("gqa mid gradient invariants", inv)
     assert inv["dv"][2] <= 1.0 and inv["dk"][2] <= 1.0, inv

@@ -55,11 +55,6 @@ def test_full_size_sampled_parity(name):
     st = stats.cpu().numpy()
     assert np.array_equal(st[0], B * H * full) and np.array_equal(st[1], B * H * part)
 
-    # invariants on every head and column (fp64 sums of the GPU tensors)
-    inv = grad_sum_errors(dv, dk, x["do"].to(DEV), x["q"].to(DEV))
-    print(name, "gradient invariants (max error, smallest bound, max error/bound):", inv)
-    assert inv["dv"][2] <= 1.0 and inv["dk"][2] <= 1.0, inv
-
     # 4096 sampled query rows: O, LSE, dQ
     rows = sample_rows(4096, B, H, S, seed=0).numpy()
     srow = _row_of_position(rows[:, 2], S, N)
@@ -110,6 +105,12 @@ def test_full_size_sampled_parity(name):
           f"max |dk| {np.abs(dk_ref).max():.3f} |dv| {np.abs(dv_ref).max():.3f}",
           f"(oracle: {t_keys:.1f} s on {oracle.default_threads()} threads)")
     assert ek <= 2e-2 and ev <= 2e-2
+
+    # invariants on every head and column (fp64 sums of the GPU tensors)
+    pos = torch.as_tensor(oracle.layout_positions(S, N, sp.STRIPED), device=DEV)
+    inv = grad_sum_errors(dv, dk, x["do"].to(DEV), x["q"].to(DEV), pos)
+    print(name, "gradient invariants (max error, smallest bound, max error/bound):", inv)
+    assert inv["dv"][2] <= 1.0 and inv["dk"][2] <= 1.0, inv
 
 
 def test_mid_contiguous_and_per_round_sampled():
@@ -163,7 +164,7 @@ def test_mid_contiguous_and_per_round_sampled():
     assert worst["o"] <= 2e-2 and worst["dq"] <= 2e-2 and worst["o_round"] <= 2e-2
     assert worst["lse"] <= 1e-3 and worst["lse_round"] <= 1e-3
     # gradient invariants of the contiguous backward on every head
-    inv = grad_sum_errors(dv, dk, do, q)
+    inv = grad_sum_errors(dv, dk, do, q, torch.arange(S, device=DEV))
     print("mid contiguous gradient invariants", inv)
     assert inv["dv"][2] <= 1.0 and inv["dk"][2] <= 1.0, inv
 
@@ -203,6 +204,7 @@ def test_mid_zigzag_sampled():
             worst[key] = max(worst[key], float(np.abs(got[key][sel] - ref).max()))
     print("mid zig-zag max errors", worst)
     assert worst["o"] <= 2e-2 and worst["dq"] <= 2e-2 and worst["lse"] <= 1e-3
-    inv = grad_sum_errors(dv, dk, x["do"].to(DEV), x["q"].to(DEV))
+    inv = grad_sum_errors(dv, dk, x["do"].to(DEV), x["q"].to(DEV),
+                          torch.as_tensor(oracle.zigzag_positions(S, N), device=DEV))
     print("mid zig-zag gradient invariants", inv)
     assert inv["dv"][2] <= 1.0 and inv["dk"][2] <= 1.0, inv
