@@ -741,6 +741,13 @@ int launch_bwd_hd(const void *q, const void *k, const void *v, const void *o, co
                                                     stats, dq_acc, g.L, nq, g.BH * g.N * (int64_t)nq * BT);
     int st = cuda_status(cudaGetLastError());
     if (st != STRIPED_OK) return st;
+    if (HD == 128 && bwd_pair_eligible(g)) {
+        // striped, whole tiles, even N: two key tiles per CTA pair
+        st = launch_tc_bwd_pair_main(q, k, v, dO, dq_acc, stats, dk, dv, g, tile_stats, stream);
+        if (st != STRIPED_OK) return st;
+        bwd_post_kernel<<<sms * 8, 256, 0, stream>>>(dq_acc, (__nv_bfloat16 *)dq, rows * HD / 8, g.scale);
+        return cuda_status(cudaGetLastError());
+    }
     CUtensorMap mq, mk, mv, mdo;
     const int64_t bh_kv = g.BH / g.G;
     if ((st = make_bf16_map(&mq, q, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 128)) ||
