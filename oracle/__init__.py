@@ -24,6 +24,9 @@ Causal Transformers"):
 * grouped-query attention (query head h reads key/value head h // G) is not
   on the pages either: ``attn_fwd_gqa`` / ``attn_bwd_gqa`` compose the
   per-head definition, summing the gradients of a shared key/value head;
+* one ring round's share of the gradients (``bwd_block``): the pairs of one
+  query block and one key block, with the rows' full-sequence LSE and
+  Jacobian sums -- §Summary (blocks circulate, each device accumulates);
 * packed variable-length batches (not on the pages): ``attn_fwd_varlen`` /
   ``attn_bwd_varlen`` apply the definition to each sequence on its own, and
   ``varlen_positions`` places each sequence on its own inside every device.
@@ -83,6 +86,7 @@ def _load():
             lib.oracle_bwd_rows.argtypes = [P, P, P, P, I64, I64, Dbl, P, I64, P, P, P, I]
             lib.oracle_bwd_keys.argtypes = [P, P, P, P, I64, I64, Dbl, P, P, I64, P, I64, P, P, I]
             lib.oracle_attn_bwd.argtypes = [P, P, P, P, I64, I64, Dbl, P, P, P, I]
+            lib.oracle_bwd_block.argtypes = [P, P, P, P, P, I64, P, P, P, I64, I64, Dbl, P, P, P]
             lib.oracle_tile_counts_bruteforce.argtypes = [I64, I, I64, I64, I, P, P]
             lib.oracle_tile_counts_closed.argtypes = [I64, I, I64, I, P, P]
             lib.oracle_critical_path.argtypes = [P, P, I]
@@ -203,6 +207,25 @@ def attn_bwd(q, k, v, dO, scale: float, nthreads: int | None = None):
     dv = np.empty((S, D), dtype=np.float64)
     _load().oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), S, D, float(scale), _ptr(dq),
                             _ptr(dk), _ptr(dv), nthreads or default_threads())
+    return dq, dk, dv
+
+
+def bwd_block(q, dO, qpos, lse, J, k, v, kpos, scale: float):
+    """One ring round's share of the gradients: query rows q, dO [nq, D] at
+    positions qpos, key rows k, v [nk, D] at positions kpos, pairs with key
+    position <= query position; lse, J are the query rows' full-sequence
+    values.  Returns the partial (dq [nq, D], dk [nk, D], dv [nk, D])."""
+    q, dO, k, v = _f64(q), _f64(dO), _f64(k), _f64(v)
+    lse, J = _f64(lse), _f64(J)
+    qpos = np.ascontiguousarray(np.asarray(qpos, dtype=np.int64))
+    kpos = np.ascontiguousarray(np.asarray(kpos, dtype=np.int64))
+    nq, D = q.shape
+    nk = k.shape[0]
+    dq = np.empty((nq, D))
+    dk = np.empty((nk, D))
+    dv = np.empty((nk, D))
+    _load().oracle_bwd_block(_ptr(q), _ptr(dO), _ptr(qpos), _ptr(lse), _ptr(J), nq, _ptr(k), _ptr(v), _ptr(kpos),
+                             nk, D, float(scale), _ptr(dq), _ptr(dk), _ptr(dv))
     return dq, dk, dv
 
 

@@ -329,6 +329,38 @@ void oracle_attn_bwd(const double *q, const double *k, const double *v, const do
     free(J);
 }
 
+/* One ring round's share of the gradients (research.elamur.ai summary page,
+ * §Summary: key/value blocks circulate and each device accumulates the work
+ * of the block it holds).  The round's query rows q, dO [nq, D] sit at
+ * positions qpos[], its key rows k, v [nk, D] at kpos[]; a pair takes part
+ * iff kpos[t] <= qpos[p].  lse[p] and J[p] are the query rows' values over
+ * the WHOLE sequence (a round sees only its own keys, the softmax of a row
+ * spans them all).  Writes the round's partial dq [nq, D] (summed over the
+ * round's keys) and dk, dv [nk, D] (summed over the round's queries):
+ *   P_pt = exp(scale <q_p, k_t> - lse_p),  dS_pt = P_pt (<dO_p, v_t> - J_p),
+ *   dq_p = scale sum_t dS_pt k_t,  dk_t = scale sum_p dS_pt q_p,
+ *   dv_t = sum_p P_pt dO_p.                                               */
+void oracle_bwd_block(const double *q, const double *dO, const int64_t *qpos, const double *lse,
+                      const double *J, int64_t nq, const double *k, const double *v, const int64_t *kpos,
+                      int64_t nk, int64_t D, double scale, double *dq, double *dk, double *dv) {
+    for (int64_t i = 0; i < nq * D; ++i) dq[i] = 0.0;
+    for (int64_t i = 0; i < nk * D; ++i) dk[i] = dv[i] = 0.0;
+    for (int64_t p = 0; p < nq; ++p) {
+        const double *qp = q + p * D, *dop = dO + p * D;
+        for (int64_t t = 0; t < nk; ++t) {
+            if (kpos[t] > qpos[p]) continue;
+            const double *kt = k + t * D, *vt = v + t * D;
+            const double P = exp(scale * dot(qp, kt, D) - lse[p]);
+            const double dS = P * (dot(dop, vt, D) - J[p]);
+            for (int64_t c = 0; c < D; ++c) {
+                dq[p * D + c] += scale * dS * kt[c];
+                dk[t * D + c] += scale * dS * qp[c];
+                dv[t * D + c] += P * dop[c];
+            }
+        }
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Per-round tile accounting                                                */
 /* ------------------------------------------------------------------------ */

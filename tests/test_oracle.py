@@ -471,3 +471,52 @@ def test_varlen_positions_independent_enumeration(oracle_lib, N, cu, layout):
     pos = oracle.varlen_positions(cu, N, layout)
     for p, row in row_of.items():
         assert pos[row] == p, (p, row)
+
+
+@pytest.mark.parametrize("layout", [STRIPED, CONTIGUOUS, ZIGZAG])
+def test_bwd_block_rounds_sum_to_the_full_backward(oracle_lib, layout):
+    """The per-round gradient shares of every (device, key block) pair of the
+    ring add up to the full backward (pinned itself to torch autograd): dq
+    of a query row over its device's N rounds, dk / dv of a key row over the
+    N devices that see its block."""
+    S, D, N = 64, 8, 4
+    rng = np.random.default_rng(5)
+    q, k, v, do = (rng.standard_normal((S, D)) for _ in range(4))
+    scale = 0.4
+    dq_ref, dk_ref, dv_ref = oracle.attn_bwd(q, k, v, do, scale)
+    lse, J, _ = oracle.bwd_rows(q, k, v, do, scale, want_dq=False)
+    pos = oracle.layout_positions(S, N, layout)
+    L = S // N
+    dq = np.zeros((S, D))
+    dk = np.zeros((S, D))
+    dv = np.zeros((S, D))
+    for d in range(N):
+        qp = pos[d * L:(d + 1) * L]
+        for r in range(N):
+            e = (d - r) % N
+            kp = pos[e * L:(e + 1) * L]
+            gq, gk, gv = oracle.bwd_block(q[qp], do[qp], qp, lse[qp], J[qp], k[kp], v[kp], kp, scale)
+            dq[qp] += gq
+            dk[kp] += gk
+            dv[kp] += gv
+    for got, ref in ((dq, dq_ref), (dk, dk_ref), (dv, dv_ref)):
+        assert np.abs(got - ref).max() < 1e-11
+
+
+def test_bwd_block_special_cases(oracle_lib):
+    """One block holding the whole sequence is the full backward; a block
+    whose keys all come after its queries contributes nothing; J_p may be
+    taken as <dO_p, O_p> (the distributed form) with the same result."""
+    S, D = 24, 6
+    rng = np.random.default_rng(6)
+    q, k, v, do = (rng.standard_normal((S, D)) for _ in range(4))
+    scale = 0.5
+    ref = oracle.attn_bwd(q, k, v, do, scale)
+    o, lse = oracle.attn_fwd(q, k, v, scale)
+    J_dot = np.einsum("pd,pd->p", do, o)
+    allpos = np.arange(S)
+    got = oracle.bwd_block(q, do, allpos, lse, J_dot, k, v, allpos, scale)
+    for g, r in zip(got, ref):
+        assert np.abs(g - r).max() < 1e-11
+    z = oracle.bwd_block(q[:8], do[:8], allpos[:8], lse[:8], J_dot[:8], k[8:], v[8:], allpos[8:], scale)
+    assert all(np.all(x == 0.0) for x in z)
