@@ -269,6 +269,43 @@ int ring_round_fwd(const void *q_d, const void *k_e, const void *v_e, float *o_a
                    int64_t stride_bh, int64_t lse_stride_bh, int layout, int dtype, float scale,
                    int first_round, int64_t *tile_stats, void *stream);
 
+/*
+ * The backward of one ring round, for a ring of N processes that each hold
+ * one stripe (§Summary: key/value blocks circulate around the ring; here
+ * the gradients of a key/value block travel with it and are summed by every
+ * device it visits, then return to its owner).  bf16 only
+ * (STRIPED_ERR_UNSUPPORTED for fp32).  Every block is the device's own
+ * CONTIGUOUS [B, H, L, D] tensor (L = S/N rows of one stripe, in the
+ * layout's row order; 16-byte aligned), lse_d fp32 [B, H, L].
+ *
+ * ring_bwd_workspace_size: bytes of the per-device statistics workspace
+ * (softmax statistics of the device's L query rows padded to 128-row tiles),
+ * or 0 for invalid sizes.
+ *
+ * ring_bwd_prepare: once per backward, on device d: writes the statistics
+ * of its query block (LSE and Delta = <dO, O> per row) into `workspace` and
+ * zeroes its fp32 dQ sum dq_acc_d [B, H, L, D].
+ *
+ * ring_round_bwd: device d's round against the key/value block of stripe e
+ * (the block it holds in ring round (d - e) mod N): adds the round's dQ
+ * share into dq_acc_d and the round's dK, dV shares (scale applied to dK)
+ * into the fp32 sums dk_acc_e, dv_acc_e [B, H, L, D] that travel with the
+ * block; with first_round != 0 the sums are overwritten instead (the
+ * block's first round, on its own device).  Same mask and tile skipping as
+ * striped_attn_bwd; tile_stats gets the round's counts at [.][r][d].
+ *
+ * ring_bwd_finish: out = bf16(mul * acc) for n fp32 values (n a multiple of
+ * 8): dQ with mul = scale, the returned dK and dV sums with mul = 1.
+ */
+size_t ring_bwd_workspace_size(int64_t B, int64_t H, int64_t L, int64_t D, int dtype);
+int ring_bwd_prepare(const void *o_d, const float *lse_d, const void *dO_d, void *workspace, size_t ws_bytes,
+                     float *dq_acc_d, int64_t B, int64_t H, int64_t L, int64_t D, int dtype, void *stream);
+int ring_round_bwd(const void *q_d, const void *k_e, const void *v_e, const void *dO_d, const void *workspace,
+                   size_t ws_bytes, float *dq_acc_d, float *dk_acc_e, float *dv_acc_e, int d, int e, int64_t B,
+                   int64_t H, int64_t L, int64_t D, int N, int layout, int dtype, float scale, int first_round,
+                   int64_t *tile_stats, void *stream);
+int ring_bwd_finish(const float *acc, void *out, int64_t n, int dtype, float mul, void *stream);
+
 /* Tile edge T (queries x keys) the kernels for (dtype, D) skip and count
  * with; writes *Tq and *Tk.  Returns STRIPED_ERR_UNSUPPORTED if no kernel. */
 int striped_kernel_tile(int dtype, int64_t D, int *Tq, int *Tk);

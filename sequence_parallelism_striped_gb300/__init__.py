@@ -76,6 +76,11 @@ def load(build_if_missing: bool = True):
                                              F, P, P]
         lib.ring_round_fwd.argtypes = [P, P, P, P, P, P, I, I, I64, I64, I64, I64, I, I64, I64, I, I, F, I,
                                        P, P]
+        lib.ring_bwd_workspace_size.argtypes = [I64, I64, I64, I64, I]
+        lib.ring_bwd_workspace_size.restype = SZ
+        lib.ring_bwd_prepare.argtypes = [P, P, P, P, SZ, P, I64, I64, I64, I64, I, P]
+        lib.ring_round_bwd.argtypes = [P, P, P, P, P, SZ, P, P, P, I, I, I64, I64, I64, I64, I, I, I, F, I, P, P]
+        lib.ring_bwd_finish.argtypes = [P, P, I64, I, F, P]
         lib.striped_varlen_permute.argtypes = [P, P, P, I, I64, I64, I, I, I, P]
         lib.striped_varlen_unpermute.argtypes = [P, P, P, I, I64, I64, I, I, I, P]
         lib.striped_attn_fwd_varlen.argtypes = [P, P, P, P, P, P, I, I64, I64, I64, I, I, I, F, P, P]
@@ -299,6 +304,69 @@ def ring_round_fwd(q, k, v, o_acc, lse_acc, d: int, e: int, N: int, layout: int 
     oo = None if o_out is None else ctypes.c_void_p(_dev(o_out, "o_out").value + d * L * D * es)
     _check(load().ring_round_fwd(qd, ke, ve, oa, la, oo, d, e, B, H, L, D, N, S * D, S, layout,
                                  _dtype_code(q), float(scale), 1 if first_round else 0,
+                                 _ptr_or_null(tile_stats), _stream(stream)), "ring_round_fwd")
+
+
+# ------------------------------------------------------------------ one device of a ring
+def ring_bwd_workspace(q_d: torch.Tensor) -> torch.Tensor:
+    """Statistics workspace of ring_bwd_prepare / ring_round_bwd for a
+    device's block q_d [B, H, L, D] (bf16)."""
+    B, H, L, D = q_d.shape
+    n = int(load().ring_bwd_workspace_size(B, H, L, D, _dtype_code(q_d)))
+    if n == 0:
+        raise StripedError(-1, "ring_bwd_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=q_d.device)
+
+
+def ring_bwd_prepare(o_d, lse_d, dO_d, workspace, dq_acc, stream=None):
+    """Statistics of device d's query block into workspace; zero dq_acc."""
+    B, H, L, D = o_d.shape
+    _check(load().ring_bwd_prepare(_dev(o_d, "o_d"), _dev(lse_d, "lse_d"), _dev(dO_d, "dO_d"),
+                                   _dev(workspace, "workspace"), workspace.numel(), _dev(dq_acc, "dq_acc"),
+                                   B, H, L, D, _dtype_code(o_d), _stream(stream)), "ring_bwd_prepare")
+
+
+def ring_round_bwd(q_d, k_e, v_e, dO_d, workspace, dq_acc, dk_acc, dv_acc, d: int, e: int, N: int,
+                   layout: int = STRIPED, scale: float | None = None, first_round: bool = False,
+                   tile_stats: torch.Tensor | None = None, stream=None):
+    """Device d's backward round against key/value block e: dQ share into
+    dq_acc, dK/dV shares into (or, first_round, onto) dk_acc/dv_acc (fp32
+    [B, H, L, D] sums travelling with block e)."""
+    B, H, L, D = q_d.shape
+    if scale is None:
+        scale = 1.0 / D ** 0.5
+    for t, nm in ((dq_acc, "dq_acc"), (dk_acc, "dk_acc"), (dv_acc, "dv_acc")):
+        if t.dtype != torch.float32:
+            raise TypeError(f"{nm} must be fp32")
+    _check(load().ring_round_bwd(_dev(q_d, "q_d"), _dev(k_e, "k_e"), _dev(v_e, "v_e"), _dev(dO_d, "dO_d"),
+                                 _dev(workspace, "workspace"), workspace.numel(), _dev(dq_acc, "dq_acc"),
+                                 _dev(dk_acc, "dk_acc"), _dev(dv_acc, "dv_acc"), d, e, B, H, L, D, N, layout,
+                                 _dtype_code(q_d), float(scale), 1 if first_round else 0, _ptr_or_null(tile_stats),
+                                 _stream(stream)), "ring_round_bwd")
+
+
+def ring_bwd_finish(acc: torch.Tensor, mul: float, out: torch.Tensor | None = None, stream=None):
+    """out = bf16(mul * acc) (the final dQ with mul = scale, dK / dV with 1)."""
+    y = torch.empty(acc.shape, dtype=torch.bfloat16, device=acc.device) if out is None else out
+    _check(load().ring_bwd_finish(_dev(acc, "acc"), _dev(y, "out"), acc.numel(), BF16, float(mul),
+                                  _stream(stream)), "ring_bwd_finish")
+    return y
+
+
+def ring_round_fwd_block(q_d, k_e, v_e, o_acc, lse_acc, d: int, e: int, N: int, layout: int = STRIPED,
+                         scale: float | None = None, first_round: bool = False, o_out=None,
+                         tile_stats: torch.Tensor | None = None, stream=None):
+    """ring_round_fwd on one device's own contiguous blocks ([B, H, L, D]
+    tensors; o_acc fp32 of the same shape, lse_acc fp32 [B, H, L])."""
+    B, H, L, D = q_d.shape
+    if scale is None:
+        scale = 1.0 / D ** 0.5
+    if o_acc.dtype != torch.float32 or lse_acc.dtype != torch.float32:
+        raise TypeError("o_acc and lse_acc must be fp32")
+    oo = None if o_out is None else _dev(o_out, "o_out")
+    _check(load().ring_round_fwd(_dev(q_d, "q_d"), _dev(k_e, "k_e"), _dev(v_e, "v_e"), _dev(o_acc, "o_acc"),
+                                 _dev(lse_acc, "lse_acc"), oo, d, e, B, H, L, D, N, L * D, L, layout,
+                                 _dtype_code(q_d), float(scale), 1 if first_round else 0,
                                  _ptr_or_null(tile_stats), _stream(stream)), "ring_round_fwd")
 
 

@@ -462,6 +462,73 @@ int striped_attn_bwd_varlen(const void *q, const void *k, const void *v, const v
                            dtype, scale, tile_stats, stream, t);
 }
 
+size_t ring_bwd_workspace_size(int64_t B, int64_t H, int64_t L, int64_t D, int dtype) {
+    if (B < 1 || H < 1 || L < 1 || D < 1 || dtype != STRIPED_BF16) return 0;
+    const size_t nq = (size_t)((L + kTcTile - 1) / kTcTile);
+    return align256((size_t)(B * H) * nq * 2 * kTcTile * sizeof(float));
+}
+
+// the geometry of one device's blocks: contiguous [BH][L][D], no stripes
+static AttnGeom round_geom(int64_t B, int64_t H, int64_t L, int64_t D, int N, int layout, float scale) {
+    AttnGeom g{};
+    g.BH = B * H;
+    g.G = 1;
+    g.L = L;
+    g.D = D;
+    g.N = N;
+    g.layout = layout;
+    g.stride_bh = L * D;
+    g.stripe_stride = 0;
+    g.lse_stride_bh = L;
+    g.lse_stripe_stride = 0;
+    g.scale = scale;
+    return g;
+}
+
+int ring_bwd_prepare(const void *o_d, const float *lse_d, const void *dO_d, void *workspace, size_t ws_bytes,
+                     float *dq_acc_d, int64_t B, int64_t H, int64_t L, int64_t D, int dtype, void *stream) {
+    if (!o_d || !lse_d || !dO_d || !dq_acc_d) return STRIPED_ERR_INVALID_ARG;
+    int st = check_sizes(B, H, L, D, 1);
+    if (st) return st;
+    if (dtype == STRIPED_FP32) return STRIPED_ERR_UNSUPPORTED;
+    if (dtype != STRIPED_BF16) return STRIPED_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return STRIPED_ERR_UNSUPPORTED;
+    if (!aligned16(o_d) || !aligned16(dO_d) || !aligned16(dq_acc_d)) return STRIPED_ERR_ALIGN;
+    if (!workspace || ws_bytes < ring_bwd_workspace_size(B, H, L, D, dtype)) return STRIPED_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return STRIPED_ERR_ALIGN;
+    return launch_round_bwd_prepare(o_d, lse_d, dO_d, (float *)workspace, dq_acc_d,
+                                    round_geom(B, H, L, D, 1, STRIPED_LAYOUT_STRIPED, 1.f), (cudaStream_t)stream);
+}
+
+int ring_round_bwd(const void *q_d, const void *k_e, const void *v_e, const void *dO_d, const void *workspace,
+                   size_t ws_bytes, float *dq_acc_d, float *dk_acc_e, float *dv_acc_e, int d, int e, int64_t B,
+                   int64_t H, int64_t L, int64_t D, int N, int layout, int dtype, float scale, int first_round,
+                   int64_t *tile_stats, void *stream) {
+    if (!q_d || !k_e || !v_e || !dO_d || !dq_acc_d || !dk_acc_e || !dv_acc_e) return STRIPED_ERR_INVALID_ARG;
+    if (L < 1) return STRIPED_ERR_INVALID_ARG;
+    int st = check_attn(B, H, L * N, D, N, layout, dtype);
+    if (st) return st;
+    if (dtype == STRIPED_FP32) return STRIPED_ERR_UNSUPPORTED;
+    if (d < 0 || d >= N || e < 0 || e >= N) return STRIPED_ERR_INVALID_ARG;
+    if (!aligned16(q_d) || !aligned16(k_e) || !aligned16(v_e) || !aligned16(dO_d) || !aligned16(dq_acc_d) ||
+        !aligned16(dk_acc_e) || !aligned16(dv_acc_e))
+        return STRIPED_ERR_ALIGN;
+    if (!workspace || ws_bytes < ring_bwd_workspace_size(B, H, L, D, dtype)) return STRIPED_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return STRIPED_ERR_ALIGN;
+    return launch_tc_round_bwd(q_d, k_e, v_e, dO_d, (const float *)workspace, dq_acc_d, dk_acc_e, dv_acc_e, d, e,
+                               first_round ? 1 : 0, round_geom(B, H, L, D, N, layout, scale), tile_stats,
+                               (cudaStream_t)stream);
+}
+
+int ring_bwd_finish(const float *acc, void *out, int64_t n, int dtype, float mul, void *stream) {
+    if (!acc || !out || n < 0 || n % 8 != 0) return STRIPED_ERR_INVALID_ARG;
+    if (dtype == STRIPED_FP32) return STRIPED_ERR_UNSUPPORTED;
+    if (dtype != STRIPED_BF16) return STRIPED_ERR_INVALID_ARG;
+    if (!aligned16(acc) || !aligned16(out)) return STRIPED_ERR_ALIGN;
+    if (n == 0) return STRIPED_OK;
+    return launch_scale_to_bf16(acc, out, n / 8, mul, (cudaStream_t)stream);
+}
+
 int ring_round_fwd(const void *q_d, const void *k_e, const void *v_e, float *o_acc, float *lse_acc,
                    void *o_out, int d, int e, int64_t B, int64_t H, int64_t L, int64_t D, int N,
                    int64_t stride_bh, int64_t lse_stride_bh, int layout, int dtype, float scale,

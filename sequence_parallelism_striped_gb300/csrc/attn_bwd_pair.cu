@@ -44,7 +44,9 @@
 // issuer; 2 (first CTA) TMA of the QK, dOP and dOV streams; 3 the
 // statistics of its own CTA; 4..11 compute (thread t of warpgroup w owns key
 // row t, query columns [64w, 64w+64)).
-// MMA order per query tile i: dV_i, S_{i+1}, dQ_i, dK_i, dP_{i+1}.
+// MMA order per query tile i: dV_i, S_{i+1}, dQ_i, dK_i, dP_{i+1}.  dQ_i
+// leaves through TMA bulk reduce-adds staged in the own dS tile once dK_i
+// has read it (per warp, the 4 KB the warp itself writes).
 #include <math.h>
 
 #include "common.cuh"
@@ -79,7 +81,7 @@ struct PairBars {
     uint64_t qs_full, qs_empty, qk_full, qk_empty;      // first CTA: Q_i streams
     uint64_t dop_full, dop_empty, dov_full, dov_empty;  // first CTA: dO_i streams
     uint64_t p_ready, ds_ready, dq_free;                // first CTA: 16 compute warps of the pair
-    uint64_t s_full, dp_full, dq_full, acc_done;        // each CTA: paired-MMA completions
+    uint64_t s_full, dp_full, dq_full, dk_done, acc_done;  // each CTA: paired-MMA completions
     uint64_t st_full[2], st_empty[2];                   // each CTA: its statistics stream
     uint64_t drain;                                     // first CTA: every MMA has completed
     uint32_t tmem_slot;
@@ -116,7 +118,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     tc_bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQh,
                        const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                        const __grid_constant__ CUtensorMap tmdO, const __grid_constant__ CUtensorMap tmdOh,
-                       const PairParams p) {
+                       const __grid_constant__ CUtensorMap tmdQ, const PairParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw;
     if ((smem_u32(smem) & 1023u) != 0) {  // the same in both CTAs: both leave here
@@ -159,6 +161,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         mbar_init(bar(bars->s_full), 1);
         mbar_init(bar(bars->dp_full), 1);
         mbar_init(bar(bars->dq_full), 1);
+        mbar_init(bar(bars->dk_done), 1);
         mbar_init(bar(bars->acc_done), 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(bars->st_full[s]), 1);
@@ -337,6 +340,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                 mma_ss_pair(tdK, sdesc_sw128(sbase + kOffDS + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024),
                             sdesc_sw128(sbase + kOffQK + kk * 2048, kBox, 1024), id_kv, (i > 0 || kk > 0) ? 1u : 0u);
             mma_commit_pair(bar(bars->qk_empty));
+            mma_commit_pair_mc(bar(bars->dk_done), kBothCtas);
             if (it.d != cnt_d) {
                 flush_counts();
                 cnt_d = it.d;
@@ -414,6 +418,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                 break;
             }
             tc_fence_after();
+            // this warp's rows of the own dS tile staged dQ_{i-1} for its bulk
+            // reduction: that must have read them before they are overwritten
+            if (lane == 0) bulk_wait_group_read0();
+            __syncwarp();
             const float *sD = stat_ptr(i) + 128;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
@@ -458,7 +466,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             // ---- dQ_i: this CTA's 64 query rows (half `rank`); warp quarter q
             // reads TMEM lanes 32q..32q+31 = query rows 32(q&1)+lane of the
             // half, head-dimension block 64(q>>1); warpgroup wg takes columns
-            // [32 wg, 32 wg + 32) of the block
+            // [32 wg, 32 wg + 32) of the block.  The 32 x 32 fp32 block goes to
+            // the accumulator by a TMA bulk reduce-add (an asynchronous copy,
+            // so the cluster-scope releases above never wait for it) from the
+            // 4 KB of the own dS tile that this warp writes (free once dK_i
+            // has read it).
             if (!mbar_wait_cl(bar(bars->dq_full), i & 1, p.wc)) {
                 ok = false;
                 break;
@@ -470,15 +482,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cl(dq_free_cl);
-            const int64_t bq = bh * G + done.h;
-            const int64_t qi = (int64_t)done.a * PT + 64 * rank + (quarter & 1) * 32 + lane;
-            float *dst = p.dq_acc + (bq * g.stride_bh + (int64_t)done.d * g.stripe_stride + qi * PT +
-                                     (quarter >> 1) * 64 + wg * 32);
+            if (!mbar_wait_cl(bar(bars->dk_done), i & 1, p.wc)) {
+                ok = false;
+                break;
+            }
+            const uint32_t stage = sbase + kOffDS + wg * kBox + quarter * 32 * 128;
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-                red_add_v4(dst + 4 * v, __uint_as_float(q0[4 * v]), __uint_as_float(q0[4 * v + 1]),
-                           __uint_as_float(q0[4 * v + 2]), __uint_as_float(q0[4 * v + 3]));
+            for (int j = 0; j < 8; ++j)
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stage + lane * 128 + ((j ^ (lane & 7)) * 16)),
+                             "r"(q0[4 * j]), "r"(q0[4 * j + 1]), "r"(q0[4 * j + 2]), "r"(q0[4 * j + 3])
+                             : "memory");
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                const int bq = (int)(bh * G + done.h);
+                tma_reduce_add_4d(&tmdQ, stage, (quarter >> 1) * 64 + wg * 32,
+                                  done.a * PT + 64 * (int)rank + (quarter & 1) * 32, done.d, bq);
+                bulk_commit_group();
+            }
         }
+        if (lane == 0) bulk_wait_group0();  // every reduction has landed
         if (ok) {
             ok = mbar_wait_cl(bar(bars->acc_done), 0, p.wc);
             tc_fence_after();
@@ -546,7 +569,7 @@ int launch_tc_bwd_pair_main(const void *q, const void *k, const void *v, const v
                                                 (int)kPairSmemBytes));
     });
     if (attr != STRIPED_OK) return attr;
-    CUtensorMap mq, mqh, mk, mv, mdo, mdoh;
+    CUtensorMap mq, mqh, mk, mv, mdo, mdoh, mdq;
     const int64_t bh_kv = g.BH / g.G;
     int st;
     if ((st = make_bf16_map(&mq, q, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 128)) ||
@@ -554,7 +577,8 @@ int launch_tc_bwd_pair_main(const void *q, const void *k, const void *v, const v
         (st = make_bf16_map(&mk, k, g.D, g.L, g.N, bh_kv, g.stripe_stride, g.stride_bh, 128)) ||
         (st = make_bf16_map(&mv, v, g.D, g.L, g.N, bh_kv, g.stripe_stride, g.stride_bh, 128)) ||
         (st = make_bf16_map(&mdo, dO, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 128)) ||
-        (st = make_bf16_map(&mdoh, dO, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 64)))
+        (st = make_bf16_map(&mdoh, dO, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 64)) ||
+        (st = make_f32_map(&mdq, dq_acc, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 32)))
         return st;
     PairParams p{};
     p.g = g;
@@ -567,7 +591,7 @@ int launch_tc_bwd_pair_main(const void *q, const void *k, const void *v, const v
     const int64_t nclusters = (g.L / PT) * (g.N / 2) * bh_kv;
     if (2 * nclusters > 0x7fffffffll) return STRIPED_ERR_UNSUPPORTED;
     tc_bwd_pair_kernel<<<(unsigned)(2 * nclusters), kPairThreads, kPairSmemBytes, stream>>>(mq, mqh, mk, mv, mdo,
-                                                                                            mdoh, p);
+                                                                                            mdoh, mdq, p);
     return cuda_status(cudaGetLastError());
 }
 

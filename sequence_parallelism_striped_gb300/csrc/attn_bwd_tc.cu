@@ -73,6 +73,8 @@ struct BwdCfg {
 
 struct BwdParams {
     AttnGeom g;
+    int d_fixed, e_fixed, first;  // one ring round only: query stripe, key stripe, start the dK/dV sums
+    float *dk_acc, *dv_acc;       // one ring round only: fp32 dK, dV sums of the key block
     const float *stats;  // [BH][N][nq][LSE*log2e 128 | Delta 128], padded per 128-row tile
     float *dq_acc;       // [BH][S][D] fp32
     __nv_bfloat16 *dk, *dv;
@@ -109,10 +111,14 @@ struct QTileIter {
 };
 
 __device__ __forceinline__ void qiter_seek(QTileIter &it, int layout, int N, int G, int e, int b, int nq,
-                                           int rows_b) {
+                                           int rows_b, int dsel) {
     while (it.h < G) {
         while (it.k < N) {
             it.d = BWD_RING_ORDER ? (e + it.k) % N : it.k;
+            if (dsel >= 0 && it.d != dsel) {  // one ring round: only query stripe dsel
+                ++it.k;
+                continue;
+            }
             const QuerySpan sp = query_span(layout, it.d, e, b, nq, rows_b);
             if (sp.a_lo < nq) {
                 it.a_lo = sp.a_lo;
@@ -128,25 +134,30 @@ __device__ __forceinline__ void qiter_seek(QTileIter &it, int layout, int N, int
     }
 }
 
-__device__ __forceinline__ QTileIter qiter_begin(int layout, int N, int G, int e, int b, int nq, int rows_b) {
+__device__ __forceinline__ QTileIter qiter_begin(int layout, int N, int G, int e, int b, int nq, int rows_b,
+                                                 int dsel) {
     QTileIter it{0, 0, 0, 0, 0, 0, 0};
-    qiter_seek(it, layout, N, G, e, b, nq, rows_b);
+    qiter_seek(it, layout, N, G, e, b, nq, rows_b, dsel);
     return it;
 }
 
 __device__ __forceinline__ void qiter_next(QTileIter &it, int layout, int N, int G, int e, int b, int nq,
-                                           int rows_b) {
+                                           int rows_b, int dsel) {
     const bool end = BWD_ASCENDING ? (++it.a >= nq) : (--it.a < it.a_lo);
     if (end) {
         ++it.k;
-        qiter_seek(it, layout, N, G, e, b, nq, rows_b);
+        qiter_seek(it, layout, N, G, e, b, nq, rows_b, dsel);
     }
 }
 
 
 // kPacked: packed variable-length sequences (the sequence table is
 // consulted); the dense instantiation compiles the span as {0, nq}.
-template <int HD, bool kPacked>
+// kRound: one ring round (ring_round_bwd): the key block of stripe e_fixed
+// against the query block of stripe d_fixed, each its own [BH][L][D]
+// tensor (stripe coordinate 0 in the tensor maps), dK and dV added into
+// fp32 sums that travel with the key block.
+template <int HD, bool kPacked, bool kRound = false>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -174,11 +185,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // b) go first.  bh is the key/value head; query head bh*G + it.h.
     const int G = (int)g.G;
     const int64_t id = blockIdx.x;
-    const int64_t per_head = (int64_t)nq * N;
+    const int64_t per_head = kRound ? (int64_t)nq : (int64_t)nq * N;
     const int64_t bh = id / per_head;
     const int rem = (int)(id % per_head);
-    const int bg = rem / N;  // key tile in the slice of stripe e
-    const int e = rem % N;
+    const int bg = kRound ? rem : rem / N;  // key tile in the slice of stripe e
+    const int e = kRound ? p.e_fixed : rem % N;
+    const int dsel = kRound ? p.d_fixed : -1;  // one ring round: its query stripe only
+    const int kst = kRound ? 0 : e;            // stripe coordinate of the key block in its tensor map
     const int rows_b = tile_rows(g.L, bg);
     // packed sequences: the key tile sees the query tiles of its own sequence
     // only (tiles qbase .. qbase + nqs - 1 of every slice)
@@ -188,7 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qbase = sq.start;
 
     int nt = 0;
-    for (int d = 0; d < N; ++d) nt += nqs - query_span(g.layout, d, e, b, nqs, rows_b).a_lo;
+    for (int d = 0; d < N; ++d)
+        if (dsel < 0 || d == dsel) nt += nqs - query_span(g.layout, d, e, b, nqs, rows_b).a_lo;
     nt *= G;
 
     if (threadIdx.x == 0) {
@@ -228,15 +242,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t kb = smem_u32(&bars->kv_full);
         mbar_arrive_expect_tx(kb, 2 * kTile);
 #pragma unroll
-        for (int x = 0; x < kBoxes; ++x) tma_load_4d(sbase + kKOff + x * kBox, &tmK, kb, 64 * x, bg * BT, e, (int)bh);
+        for (int x = 0; x < kBoxes; ++x) tma_load_4d(sbase + kKOff + x * kBox, &tmK, kb, 64 * x, bg * BT, kst, (int)bh);
 #pragma unroll
-        for (int x = 0; x < kBoxes; ++x) tma_load_4d(sbase + kVOff + x * kBox, &tmV, kb, 64 * x, bg * BT, e, (int)bh);
+        for (int x = 0; x < kBoxes; ++x) tma_load_4d(sbase + kVOff + x * kBox, &tmV, kb, 64 * x, bg * BT, kst, (int)bh);
         // test hook: the first Q tile is never loaded, so every wait on it
         // runs out (the kernel must then record the timeout and return)
         const bool skip_first = p.wc.inject == kInjectBwdSkipQ;
-        QTileIter it = qiter_begin(g.layout, N, G, e, b, nqs, rows_b);
+        QTileIter it = qiter_begin(g.layout, N, G, e, b, nqs, rows_b, dsel);
         int i = 0;
-        for (; i < nt; ++i, qiter_next(it, g.layout, N, G, e, b, nqs, rows_b)) {
+        for (; i < nt; ++i, qiter_next(it, g.layout, N, G, e, b, nqs, rows_b, dsel)) {
             const int s = i % QS;
             if (i >= QS && !mbar_wait(smem_u32(&bars->q_empty[s]), ((i / QS) + 1) & 1, p.wc)) break;
             if (skip_first && i == 0) continue;
@@ -244,11 +258,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t qdst = sbase + kQOff + s * 2 * kTile;
             const int64_t bq = bh * G + it.h;  // query head
             mbar_arrive_expect_tx(fb, kTile + kStatBytes);
+            const int qst = kRound ? 0 : it.d;  // stripe coordinate of the query block
             bulk_load(sbase + kStatOff + s * kStatBytes,
-                      p.stats + (((bq * N + it.d) * (int64_t)nq + qbase + it.a) << 8), kStatBytes, fb);
+                      p.stats + (((bq * (kRound ? 1 : N) + qst) * (int64_t)nq + qbase + it.a) << 8), kStatBytes, fb);
 #pragma unroll
             for (int x = 0; x < kBoxes; ++x)
-                tma_load_4d(qdst + x * kBox, &tmQ, fb, 64 * x, (qbase + it.a) * BT, it.d, (int)bq);
+                tma_load_4d(qdst + x * kBox, &tmQ, fb, 64 * x, (qbase + it.a) * BT, qst, (int)bq);
         }
         // K, V and loads [0, i) were issued: wait (bounded) for the last of
         // each stage, so that on an error path none lands after the CTA exits
@@ -259,9 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- TMA producer: dO_i (its own stream: the buffer is
         // released later than Q_i's, after the dQ_i half staged in it is read)
         tma_prefetch_desc(&tmdO);
-        QTileIter it = qiter_begin(g.layout, N, G, e, b, nqs, rows_b);
+        QTileIter it = qiter_begin(g.layout, N, G, e, b, nqs, rows_b, dsel);
         int i = 0;
-        for (; i < nt; ++i, qiter_next(it, g.layout, N, G, e, b, nqs, rows_b)) {
+        for (; i < nt; ++i, qiter_next(it, g.layout, N, G, e, b, nqs, rows_b, dsel)) {
             const int s = i % QS;
             if (i >= QS && !mbar_wait(smem_u32(&bars->do_empty[s]), ((i / QS) + 1) & 1, p.wc)) break;
             const uint32_t fb = smem_u32(&bars->do_full[s]);
@@ -270,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(fb, kTile);
 #pragma unroll
             for (int x = 0; x < kBoxes; ++x)
-                tma_load_4d(odst + x * kBox, &tmdO, fb, 64 * x, (qbase + it.a) * BT, it.d, bq);
+                tma_load_4d(odst + x * kBox, &tmdO, fb, 64 * x, (qbase + it.a) * BT, kRound ? 0 : it.d, bq);
         }
         for (int t = i > QS ? i - QS : 0; t < i; ++t)  // in-flight loads, as above
             mbar_wait(smem_u32(&bars->do_full[t % QS]), (t / QS) & 1, p.wc);
@@ -312,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         // tiles whose five MMAs were issued, per query stripe: added to the
         // (round, device) counter when the stripe changes
-        QTileIter it = qiter_begin(g.layout, N, G, e, b, nqs, rows_b);
+        QTileIter it = qiter_begin(g.layout, N, G, e, b, nqs, rows_b, dsel);
         int cnt_d = -1, n_full = 0, n_part = 0;
         auto flush_counts = [&]() {
             if (p.tile_stats && cnt_d >= 0 && (n_full | n_part)) {
@@ -324,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         bool ok = mbar_wait(smem_u32(&bars->kv_full), 0, p.wc) && issue_s(0);
         if (ok) ok = issue_dp(0);
-        for (int i = 0; i < nt && ok; ++i, qiter_next(it, g.layout, N, G, e, b, nqs, rows_b)) {
+        for (int i = 0; i < nt && ok; ++i, qiter_next(it, g.layout, N, G, e, b, nqs, rows_b, dsel)) {
             const int s = i % QS;
             const uint32_t qaddr = sbase + kQOff + s * 2 * kTile;
             const uint32_t oaddr = qaddr + kTile;
@@ -427,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             return true;
         };
 
-        QTileIter cur = qiter_begin(g.layout, N, G, e, b, nqs, rows_b);
+        QTileIter cur = qiter_begin(g.layout, N, G, e, b, nqs, rows_b, dsel);
         // warpgroup 1, lane 0: stage whose dQ bulk reduce still reads shared
         // memory (-1: none); the wait for it is deferred to the next tile
         int pending = -1;
@@ -478,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- P of the next tile while the tensor core runs dQ_i / dK_i
             const QTileIter done = cur;
             if (i + 1 < nt) {
-                qiter_next(cur, g.layout, N, G, e, b, nqs, rows_b);
+                qiter_next(cur, g.layout, N, G, e, b, nqs, rows_b, dsel);
                 if (!compute_p(cur, i + 1)) {
                     ok = false;
                     break;
@@ -541,8 +556,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) {
                         const uint32_t wofs = (uint32_t)quarter * 32 * 128;
                         const int r0 = (qbase + done.a) * BT + quarter * 32;
-                        tma_reduce_add_4d(&tmdQ, stage + wofs, cbase, r0, done.d, (int)bq);
-                        tma_reduce_add_4d(&tmdQ, stage + kBox + wofs, cbase + 32, r0, done.d, (int)bq);
+                        tma_reduce_add_4d(&tmdQ, stage + wofs, cbase, r0, kRound ? 0 : done.d, (int)bq);
+                        tma_reduce_add_4d(&tmdQ, stage + kBox + wofs, cbase + 32, r0, kRound ? 0 : done.d, (int)bq);
                         bulk_commit_group();
                         pending = s;
                     }
@@ -579,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) {
                         const uint32_t wofs = (uint32_t)quarter * 32 * 128;
                         const int r0 = (qbase + done.a) * BT + quarter * 32;
-                        tma_reduce_add_4d(&tmdQ, stage + wofs, dbase, r0, done.d, (int)bq);
+                        tma_reduce_add_4d(&tmdQ, stage + wofs, dbase, r0, kRound ? 0 : done.d, (int)bq);
                         bulk_commit_group();
                         pending = s;
                     }
@@ -610,7 +625,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int u = 0; u < 32; ++u) rr[u] = 0u;
                 }
-                if (kj < g.L) {
+                if (kRound && kj < g.L) {
+                    // one ring round: add into (or, first, start) the block's fp32 sums
+                    float *acc = (which ? p.dk_acc : p.dv_acc) + krow + c * 32;
+#pragma unroll
+                    for (int u = 0; u < 32; u += 4) {
+                        float4 a4 = p.first ? make_float4(0.f, 0.f, 0.f, 0.f) : *reinterpret_cast<float4 *>(acc + u);
+                        a4.x += __uint_as_float(rr[u]) * mul;
+                        a4.y += __uint_as_float(rr[u + 1]) * mul;
+                        a4.z += __uint_as_float(rr[u + 2]) * mul;
+                        a4.w += __uint_as_float(rr[u + 3]) * mul;
+                        *reinterpret_cast<float4 *>(acc + u) = a4;
+                    }
+                } else if (kj < g.L) {
                     uint4 *dst = reinterpret_cast<uint4 *>(outp + krow + c * 32);
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
@@ -731,6 +758,9 @@ int launch_bwd_hd(const void *q, const void *k, const void *v, const void *o, co
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(tc_bwd_kernel<HD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(tc_bwd_kernel<HD, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemBytes);
         return cuda_status(e);
     });
     if (attr != STRIPED_OK) return attr;
@@ -778,7 +808,78 @@ int launch_bwd_hd(const void *q, const void *k, const void *v, const void *o, co
     return cuda_status(cudaGetLastError());
 }
 
+template <int HD>
+int launch_round_bwd_hd(const void *q_d, const void *k_e, const void *v_e, const void *dO_d, const float *stats,
+                        float *dq_acc, float *dk_acc, float *dv_acc, int d, int e, int first, const AttnGeom &g,
+                        int64_t *tile_stats, cudaStream_t stream) {
+    constexpr size_t kSmemBytes = BwdCfg<HD>::kSmemBytes;
+    static PerDeviceOnce attr_once;
+    const int attr = attr_once.get([] {
+        return cuda_status(cudaFuncSetAttribute(tc_bwd_kernel<HD, false, true>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes));
+    });
+    if (attr != STRIPED_OK) return attr;
+    // every block is its own [BH][L][D] tensor: a stripe dimension of extent 1
+    const int64_t ld = g.L * g.D;
+    CUtensorMap mq, mk, mv, mdo, mdq;
+    int st;
+    if ((st = make_bf16_map(&mq, q_d, g.D, g.L, 1, g.BH, ld, ld, 128)) ||
+        (st = make_bf16_map(&mk, k_e, g.D, g.L, 1, g.BH, ld, ld, 128)) ||
+        (st = make_bf16_map(&mv, v_e, g.D, g.L, 1, g.BH, ld, ld, 128)) ||
+        (st = make_bf16_map(&mdo, dO_d, g.D, g.L, 1, g.BH, ld, ld, 128)) ||
+        (st = make_f32_map(&mdq, dq_acc, g.D, g.L, 1, g.BH, ld, ld, 32)))
+        return st;
+    BwdParams p{};
+    p.g = g;
+    p.g.G = 1;
+    p.g.stride_bh = ld;
+    p.g.stripe_stride = 0;
+    p.d_fixed = d;
+    p.e_fixed = e;
+    p.first = first;
+    p.dk_acc = dk_acc;
+    p.dv_acc = dv_acc;
+    p.stats = stats;
+    p.dq_acc = dq_acc;
+    p.tile_stats = tile_stats;
+    p.wc = device_wait_ctl();
+    const int64_t nq = (g.L + BT - 1) / BT;
+    const int64_t nblocks = nq * g.BH;
+    if (nblocks > 0x7fffffffll) return STRIPED_ERR_UNSUPPORTED;
+    tc_bwd_kernel<HD, false, true><<<(unsigned)nblocks, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, p);
+    return cuda_status(cudaGetLastError());
+}
+
 }  // namespace
+
+int launch_round_bwd_prepare(const void *o_d, const float *lse_d, const void *dO_d, float *stats, float *dq_acc,
+                             const AttnGeom &g, cudaStream_t stream) {
+    const int nq = (int)((g.L + BT - 1) / BT);
+    const int sms = device_sm_count();
+    const int64_t padded = g.BH * (int64_t)nq * BT;
+    if (g.D == 64)
+        bwd_pre_kernel<64><<<sms * 8, 256, 0, stream>>>((const __nv_bfloat16 *)o_d, (const __nv_bfloat16 *)dO_d,
+                                                        lse_d, stats, dq_acc, g.L, nq, padded);
+    else
+        bwd_pre_kernel<128><<<sms * 8, 256, 0, stream>>>((const __nv_bfloat16 *)o_d, (const __nv_bfloat16 *)dO_d,
+                                                         lse_d, stats, dq_acc, g.L, nq, padded);
+    return cuda_status(cudaGetLastError());
+}
+
+int launch_tc_round_bwd(const void *q_d, const void *k_e, const void *v_e, const void *dO_d, const float *stats,
+                        float *dq_acc, float *dk_acc, float *dv_acc, int d, int e, int first, const AttnGeom &g,
+                        int64_t *tile_stats, cudaStream_t stream) {
+    if (g.D == 64)
+        return launch_round_bwd_hd<64>(q_d, k_e, v_e, dO_d, stats, dq_acc, dk_acc, dv_acc, d, e, first, g, tile_stats,
+                                       stream);
+    return launch_round_bwd_hd<128>(q_d, k_e, v_e, dO_d, stats, dq_acc, dk_acc, dv_acc, d, e, first, g, tile_stats,
+                                    stream);
+}
+
+int launch_scale_to_bf16(const float *acc, void *out, int64_t n8, float mul, cudaStream_t stream) {
+    bwd_post_kernel<<<device_sm_count() * 8, 256, 0, stream>>>(acc, (__nv_bfloat16 *)out, n8, mul);
+    return cuda_status(cudaGetLastError());
+}
 
 int launch_tc_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
                   const void *dO, void *dq, void *dk, void *dv, float *dq_acc, float *stats,

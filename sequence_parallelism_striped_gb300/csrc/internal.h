@@ -119,6 +119,18 @@ int launch_tc_bwd(const void *q, const void *k, const void *v, const void *o, co
                   const void *dO, void *dq, void *dk, void *dv, float *dq_acc, float *stats,
                   const AttnGeom &g, int64_t *tile_stats, cudaStream_t stream);
 
+// One ring round of the backward (every block its own contiguous
+// [BH][L][D] tensor): the statistics of device d's query block and its
+// zeroed fp32 dQ sum; the round itself (dQ added into dq_acc, dK and dV
+// added into -- or with first, written to -- the fp32 sums of key block
+// e); and the final out = bf16(mul * sum) of n8 * 8 values.
+int launch_round_bwd_prepare(const void *o_d, const float *lse_d, const void *dO_d, float *stats, float *dq_acc,
+                             const AttnGeom &g, cudaStream_t stream);
+int launch_tc_round_bwd(const void *q_d, const void *k_e, const void *v_e, const void *dO_d, const float *stats,
+                        float *dq_acc, float *dk_acc, float *dv_acc, int d, int e, int first, const AttnGeom &g,
+                        int64_t *tile_stats, cudaStream_t stream);
+int launch_scale_to_bf16(const float *acc, void *out, int64_t n8, float mul, cudaStream_t stream);
+
 // attn_bwd_pair.cu: the main backward kernel on CTA pairs (striped
 // placement, D = 128, whole 128-row tiles, N even, dense batch); the
 // statistics/accumulator pass before it and the dQ pass after it are the
