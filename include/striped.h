@@ -322,15 +322,6 @@ int striped_kernel_tile(int dtype, int64_t D, int *Tq, int *Tk);
 int striped_fwd_query_tiles_per_cta(int64_t B, int64_t H, int64_t S, int64_t D, int N, int layout, int dtype,
                                     int num_sms);
 
-/* Host-only: how many key tiles one cluster of striped_attn_bwd /
- * striped_attn_bwd_gqa holds: 2 when key tile b of stripes e and e + 1
- * (e even) go to one pair of CTAs that contract dQ over both on the paired
- * tensor core (bf16, D = 128, striped placement, L = S/N a whole number of
- * 128-row tiles, N even), else 1.  Both schedules compute dK, dV and dQ to
- * the same tolerance.  Returns 1 or 2, or STRIPED_ERR_INVALID_ARG /
- * STRIPED_ERR_UNSUPPORTED for arguments the backward rejects. */
-int striped_bwd_key_tiles_per_cluster(int64_t B, int64_t H, int64_t S, int64_t D, int N, int layout, int dtype);
-
 /*
  * Host-only, exact: per-(b,h) processed-tile table of the ring (§Summary
  * and §Key points "Imbalance": per-round work per device).  full and

@@ -88,7 +88,6 @@ def load(build_if_missing: bool = True):
                                                 F, P, P]
         lib.striped_kernel_tile.argtypes = [I, I64, P, P]
         lib.striped_fwd_query_tiles_per_cta.argtypes = [I64, I64, I64, I64, I, I, I, I]
-        lib.striped_bwd_key_tiles_per_cluster.argtypes = [I64, I64, I64, I64, I, I, I]
         lib.striped_tile_counts.argtypes = [I64, I, I, I, I, P, P]
         lib.striped_critical_path.argtypes = [I64, I, I, I, I]
         lib.striped_critical_path.restype = I64
@@ -191,16 +190,6 @@ def fwd_query_tiles_per_cta(B: int, H: int, S: int, D: int, N: int, layout: int 
     r = load().striped_fwd_query_tiles_per_cta(B, H, S, D, N, layout, code, num_sms)
     if r < 0:
         raise StripedError(r, "striped_fwd_query_tiles_per_cta")
-    return r
-
-
-def bwd_key_tiles_per_cluster(B: int, H: int, S: int, D: int, N: int, layout: int = STRIPED,
-                              dtype: torch.dtype = torch.bfloat16) -> int:
-    """Key tiles one backward cluster holds (1, or 2 for the CTA-pair kernel)."""
-    code = BF16 if dtype == torch.bfloat16 else FP32
-    r = load().striped_bwd_key_tiles_per_cluster(B, H, S, D, N, layout, code)
-    if r < 0:
-        raise StripedError(r, "striped_bwd_key_tiles_per_cluster")
     return r
 
 

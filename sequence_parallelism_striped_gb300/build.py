@@ -18,8 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libstriped.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "permute.cu", "attn_simt.cu", "attn_fwd_tc.cu", "attn_fwd_pair.cu", "attn_bwd_tc.cu", "attn_bwd_pair.cu",
-           "attn_bwd_noalloc.cu",
+SOURCES = ["api.cu", "permute.cu", "attn_simt.cu", "attn_fwd_tc.cu", "attn_fwd_pair.cu", "attn_bwd_tc.cu", "attn_bwd_noalloc.cu",
            "host_model.cpp"]
 
 

@@ -253,13 +253,6 @@ int striped_fwd_query_tiles_per_cta(int64_t B, int64_t H, int64_t S, int64_t D, 
     return fwd_pair_eligible(full_geom(B, H, H, S, D, N, layout, 1.0f), num_sms) ? 2 : 1;
 }
 
-int striped_bwd_key_tiles_per_cluster(int64_t B, int64_t H, int64_t S, int64_t D, int N, int layout, int dtype) {
-    const int st = check_attn(B, H, S, D, N, layout, dtype);
-    if (st) return st;
-    if (dtype != STRIPED_BF16) return 1;
-    return bwd_pair_eligible(full_geom(B, H, H, S, D, N, layout, 1.0f)) ? 2 : 1;
-}
-
 // ---------------------------------------------------------------- permutation
 // Packed sequences: check the HOST array cu_seqlens[0..nseq] (starts at 0,
 // every length a positive multiple of N * unit rows) and build the table

@@ -424,14 +424,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_wait(rr);
                 uint32_t pk[16];
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const int c0 = c * 32 + 2 * u;
-                    const float p0 = ex2(fmaf(__uint_as_float(rr[2 * u]), cl2, -sL[c0]));
-                    const float p1 = ex2(fmaf(__uint_as_float(rr[2 * u + 1]), cl2, -sL[c0 + 1]));
-                    const bool k0 = key_valid && (cbase + c0 >= cmin);
-                    const bool k1 = key_valid && (cbase + c0 + 1 >= cmin);
-                    pk[u] = pack_bf16x2(k0 ? p0 : 0.f, k1 ? p1 : 0.f);
-                    pkP[c * 16 + u] = pk[u];
+                for (int u = 0; u < 16; u += 2) {
+                    // four row statistics per 16-byte shared-memory load
+                    const float4 l4 = *reinterpret_cast<const float4 *>(sL + c * 32 + 2 * u);
+                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int c0 = c * 32 + 2 * (u + h);
+                        const float p0 = ex2(fmaf(__uint_as_float(rr[2 * (u + h)]), cl2, -lv[2 * h]));
+                        const float p1 = ex2(fmaf(__uint_as_float(rr[2 * (u + h) + 1]), cl2, -lv[2 * h + 1]));
+                        const bool k0 = key_valid && (cbase + c0 >= cmin);
+                        const bool k1 = key_valid && (cbase + c0 + 1 >= cmin);
+                        pk[u + h] = pack_bf16x2(k0 ? p0 : 0.f, k1 ? p1 : 0.f);
+                        pkP[c * 16 + u + h] = pk[u + h];
+                    }
                 }
                 tmem_st16(tS + lane_off + pbase + c * 16, pk);
             }
@@ -470,14 +476,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
                     uint32_t w[4];
+                    // the chunk's eight Delta values in two 16-byte loads
+                    const float4 d0 = *reinterpret_cast<const float4 *>(sD + c * 32 + 8 * v);
+                    const float4 d1 = *reinterpret_cast<const float4 *>(sD + c * 32 + 8 * v + 4);
+                    const float dv8[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
                         const int u = v * 4 + h;  // pair index within the chunk
-                        const int c0 = c * 32 + 2 * u;
                         __nv_bfloat162 pv = *reinterpret_cast<__nv_bfloat162 *>(&pkP[c * 16 + u]);
                         const float2 pf = __bfloat1622float2(pv);
-                        w[h] = pack_bf16x2(pf.x * (__uint_as_float(rr[2 * u]) - sD[c0]),
-                                           pf.y * (__uint_as_float(rr[2 * u + 1]) - sD[c0 + 1]));
+                        w[h] = pack_bf16x2(pf.x * (__uint_as_float(rr[2 * u]) - dv8[2 * h]),
+                                           pf.y * (__uint_as_float(rr[2 * u + 1]) - dv8[2 * h + 1]));
                     }
                     const int chunk = c * 4 + v;
                     *reinterpret_cast<uint4 *>(sDS + ((chunk ^ (row & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -771,13 +780,6 @@ int launch_bwd_hd(const void *q, const void *k, const void *v, const void *o, co
                                                     stats, dq_acc, g.L, nq, g.BH * g.N * (int64_t)nq * BT);
     int st = cuda_status(cudaGetLastError());
     if (st != STRIPED_OK) return st;
-    if (HD == 128 && bwd_pair_eligible(g)) {
-        // striped, whole tiles, even N: two key tiles per CTA pair
-        st = launch_tc_bwd_pair_main(q, k, v, dO, dq_acc, stats, dk, dv, g, tile_stats, stream);
-        if (st != STRIPED_OK) return st;
-        bwd_post_kernel<<<sms * 8, 256, 0, stream>>>(dq_acc, (__nv_bfloat16 *)dq, rows * HD / 8, g.scale);
-        return cuda_status(cudaGetLastError());
-    }
     CUtensorMap mq, mk, mv, mdo;
     const int64_t bh_kv = g.BH / g.G;
     if ((st = make_bf16_map(&mq, q, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 128)) ||

@@ -479,130 +479,4 @@ __device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float 
                  : "memory");
 }
 
-// --------------------------------------------------------------------------
-// CTA pairs (a cluster of two CTAs sharing one tcgen05 cta_group::2 MMA)
-// --------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// Address of the same shared-memory offset in CTA `rank` of the cluster
-// (a shared::cluster address).
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
-
-// All threads of both CTAs meet here (release / acquire at cluster scope).
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait on a barrier of this CTA whose arrivals may come from the
-// other CTA of the pair (acquire at cluster scope).
-__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, const WaitCtl &w) {
-    for (int it = 0; it < 64; ++it)
-        if (mbar_try_wait_cl(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 0;; ++it) {
-        if (mbar_try_wait_cl(bar, parity)) return true;
-        if ((it & 255u) == 255u && global_timer_ns() - t0 > w.limit_ns) break;
-    }
-    record_timeout(w);
-    return false;
-}
-
-// Arrive on a barrier given by its shared::cluster address (either CTA).
-__device__ __forceinline__ void mbar_arrive_cl(uint32_t bar_cl) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cl) : "memory");
-}
-
-// TMA tile load into the shared memory of either CTA of the pair (dst_cl a
-// shared::cluster address), completing on a barrier of either CTA (bar_cl).
-__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst_cl, const CUtensorMap *m, uint32_t bar_cl, int c0,
-                                                 int c1, int c2, int c3) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
-        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst_cl),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar_cl)
-        : "memory");
-}
-
-// 16 bytes to the shared memory of either CTA (shared::cluster address).
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr_cl, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr_cl), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
-}
-
-// Generic-proxy writes to shared memory of the cluster become visible to
-// the tensor core (async proxy).
-__device__ __forceinline__ void fence_proxy_async_cluster() {
-    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-}
-
-// Tensor memory of a CTA pair: one warp of EACH CTA executes these together;
-// both CTAs get the same columns.
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish_pair() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-// Paired MMA issued by one thread of the pair's first CTA: CTA r supplies
-// rows [r*M/2, (r+1)*M/2) of A and columns [r*N/2, (r+1)*N/2) of B (at the
-// same shared-memory offsets in both CTAs) and holds its M/2 rows of D in
-// its own tensor memory.
-__device__ __forceinline__ void mma_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void mma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// Arrive on a barrier of the issuing CTA once every paired MMA issued so far
-// by this thread has completed.
-__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-// The same, arriving on the barrier at this offset in every CTA of `mask`.
-__device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            bar),
-        "h"(mask)
-        : "memory");
-}
-
 }  // namespace striped

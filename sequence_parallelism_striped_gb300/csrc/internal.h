@@ -131,15 +131,6 @@ int launch_tc_round_bwd(const void *q_d, const void *k_e, const void *v_e, const
                         int64_t *tile_stats, cudaStream_t stream);
 int launch_scale_to_bf16(const float *acc, void *out, int64_t n8, float mul, cudaStream_t stream);
 
-// attn_bwd_pair.cu: the main backward kernel on CTA pairs (striped
-// placement, D = 128, whole 128-row tiles, N even, dense batch); the
-// statistics/accumulator pass before it and the dQ pass after it are the
-// one-CTA backward's.  STRIPED_ERR_UNSUPPORTED unless bwd_pair_eligible(g).
-bool bwd_pair_eligible(const AttnGeom &g);
-int launch_tc_bwd_pair_main(const void *q, const void *k, const void *v, const void *dO, float *dq_acc,
-                            const float *stats, void *dk, void *dv, const AttnGeom &g, int64_t *tile_stats,
-                            cudaStream_t stream);
-
 // bf16 tensor viewed as [BH][N][L][D] -> 4-D tensor map with boxes of
 // 64 elements x box_rows rows, 128-byte swizzle, zero fill out of range.
 // Returns a status code.

@@ -252,23 +252,3 @@ def test_test_hook_rejects_unknown_faults(lib):
     assert lib.striped_test_inject(-1, 1000) == -1
     assert "striped_test_inject" in _declared_functions()
 
-
-def test_backward_schedule_rule(lib):
-    """The CTA-pair backward serves bf16, D = 128, striped, whole 128-row
-    tiles per stripe and an even number of stripes; everything else keeps
-    one key tile per CTA."""
-    f = sp.bwd_key_tiles_per_cluster
-    assert f(1, 32, 262144, 128, 8) == 2
-    assert f(1, 8, 8192, 128, 8) == 2
-    assert f(1, 16, 786432, 128, 16) == 2
-    assert f(1, 2, 2048, 128, 4) == 2
-    assert f(1, 2, 2048, 128, 4, sp.CONTIGUOUS) == 1
-    assert f(1, 2, 2048, 128, 4, sp.ZIGZAG) == 1
-    assert f(1, 2, 1200, 128, 4) == 1      # ragged stripes (L = 300)
-    assert f(1, 2, 3 * 1024, 128, 3) == 1  # odd N
-    assert f(1, 2, 2048, 64, 4) == 1       # head dimension 64
-    import torch
-
-    assert f(1, 1, 256, 64, 4, sp.STRIPED, torch.float32) == 1
-    with pytest.raises(sp.StripedError):
-        f(1, 1, 1000, 128, 3)
