@@ -245,9 +245,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
                 for (int t = 0; t < 8; ++t) mx8[t] = sv[t];
 #pragma unroll
-                for (int c = 8; c < PB; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sv[c]);
-                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                for (int c = 8; c < PB; c += 16)
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) mx8[t] = fmax3(mx8[t], sv[c + t], sv[c + 8 + t]);
+                const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                       fmaxf(mx8[6], mx8[7]));
                 const float m_tile = mx * cl2;
                 const bool move = (j == 0) ? true : (m_tile > m_ref + kPRescale);
                 const float m_new = move ? fmaxf(m_ref, m_tile) : m_ref;
@@ -255,21 +257,25 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
                 // P in two halves of 64 columns, each stored as soon as it is
                 // packed (ten warps leave 168 registers a thread)
-                float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                // the same arithmetic, in the same order, as the one-tile
+                // kernel (paired FMA for the exponent arguments, four paired
+                // row-sum accumulators), so both give identical results
+                const uint64_t cl2x2 = f2(cl2, cl2), nm2 = f2(-m_use, -m_use);
+                uint64_t acc4[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t pk[32];
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
-                        const float p0 = ex2(fmaf(sv[64 * h + 2 * c], cl2, -m_use));
-                        const float p1 = ex2(fmaf(sv[64 * h + 2 * c + 1], cl2, -m_use));
-                        sum8[c & 7] += p0 + p1;
+                        const float2 x = f2_split(fma2(f2(sv[64 * h + 2 * c], sv[64 * h + 2 * c + 1]), cl2x2, nm2));
+                        const float p0 = ex2(x.x), p1 = ex2(x.y);
+                        acc4[c & 3] = add2(acc4[c & 3], f2(p0, p1));
                         pk[c] = pack_bf16x2(p0, p1);
                     }
                     tmem_st32(tS + 32 * h, pk);
                 }
-                const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                                  ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+                const float2 s01 = f2_split(add2(acc4[0], acc4[1])), s23 = f2_split(add2(acc4[2], acc4[3]));
+                const float sum = (s01.x + s01.y) + (s23.x + s23.y);
                 tmem_st_wait();
                 l = l * alpha + sum;
                 m_ref = m_new;

@@ -313,32 +313,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < BN; ++c)
                         if (c > lim) sv[c] = -INFINITY;
                 }
-                // row max as 8 independent chains (a single chain of 128
-                // dependent max operations would be pure latency)
+                // row max as 8 independent chains of three-input max (a
+                // single chain of 128 dependent max operations would be pure
+                // latency)
                 float mx8[8];
 #pragma unroll
                 for (int t = 0; t < 8; ++t) mx8[t] = sv[t];
 #pragma unroll
-                for (int c = 8; c < BN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sv[c]);
-                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                for (int c = 8; c < BN; c += 16)
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) mx8[t] = fmax3(mx8[t], sv[c + t], sv[c + 8 + t]);
+                const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                       fmaxf(mx8[6], mx8[7]));
                 const float m_tile = mx * cl2;
                 // lazy rescale: move the reference only when the max grows a lot
                 bool move = (j == 0) ? true : (m_tile > m_ref + kRescaleThreshold);
                 const float m_new = move ? fmaxf(m_ref, m_tile) : m_ref;
                 const float alpha = (j == 0 || !move) ? 1.f : ex2(m_ref - m_new);
                 const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-                float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                // exponent arguments two at a time (paired fp32 FMA), the row
+                // sum in four paired accumulators
+                const uint64_t cl2x2 = f2(cl2, cl2), nm2 = f2(-m_use, -m_use);
+                uint64_t acc4[4] = {0ull, 0ull, 0ull, 0ull};
                 uint32_t pk[BN / 2];
 #pragma unroll
                 for (int c = 0; c < BN / 2; ++c) {
-                    const float p0 = ex2(fmaf(sv[2 * c], cl2, -m_use));
-                    const float p1 = ex2(fmaf(sv[2 * c + 1], cl2, -m_use));
-                    sum8[c & 7] += p0 + p1;
+                    const float2 x = f2_split(fma2(f2(sv[2 * c], sv[2 * c + 1]), cl2x2, nm2));
+                    const float p0 = ex2(x.x), p1 = ex2(x.y);
+                    acc4[c & 3] = add2(acc4[c & 3], f2(p0, p1));
                     pk[c] = pack_bf16x2(p0, p1);
                 }
-                const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                                  ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+                const float2 s01 = f2_split(add2(acc4[0], acc4[1])), s23 = f2_split(add2(acc4[2], acc4[3]));
+                const float sum = (s01.x + s01.y) + (s23.x + s23.y);
                 {
                     uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
                     uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
