@@ -479,14 +479,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // the chunk's eight Delta values in two 16-byte loads
                     const float4 d0 = *reinterpret_cast<const float4 *>(sD + c * 32 + 8 * v);
                     const float4 d1 = *reinterpret_cast<const float4 *>(sD + c * 32 + 8 * v + 4);
-                    const float dv8[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+                    const uint64_t dd[4] = {f2(d0.x, d0.y), f2(d0.z, d0.w), f2(d1.x, d1.y), f2(d1.z, d1.w)};
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
                         const int u = v * 4 + h;  // pair index within the chunk
                         __nv_bfloat162 pv = *reinterpret_cast<__nv_bfloat162 *>(&pkP[c * 16 + u]);
                         const float2 pf = __bfloat1622float2(pv);
-                        w[h] = pack_bf16x2(pf.x * (__uint_as_float(rr[2 * u]) - dv8[2 * h]),
-                                           pf.y * (__uint_as_float(rr[2 * u + 1]) - dv8[2 * h + 1]));
+                        // dS = P * (dP - Delta), two at a time
+                        const float2 ds = f2_split(mul2(f2(pf.x, pf.y), sub2(f2(__uint_as_float(rr[2 * u]),
+                                                                                  __uint_as_float(rr[2 * u + 1])), dd[h])));
+                        w[h] = pack_bf16x2(ds.x, ds.y);
                     }
                     const int chunk = c * 4 + v;
                     *reinterpret_cast<uint4 *>(sDS + ((chunk ^ (row & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
