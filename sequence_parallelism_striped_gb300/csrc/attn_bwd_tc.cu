@@ -28,18 +28,19 @@
 //                S^T  = K Q_i^T      SS, both K-major
 //                dP^T = V dO_i^T     SS, both K-major
 //                dV  += P^T dO_i     TS, A = P^T in TMEM, B = dO_i MN-major
-//                dQ_i = dS K         SS, A = dS smem tile read MN-major
-//                dK  += dS^T Q_i     SS, A = the same smem tile read K-major
+//                dK  += dS^T Q_i     SS, A = dS smem tile read K-major
+//                dQ_i = dS K         SS, A = the same smem tile read MN-major
 //              The dS tile ([key][query], 128-byte swizzle) is a valid
 //              operand both ways, so dS^T never goes through TMEM.  Issue
-//              order dV_i, S_{i+1}, dQ_i, dK_i, dP_{i+1} keeps the tensor core
+//              order dV_i, S_{i+1}, dK_i, dQ_i, dP_{i+1} keeps the tensor core
 //              busy while the compute warps form dS_i, P_{i+1} and read dQ_i
-//              out.  dQ_i goes to the fp32 accumulator half by vector
-//              reductions (warpgroup 0) and half by TMA bulk reduce-add from
-//              the dO_i buffer, dead by then (warpgroup 1; the wait for the
-//              reduce to read the buffer is deferred by one tile); Q_i is
-//              released as soon as dK_i completes so the next Q tile loads
-//              early.
+//              out; dK_i goes before dQ_i so that Q_i, whose last reader it
+//              is, returns to the producer one MMA earlier and the next Q
+//              tile loads early.  dQ_i goes to the fp32 accumulator half by
+//              vector reductions (warpgroup 0) and half by TMA bulk
+//              reduce-add from the dO_i buffer, dead by then (warpgroup 1;
+//              the wait for the reduce to read the buffer is deferred by one
+//              tile).
 //   bwd_post   dQ = bf16(scale * accumulator)
 #include <math.h>
 
@@ -292,9 +293,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1 && lane == 0 && nt > 0) {
         // ---------------- MMA issuer
         // Per query tile i (TMEM: S = S^T then P^T; DP = dP^T then dQ_i):
-        //   dV += P^T dO | S(i+1) | dQ_i = dS K | dK += dS^T Q | dP(i+1)
-        // so S(i+1) runs while the compute warps form dS_i, dK_i runs while
-        // they read dQ_i out, and dP(i+1) follows as soon as dQ_i is out.
+        //   dV += P^T dO | S(i+1) | dK += dS^T Q | dQ_i = dS K | dP(i+1)
+        // so S(i+1) runs while the compute warps form dS_i and P(i+1), Q_i
+        // is released at dK_i, and dP(i+1) follows as soon as dQ_i is out.
         constexpr uint32_t id_kk = idesc_bf16_f32(BT, BT, false, false);
         constexpr uint32_t id_kmn = idesc_bf16_f32(BT, HD, false, true);
         constexpr uint32_t id_mnmn = idesc_bf16_f32(BT, HD, true, true);
@@ -352,21 +353,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_ts(tdV, tS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
                        sdesc_sw128(oaddr + kk * 2048, kBox, 1024), id_kmn, (i > 0 || kk > 0) ? 1u : 0u);
             if (i + 1 < nt && !issue_s(i + 1)) break;
-            // dQ_i = dS K (A = dS, MN-major view of the smem tile) -> DP columns
+            // dK += dS^T Q (A = dS^T, K-major view of the dS smem tile)
             if (!mbar_wait(smem_u32(&bars->ds_ready), i & 1, p.wc)) break;
             tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < BT / 16; ++kk)
-                mma_ss(tdP, sdesc_sw128(sbase + kDSOff + kk * 2048, kBox, 1024),
-                       sdesc_sw128(sbase + kKOff + kk * 2048, kBox, 1024), id_mnmn, kk > 0 ? 1u : 0u);
-            mma_commit(smem_u32(&bars->dq_full));
-            // dK += dS^T Q (A = dS^T, K-major view of the same smem tile)
 #pragma unroll
             for (int kk = 0; kk < BT / 16; ++kk)
                 mma_ss(tdK, sdesc_sw128(sbase + kDSOff + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024),
                        sdesc_sw128(qaddr + kk * 2048, kBox, 1024), id_kmn, (i > 0 || kk > 0) ? 1u : 0u);
             // Q_i (and its statistics) are free once dK_i completes
             if (i + QS < nt) mma_commit(smem_u32(&bars->q_empty[s]));
+            // dQ_i = dS K (A = dS, MN-major view of the same tile) -> DP columns
+#pragma unroll
+            for (int kk = 0; kk < BT / 16; ++kk)
+                mma_ss(tdP, sdesc_sw128(sbase + kDSOff + kk * 2048, kBox, 1024),
+                       sdesc_sw128(sbase + kKOff + kk * 2048, kBox, 1024), id_mnmn, kk > 0 ? 1u : 0u);
+            mma_commit(smem_u32(&bars->dq_full));
             if (it.d != cnt_d) {
                 flush_counts();
                 cnt_d = it.d;
