@@ -483,53 +483,12 @@ def run_gpu(args, rank, world, local_rank):
     stats_np = stats.cpu().numpy() // args.steps  # counters of one step, all heads
     T = sp.kernel_tile(torch.bfloat16, D)
 
-    # the other placements on the same inputs, for comparison: contiguous
-    # (Ring Attention) and zig-zag (load-balanced), 2 timed steps each
-    contig = zigzag = None
-    if args.compare:
-        def layout_steps(layout, nc=2):
-            step(layout=layout)
-            torch.cuda.synchronize()
-            c0 = torch.cuda.Event(enable_timing=True)
-            c1 = torch.cuda.Event(enable_timing=True)
-            c0.record()
-            for _ in range(nc):
-                step(layout=layout)
-            c1.record()
-            torch.cuda.synchronize()
-            cms = c0.elapsed_time(c1) / nc
-            return {"ms_per_step": cms, "tflops": fl_step / (cms / 1000.0) / 1e12}
-
-        contig = layout_steps(sp.CONTIGUOUS)
-        zigzag = layout_steps(sp.ZIGZAG)
-
-    # per-round variant: N x N ring_round_fwd launches (one per device and
-    # ring round, merged into an fp32 (O, LSE) accumulator) against the
-    # batched forward of the same layout
-    per_round = None
-    if args.compare:
-        per_round = {}
-        o_acc = torch.empty(B, H, S, D, dtype=torch.float32, device=dev)
-        lse_acc = torch.empty(B, H, S, dtype=torch.float32, device=dev)
-        for lname, layout in (("striped", sp.STRIPED), ("zigzag", sp.ZIGZAG), ("contiguous", sp.CONTIGUOUS)):
-            if layout == sp.STRIPED:
-                q_, k_, v_ = (sp.striped_permute(x[n_], N, out=buf) for n_, buf in (("q", qs), ("k", ks), ("v", vs)))
-            elif layout == sp.ZIGZAG:
-                q_, k_, v_ = (sp.layout_permute(x[n_], N, layout, out=buf) for n_, buf in (("q", qs), ("k", ks),
-                                                                                        ("v", vs)))
-            else:
-                q_, k_, v_ = x["q"], x["k"], x["v"]
-            per_round[lname] = _time_rounds(sp, torch, q_, k_, v_, o_acc, lse_acc, N, layout, B, H, S, D)
-            sp.striped_attn_fwd(q_, k_, v_, N, layout, out=o, lse_out=lse)
-            torch.cuda.synchronize()
-            per_round[lname]["lse_matches_batched"] = bool((lse_acc - lse).abs().max().item() <= 1e-3)
-            per_round[lname]["o_matches_batched"] = bool(
-                (o_acc[:, :, ::97].to(torch.bfloat16).float() - o[:, :, ::97].float()).abs().max().item() <= 2e-2)
-        del o_acc, lse_acc
-
     # End to end through the C ABI with host buffers (pinned): every step
     # copies its Q, K, V, dO in from host memory and its O, dQ, dK, dV back
-    # out, inside the timed region.  Copies run on their own streams and are
+    # out, inside the timed region.  Measured right after the device-timed
+    # steps, so that both run on a GPU in the same state (the step draws
+    # the GPU's whole power budget; measured later in the run, after the
+    # comparison legs, the same pipeline ran about 4% slower).  Copies run on their own streams and are
     # double-buffered, so step k's compute overlaps step k+1's inputs and
     # step k-1's outputs.
     e2e = None
@@ -589,7 +548,9 @@ def run_gpu(args, rank, world, local_rank):
 
         pipeline(2)  # untimed warm-up of the copy pipeline (first touches of the buffers)
         K = args.e2e_steps
-        t_e2e = pipeline(K)
+        with ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                          else local_rank) as clk_e2e:
+            t_e2e = pipeline(K)
         e_ms = max_over_ranks(t_e2e, dist, dev) / K
         # the copied-out results of the last step match the device results
         last = host_out[(K - 1) % 2]
@@ -601,8 +562,54 @@ def run_gpu(args, rank, world, local_rank):
         e2e = {"value": job_tflops(fl_step, e_ms, world), "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": bo, "ms_per_step": e_ms, "steps": K,
                "copies": "pinned host buffers, own streams, double-buffered (overlapped with compute); "
-                         "one untimed 2-step pass of the pipeline first"}
+                         "one untimed 2-step pass of the pipeline first; measured right after the "
+                         "device-timed steps",
+               "clocks": clk_e2e.summary()}
         del host_in, host_out, dev_in, dev_out
+
+    # the other placements on the same inputs, for comparison: contiguous
+    # (Ring Attention) and zig-zag (load-balanced), 2 timed steps each
+    contig = zigzag = None
+    if args.compare:
+        def layout_steps(layout, nc=2):
+            step(layout=layout)
+            torch.cuda.synchronize()
+            c0 = torch.cuda.Event(enable_timing=True)
+            c1 = torch.cuda.Event(enable_timing=True)
+            c0.record()
+            for _ in range(nc):
+                step(layout=layout)
+            c1.record()
+            torch.cuda.synchronize()
+            cms = c0.elapsed_time(c1) / nc
+            return {"ms_per_step": cms, "tflops": fl_step / (cms / 1000.0) / 1e12}
+
+        contig = layout_steps(sp.CONTIGUOUS)
+        zigzag = layout_steps(sp.ZIGZAG)
+
+    # per-round variant: N x N ring_round_fwd launches (one per device and
+    # ring round, merged into an fp32 (O, LSE) accumulator) against the
+    # batched forward of the same layout
+    per_round = None
+    if args.compare:
+        per_round = {}
+        o_acc = torch.empty(B, H, S, D, dtype=torch.float32, device=dev)
+        lse_acc = torch.empty(B, H, S, dtype=torch.float32, device=dev)
+        for lname, layout in (("striped", sp.STRIPED), ("zigzag", sp.ZIGZAG), ("contiguous", sp.CONTIGUOUS)):
+            if layout == sp.STRIPED:
+                q_, k_, v_ = (sp.striped_permute(x[n_], N, out=buf) for n_, buf in (("q", qs), ("k", ks), ("v", vs)))
+            elif layout == sp.ZIGZAG:
+                q_, k_, v_ = (sp.layout_permute(x[n_], N, layout, out=buf) for n_, buf in (("q", qs), ("k", ks),
+                                                                                        ("v", vs)))
+            else:
+                q_, k_, v_ = x["q"], x["k"], x["v"]
+            per_round[lname] = _time_rounds(sp, torch, q_, k_, v_, o_acc, lse_acc, N, layout, B, H, S, D)
+            sp.striped_attn_fwd(q_, k_, v_, N, layout, out=o, lse_out=lse)
+            torch.cuda.synchronize()
+            per_round[lname]["lse_matches_batched"] = bool((lse_acc - lse).abs().max().item() <= 1e-3)
+            per_round[lname]["o_matches_batched"] = bool(
+                (o_acc[:, :, ::97].to(torch.bfloat16).float() - o[:, :, ::97].float()).abs().max().item() <= 2e-2)
+        del o_acc, lse_acc
 
     if rank != 0:
         if dist is not None:
