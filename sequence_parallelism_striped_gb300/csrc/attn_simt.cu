@@ -11,7 +11,11 @@
 // Block = kSimtTile query (or key) rows x 8 threads per row; each thread
 // owns D/8 of the head dimension and dot products are reduced over the 8
 // threads of a row with warp shuffles.  Key/value (or query/dO) tiles are
-// staged in shared memory.
+// staged in shared memory; the 16 scores of a tile are formed together (so
+// their dot products, shuffles and exponentials overlap) and the forward's
+// running maximum is updated once per tile.  The kernels are instantiated
+// for D/8 = 8 and 16 (D = 64, 128) and, for the other multiples of 8, with
+// D/8 read at run time.
 #include <math.h>
 
 #include "common.cuh"
@@ -25,6 +29,10 @@ constexpr int T = kSimtTile;
 constexpr int kTPR = 8;             // threads per row
 constexpr int kThreads = T * kTPR;  // 128
 constexpr int kMaxDPT = 16;         // D <= 128
+// keys (query rows) per chunk in the gradient kernels: the unrolled chunk
+// keeps its K/Q and V/dO rows in flight, so it shrinks as D grows
+template <int DPT>
+__host__ __device__ constexpr int grad_chunk() { return DPT == 16 ? 4 : 8; }
 
 __device__ __forceinline__ float group_sum(float x) {
     x += __shfl_xor_sync(0xffffffffu, x, 4);
@@ -38,13 +46,27 @@ __device__ __forceinline__ int rows_in_tile(int64_t L, int t) {
     return r >= T ? T : (int)r;
 }
 
-// Stage tile t of a stripe (T rows of D floats) into smem, zero beyond L.
-__device__ __forceinline__ void stage_rows(float *dst, const float *src_stripe, int64_t L, int64_t D,
+// Head dimension of an instantiation: DPT = D/8 elements per thread, or 0
+// for D read at run time.
+template <int DPT>
+struct Dim {
+    static constexpr int kU = DPT ? DPT : kMaxDPT;  // unrolled loop bound
+    int dpt, D;
+    __device__ __forceinline__ explicit Dim(int64_t d) : dpt(DPT ? DPT : (int)d / kTPR), D(DPT ? DPT * kTPR : (int)d) {}
+};
+
+// Stage tile t of a stripe (T rows of D floats) into smem, zero beyond L;
+// 16-byte vectors (D is a multiple of 8).
+template <int DPT>
+__device__ __forceinline__ void stage_rows(float *dst, const float *src_stripe, int64_t L, const Dim<DPT> &dm,
                                            int t) {
     const int rows = rows_in_tile(L, t);
-    for (int idx = threadIdx.x; idx < T * D; idx += kThreads) {
-        const int r = idx / (int)D;
-        dst[idx] = (r < rows) ? src_stripe[((int64_t)t * T + r) * D + (idx - r * (int)D)] : 0.f;
+    const int D4 = dm.D / 4;
+    const float4 *src = reinterpret_cast<const float4 *>(src_stripe + (int64_t)t * T * dm.D);
+    float4 *d4 = reinterpret_cast<float4 *>(dst);
+    for (int idx = threadIdx.x; idx < T * D4; idx += kThreads) {
+        const int r = idx / D4;
+        d4[idx] = (r < rows) ? src[idx] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 }
 
@@ -56,21 +78,24 @@ struct RowState {
 // Online-softmax forward of query tile ag of stripe d over rounds
 // [r_lo, r_hi) (e_fixed >= 0: the single key stripe e_fixed).  With packed
 // sequences the schedule runs over the tiles of ag's own sequence.
+template <int DPT>
 __device__ void fwd_tile(const float *__restrict__ q_stripe, const float *__restrict__ k_head,
                          const float *__restrict__ v_head, const AttnGeom &g, int d, int ag, int r_lo,
                          int r_hi, int e_fixed, RowState &st, int64_t *tile_stats, float *sK,
                          float *sV) {
-    const int64_t L = g.L, D = g.D;
-    const int dpt = (int)D / kTPR;
+    constexpr int kU = Dim<DPT>::kU;
+    const Dim<DPT> dm(g.D);
+    const int64_t L = g.L;
+    const int D = dm.D, dpt = dm.dpt;
     const int row = threadIdx.x / kTPR, sub = threadIdx.x % kTPR;
     const int nq = (int)((L + T - 1) / T);
     const int rows_a = rows_in_tile(L, ag);
     const int64_t i = (int64_t)ag * T + row;
     const SeqSpan sq = seq_of(g.seqs, ag, T, nq);
     const int a = ag - sq.start, nqs = sq.count;
-    float qreg[kMaxDPT];
+    float qreg[kU];
 #pragma unroll
-    for (int c = 0; c < kMaxDPT; ++c)
+    for (int c = 0; c < kU; ++c)
         qreg[c] = (c < dpt && i < L) ? q_stripe[i * D + sub * dpt + c] : 0.f;
     st.m = -INFINITY;
     st.l = 0.f;
@@ -88,26 +113,47 @@ __device__ void fwd_tile(const float *__restrict__ q_stripe, const float *__rest
         const float *v_stripe = v_head + (int64_t)e * g.stripe_stride;
         for (int b = 0; b < ntiles; ++b) {
             __syncthreads();
-            stage_rows(sK, k_stripe, L, D, sq.start + b);
-            stage_rows(sV, v_stripe, L, D, sq.start + b);
+            stage_rows(sK, k_stripe, L, dm, sq.start + b);
+            stage_rows(sV, v_stripe, L, dm, sq.start + b);
             __syncthreads();
             const int rows_b = rows_in_tile(L, sq.start + b);
             const bool diag = sp.has_diag && b == sp.nfull;
-            for (int c = 0; c < rows_b; ++c) {
+            // the tile's scores; rows past the stripe end and masked pairs
+            // become -inf and drop out of the max and the sums
+            float sc[T];
+#pragma unroll
+            for (int c = 0; c < T; ++c) {
                 float part = 0.f;
 #pragma unroll
-                for (int u = 0; u < kMaxDPT; ++u)
+                for (int u = 0; u < kU; ++u)
                     if (u < dpt) part += qreg[u] * sK[c * D + sub * dpt + u];
-                const float s = g.scale * group_sum(part);
-                const bool keep = !diag || (c <= row + sp.diag_off);
-                if (!keep) continue;
-                const float m_new = fmaxf(st.m, s);
-                const float alpha = expf(st.m - m_new);  // exp(-inf) = 0 on the first key
-                const float p = expf(s - m_new);
-                st.l = st.l * alpha + p;
+                sc[c] = part;
+            }
+            float mt = -INFINITY;
 #pragma unroll
-                for (int u = 0; u < kMaxDPT; ++u)
-                    if (u < dpt) st.acc[u] = st.acc[u] * alpha + p * sV[c * D + sub * dpt + u];
+            for (int c = 0; c < T; ++c) {
+                const float s = g.scale * group_sum(sc[c]);
+                const bool keep = c < rows_b && (!diag || c <= row + sp.diag_off);
+                sc[c] = keep ? s : -INFINITY;
+                mt = fmaxf(mt, sc[c]);
+            }
+            if (mt != -INFINITY) {
+                const float m_new = fmaxf(st.m, mt);
+                const float alpha = expf(st.m - m_new);  // exp(-inf) = 0 on the first kept key
+                float lsum = 0.f;
+#pragma unroll
+                for (int c = 0; c < T; ++c) {
+                    sc[c] = expf(sc[c] - m_new);
+                    lsum += sc[c];
+                }
+                st.l = st.l * alpha + lsum;
+#pragma unroll
+                for (int u = 0; u < kU; ++u) st.acc[u] *= alpha;
+#pragma unroll
+                for (int c = 0; c < T; ++c)
+#pragma unroll
+                    for (int u = 0; u < kU; ++u)
+                        if (u < dpt) st.acc[u] += sc[c] * sV[c * D + sub * dpt + u];
                 st.m = m_new;
             }
             if (diag) ++n_part;
@@ -121,13 +167,14 @@ __device__ void fwd_tile(const float *__restrict__ q_stripe, const float *__rest
     }
 }
 
+template <int DPT>
 __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(const float *__restrict__ q,
                                                              const float *__restrict__ k,
                                                              const float *__restrict__ v,
                                                              float *__restrict__ o,
                                                              float *__restrict__ lse, AttnGeom g,
                                                              int64_t *tile_stats) {
-    extern __shared__ float smem[];
+    extern __shared__ __align__(16) float smem[];
     float *sK = smem, *sV = smem + T * g.D;
     const int nq = (int)((g.L + T - 1) / T);
     const int a = nq - 1 - (int)(blockIdx.x % nq);  // heavy query tiles first
@@ -136,36 +183,39 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(const float *__restr
     const int64_t kvh = bh / g.G;  // key/value head of query head bh
     const float *q_stripe = q + bh * g.stride_bh + (int64_t)d * g.stripe_stride;
     RowState st;
-    fwd_tile(q_stripe, k + kvh * g.stride_bh, v + kvh * g.stride_bh, g, d, a, 0, g.N, -1, st,
-             tile_stats, sK, sV);
+    fwd_tile<DPT>(q_stripe, k + kvh * g.stride_bh, v + kvh * g.stride_bh, g, d, a, 0, g.N, -1, st,
+                  tile_stats, sK, sV);
     const int row = threadIdx.x / kTPR, sub = threadIdx.x % kTPR;
     const int64_t i = (int64_t)a * T + row;
     if (i >= g.L) return;
-    const int dpt = (int)g.D / kTPR;
+    const int dpt = Dim<DPT>(g.D).dpt;
     float *orow = o + bh * g.stride_bh + (int64_t)d * g.stripe_stride + i * g.D + sub * dpt;
     const float inv = 1.f / st.l;
-    for (int u = 0; u < dpt; ++u) orow[u] = st.acc[u] * inv;
+#pragma unroll
+    for (int u = 0; u < Dim<DPT>::kU; ++u)
+        if (u < dpt) orow[u] = st.acc[u] * inv;
     if (sub == 0)
         lse[bh * g.lse_stride_bh + (int64_t)d * g.lse_stripe_stride + i] = st.m + logf(st.l);
 }
 
+template <int DPT>
 __global__ void __launch_bounds__(kThreads) simt_round_kernel(
     const float *__restrict__ q_d, const float *__restrict__ k_e, const float *__restrict__ v_e,
     float *__restrict__ o_acc, float *__restrict__ lse_acc, float *__restrict__ o_out, int d, int e,
     int first, AttnGeom g, int64_t *tile_stats) {
-    extern __shared__ float smem[];
+    extern __shared__ __align__(16) float smem[];
     float *sK = smem, *sV = smem + T * g.D;
     const int nq = (int)((g.L + T - 1) / T);
     const int a = nq - 1 - (int)blockIdx.x;
     const int64_t bh = blockIdx.y;
     RowState st;
     // the launcher sets stripe_stride = 0: k_e / v_e are the stripe slices
-    fwd_tile(q_d + bh * g.stride_bh, k_e + bh * g.stride_bh, v_e + bh * g.stride_bh, g, d, a, 0, 1,
-             e, st, tile_stats, sK, sV);
+    fwd_tile<DPT>(q_d + bh * g.stride_bh, k_e + bh * g.stride_bh, v_e + bh * g.stride_bh, g, d, a, 0, 1,
+                  e, st, tile_stats, sK, sV);
     const int row = threadIdx.x / kTPR, sub = threadIdx.x % kTPR;
     const int64_t i = (int64_t)a * T + row;
     if (i >= g.L) return;
-    const int dpt = (int)g.D / kTPR;
+    const int dpt = Dim<DPT>(g.D).dpt;
     // this round's normalised partial result; LSE_r = -inf when nothing kept
     const bool empty = !(st.l > 0.f);
     const float lse_r = empty ? -INFINITY : st.m + logf(st.l);
@@ -183,7 +233,9 @@ __global__ void __launch_bounds__(kThreads) simt_round_kernel(
         wr *= inv;
     }
     const float inv_l = empty ? 0.f : 1.f / st.l;
-    for (int u = 0; u < dpt; ++u) {
+#pragma unroll
+    for (int u = 0; u < Dim<DPT>::kU; ++u) {
+        if (u >= dpt) continue;
         const float o_r = st.acc[u] * inv_l;
         float val;
         if (mx == -INFINITY) val = first ? 0.f : acc_row[u];
@@ -208,18 +260,21 @@ __global__ void simt_delta_kernel(const float *__restrict__ o, const float *__re
 }
 
 // dQ: query tile of stripe d, same schedule as the forward.
+template <int DPT>
 __global__ void __launch_bounds__(kThreads) simt_dq_kernel(
     const float *__restrict__ q, const float *__restrict__ k, const float *__restrict__ v,
     const float *__restrict__ lse, const float *__restrict__ dO, const float *__restrict__ delta,
     float *__restrict__ dq, AttnGeom g, int64_t *tile_stats) {
-    extern __shared__ float smem[];
+    extern __shared__ __align__(16) float smem[];
     float *sK = smem, *sV = smem + T * g.D;
-    const int64_t L = g.L, D = g.D;
+    constexpr int kU = Dim<DPT>::kU, kCh = grad_chunk<DPT>();
+    const Dim<DPT> dm(g.D);
+    const int64_t L = g.L;
+    const int D = dm.D, dpt = dm.dpt;
     const int nq = (int)((L + T - 1) / T);
     const int ag = nq - 1 - (int)(blockIdx.x % nq);
     const int d = (int)(blockIdx.x / nq);
     const int64_t bh = blockIdx.y;
-    const int dpt = (int)D / kTPR;
     const int row = threadIdx.x / kTPR, sub = threadIdx.x % kTPR;
     const int64_t i = (int64_t)ag * T + row;
     const bool valid = i < L;
@@ -227,9 +282,9 @@ __global__ void __launch_bounds__(kThreads) simt_dq_kernel(
     const int a = ag - sq.start, nqs = sq.count;
     const int64_t qoff = bh * g.stride_bh + (int64_t)d * g.stripe_stride + i * D + sub * dpt;
     const int64_t soff = bh * g.lse_stride_bh + (int64_t)d * g.lse_stripe_stride + i;
-    float qreg[kMaxDPT], doreg[kMaxDPT], acc[kMaxDPT];
+    float qreg[kU], doreg[kU], acc[kU];
 #pragma unroll
-    for (int u = 0; u < kMaxDPT; ++u) {
+    for (int u = 0; u < kU; ++u) {
         qreg[u] = (u < dpt && valid) ? q[qoff + u] : 0.f;
         doreg[u] = (u < dpt && valid) ? dO[qoff + u] : 0.f;
         acc[u] = 0.f;
@@ -246,28 +301,42 @@ __global__ void __launch_bounds__(kThreads) simt_dq_kernel(
         const float *v_stripe = v + (bh / g.G) * g.stride_bh + (int64_t)e * g.stripe_stride;
         for (int b = 0; b < ntiles; ++b) {
             __syncthreads();
-            stage_rows(sK, k_stripe, L, D, sq.start + b);
-            stage_rows(sV, v_stripe, L, D, sq.start + b);
+            stage_rows(sK, k_stripe, L, dm, sq.start + b);
+            stage_rows(sV, v_stripe, L, dm, sq.start + b);
             __syncthreads();
             const int rows_b = rows_in_tile(L, sq.start + b);
             const bool diag = sp.has_diag && b == sp.nfull;
-            for (int c = 0; c < rows_b; ++c) {
-                float ps = 0.f, pp = 0.f;
+            // the tile's keys in chunks of kCh (a rolled loop bounds the
+            // registers the unrolled chunk keeps live)
+#pragma unroll 1
+            for (int c0 = 0; c0 < T; c0 += kCh) {
+                float ps[kCh], pp[kCh];
 #pragma unroll
-                for (int u = 0; u < kMaxDPT; ++u)
-                    if (u < dpt) {
-                        ps += qreg[u] * sK[c * D + sub * dpt + u];
-                        pp += doreg[u] * sV[c * D + sub * dpt + u];
-                    }
-                const float s = g.scale * group_sum(ps);
-                const float dp = group_sum(pp);
-                const bool keep = valid && (!diag || (c <= row + sp.diag_off));
-                if (!keep) continue;
-                const float P = expf(s - lse_i);
-                const float dS = P * (dp - delta_i);
+                for (int c = 0; c < kCh; ++c) {
+                    float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-                for (int u = 0; u < kMaxDPT; ++u)
-                    if (u < dpt) acc[u] += dS * sK[c * D + sub * dpt + u];
+                    for (int u = 0; u < kU; ++u)
+                        if (u < dpt) {
+                            s0 += qreg[u] * sK[(c0 + c) * D + sub * dpt + u];
+                            s1 += doreg[u] * sV[(c0 + c) * D + sub * dpt + u];
+                        }
+                    ps[c] = s0;
+                    pp[c] = s1;
+                }
+                // dS of the chunk's kept pairs (0 elsewhere), in ps
+#pragma unroll
+                for (int c = 0; c < kCh; ++c) {
+                    const float s = g.scale * group_sum(ps[c]);
+                    const float dp = group_sum(pp[c]);
+                    const bool keep = valid && c0 + c < rows_b && (!diag || c0 + c <= row + sp.diag_off);
+                    const float P = keep ? expf(s - lse_i) : 0.f;
+                    ps[c] = P * (dp - delta_i);
+                }
+#pragma unroll
+                for (int c = 0; c < kCh; ++c)
+#pragma unroll
+                    for (int u = 0; u < kU; ++u)
+                        if (u < dpt) acc[u] += ps[c] * sK[(c0 + c) * D + sub * dpt + u];
             }
             if (diag) ++n_part;
             else ++n_full;
@@ -278,34 +347,39 @@ __global__ void __launch_bounds__(kThreads) simt_dq_kernel(
         }
     }
     if (!valid) return;
-    for (int u = 0; u < dpt; ++u) dq[qoff + u] = g.scale * acc[u];
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+        if (u < dpt) dq[qoff + u] = g.scale * acc[u];
 }
 
 // dK, dV: key tile b of stripe e of key/value head blockIdx.y; visits every
 // query tile that sees it, for each of the G query heads that read the head,
 // in ring order (round r: the key stripe sits on device d = e + r).
+template <int DPT>
 __global__ void __launch_bounds__(kThreads) simt_dkdv_kernel(
     const float *__restrict__ q, const float *__restrict__ k, const float *__restrict__ v,
     const float *__restrict__ lse, const float *__restrict__ dO, const float *__restrict__ delta,
     float *__restrict__ dk, float *__restrict__ dv, AttnGeom g) {
-    extern __shared__ float smem[];
+    extern __shared__ __align__(16) float smem[];
     float *sQ = smem, *sdO = smem + T * g.D;
     float *sL = smem + 2 * T * g.D, *sDel = sL + T;
-    const int64_t L = g.L, D = g.D;
+    constexpr int kU = Dim<DPT>::kU, kCh = grad_chunk<DPT>();
+    const Dim<DPT> dm(g.D);
+    const int64_t L = g.L;
+    const int D = dm.D, dpt = dm.dpt;
     const int nq = (int)((L + T - 1) / T);
     const int bg = nq - 1 - (int)(blockIdx.x % nq);
     const int e = (int)(blockIdx.x / nq);
     const int64_t bh = blockIdx.y;
-    const int dpt = (int)D / kTPR;
     const int row = threadIdx.x / kTPR, sub = threadIdx.x % kTPR;  // key row in the tile
     const int64_t j = (int64_t)bg * T + row;
     const SeqSpan sq = seq_of(g.seqs, bg, T, nq);  // packed sequences: own sequence's tiles
     const int b = bg - sq.start, nqs = sq.count;
     const bool valid = j < L;
     const int64_t koff = bh * g.stride_bh + (int64_t)e * g.stripe_stride + j * D + sub * dpt;
-    float kreg[kMaxDPT], vreg[kMaxDPT], ak[kMaxDPT], av[kMaxDPT];
+    float kreg[kU], vreg[kU], ak[kU], av[kU];
 #pragma unroll
-    for (int u = 0; u < kMaxDPT; ++u) {
+    for (int u = 0; u < kU; ++u) {
         kreg[u] = (u < dpt && valid) ? k[koff + u] : 0.f;
         vreg[u] = (u < dpt && valid) ? v[koff + u] : 0.f;
         ak[u] = av[u] = 0.f;
@@ -323,8 +397,8 @@ __global__ void __launch_bounds__(kThreads) simt_dkdv_kernel(
         for (int a = sp.a_lo; a < nqs; ++a) {
             const int ag = sq.start + a;  // query tile in the slice
             __syncthreads();
-            stage_rows(sQ, q_stripe, L, D, ag);
-            stage_rows(sdO, do_stripe, L, D, ag);
+            stage_rows(sQ, q_stripe, L, dm, ag);
+            stage_rows(sdO, do_stripe, L, dm, ag);
             const int rows_a = rows_in_tile(L, ag);
             if (threadIdx.x < T) {
                 sL[threadIdx.x] = threadIdx.x < rows_a ? l_stripe[(int64_t)ag * T + threadIdx.x] : 0.f;
@@ -333,35 +407,50 @@ __global__ void __launch_bounds__(kThreads) simt_dkdv_kernel(
             }
             __syncthreads();
             const bool diag = sp.has_diag && a == sp.a_lo;
-            for (int c = 0; c < rows_a; ++c) {  // c = query row in tile a
-                float ps = 0.f, pp = 0.f;
+#pragma unroll 1
+            for (int c0 = 0; c0 < T; c0 += kCh) {  // query rows c0 + c of tile a
+                float ps[kCh], pp[kCh];
 #pragma unroll
-                for (int u = 0; u < kMaxDPT; ++u)
-                    if (u < dpt) {
-                        ps += kreg[u] * sQ[c * D + sub * dpt + u];
-                        pp += vreg[u] * sdO[c * D + sub * dpt + u];
-                    }
-                const float s = g.scale * group_sum(ps);
-                const float dp = group_sum(pp);
-                // pair (query row c, key row `row`) kept iff row <= c + diag_off
-                const bool keep = valid && (!diag || (row <= c + sp.diag_off));
-                if (!keep) continue;
-                const float P = expf(s - sL[c]);
-                const float dS = P * (dp - sDel[c]);
+                for (int c = 0; c < kCh; ++c) {
+                    float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-                for (int u = 0; u < kMaxDPT; ++u)
-                    if (u < dpt) {
-                        ak[u] += dS * sQ[c * D + sub * dpt + u];
-                        av[u] += P * sdO[c * D + sub * dpt + u];
-                    }
+                    for (int u = 0; u < kU; ++u)
+                        if (u < dpt) {
+                            s0 += kreg[u] * sQ[(c0 + c) * D + sub * dpt + u];
+                            s1 += vreg[u] * sdO[(c0 + c) * D + sub * dpt + u];
+                        }
+                    ps[c] = s0;
+                    pp[c] = s1;
+                }
+                // P (in pp) and dS (in ps) of the kept pairs, 0 elsewhere: pair
+                // (query row c0 + c, key row `row`) kept iff row <= c0 + c + diag_off
+#pragma unroll
+                for (int c = 0; c < kCh; ++c) {
+                    const float s = g.scale * group_sum(ps[c]);
+                    const float dp = group_sum(pp[c]);
+                    const bool keep = valid && c0 + c < rows_a && (!diag || row <= c0 + c + sp.diag_off);
+                    const float P = keep ? expf(s - sL[c0 + c]) : 0.f;
+                    ps[c] = P * (dp - sDel[c0 + c]);
+                    pp[c] = P;
+                }
+#pragma unroll
+                for (int c = 0; c < kCh; ++c)
+#pragma unroll
+                    for (int u = 0; u < kU; ++u)
+                        if (u < dpt) {
+                            ak[u] += ps[c] * sQ[(c0 + c) * D + sub * dpt + u];
+                            av[u] += pp[c] * sdO[(c0 + c) * D + sub * dpt + u];
+                        }
             }
         }
     }
     if (!valid) return;
-    for (int u = 0; u < dpt; ++u) {
-        dk[koff + u] = g.scale * ak[u];
-        dv[koff + u] = av[u];
-    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+        if (u < dpt) {
+            dk[koff + u] = g.scale * ak[u];
+            dv[koff + u] = av[u];
+        }
 }
 
 }  // namespace
@@ -371,7 +460,12 @@ int launch_simt_fwd(const float *q, const float *k, const float *v, float *o, fl
     const int nq = (int)((g.L + T - 1) / T);
     dim3 grid((unsigned)(nq * g.N), (unsigned)g.BH);
     const size_t smem = 2 * T * g.D * sizeof(float);
-    simt_fwd_kernel<<<grid, kThreads, smem, stream>>>(q, k, v, o, lse, g, tile_stats);
+    if (g.D == 64)
+        simt_fwd_kernel<8><<<grid, kThreads, smem, stream>>>(q, k, v, o, lse, g, tile_stats);
+    else if (g.D == 128)
+        simt_fwd_kernel<16><<<grid, kThreads, smem, stream>>>(q, k, v, o, lse, g, tile_stats);
+    else
+        simt_fwd_kernel<0><<<grid, kThreads, smem, stream>>>(q, k, v, o, lse, g, tile_stats);
     return cuda_status(cudaGetLastError());
 }
 
@@ -384,8 +478,31 @@ int launch_simt_round(const float *q_d, const float *k_e, const float *v_e, floa
     AttnGeom gs = g;
     gs.stripe_stride = 0;
     gs.lse_stripe_stride = 0;
-    simt_round_kernel<<<grid, kThreads, smem, stream>>>(q_d, k_e, v_e, o_acc, lse_acc, o_out, d, e,
-                                                        first, gs, tile_stats);
+    if (g.D == 64)
+        simt_round_kernel<8><<<grid, kThreads, smem, stream>>>(q_d, k_e, v_e, o_acc, lse_acc, o_out, d, e,
+                                                              first, gs, tile_stats);
+    else if (g.D == 128)
+        simt_round_kernel<16><<<grid, kThreads, smem, stream>>>(q_d, k_e, v_e, o_acc, lse_acc, o_out, d, e,
+                                                               first, gs, tile_stats);
+    else
+        simt_round_kernel<0><<<grid, kThreads, smem, stream>>>(q_d, k_e, v_e, o_acc, lse_acc, o_out, d, e,
+                                                              first, gs, tile_stats);
+    return cuda_status(cudaGetLastError());
+}
+
+template <int DPT>
+static int launch_simt_grads(const float *q, const float *k, const float *v, const float *lse, const float *dO,
+                             float *dq, float *dk, float *dv, const float *delta_ws, const AttnGeom &g,
+                             int64_t *tile_stats, cudaStream_t stream) {
+    const int nq = (int)((g.L + T - 1) / T);
+    dim3 grid((unsigned)(nq * g.N), (unsigned)g.BH);
+    const size_t smem = 2 * T * g.D * sizeof(float);
+    simt_dq_kernel<DPT><<<grid, kThreads, smem, stream>>>(q, k, v, lse, dO, delta_ws, dq, g, tile_stats);
+    const int st = cuda_status(cudaGetLastError());
+    if (st != STRIPED_OK) return st;
+    dim3 grid_kv((unsigned)(nq * g.N), (unsigned)(g.BH / g.G));  // key tiles of every key/value head
+    simt_dkdv_kernel<DPT><<<grid_kv, kThreads, smem + 2 * T * sizeof(float), stream>>>(q, k, v, lse, dO,
+                                                                                       delta_ws, dk, dv, g);
     return cuda_status(cudaGetLastError());
 }
 
@@ -395,18 +512,11 @@ int launch_simt_bwd(const float *q, const float *k, const float *v, const float 
     // full [BH][S][D] tensors: rows of all heads are contiguous
     const int64_t rows = g.BH * g.N * g.L;
     simt_delta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(o, dO, delta_ws, rows, g.D);
-    int st = cuda_status(cudaGetLastError());
+    const int st = cuda_status(cudaGetLastError());
     if (st != STRIPED_OK) return st;
-    const int nq = (int)((g.L + T - 1) / T);
-    dim3 grid((unsigned)(nq * g.N), (unsigned)g.BH);
-    const size_t smem = 2 * T * g.D * sizeof(float);
-    simt_dq_kernel<<<grid, kThreads, smem, stream>>>(q, k, v, lse, dO, delta_ws, dq, g, tile_stats);
-    st = cuda_status(cudaGetLastError());
-    if (st != STRIPED_OK) return st;
-    dim3 grid_kv((unsigned)(nq * g.N), (unsigned)(g.BH / g.G));  // key tiles of every key/value head
-    simt_dkdv_kernel<<<grid_kv, kThreads, smem + 2 * T * sizeof(float), stream>>>(q, k, v, lse, dO,
-                                                                                  delta_ws, dk, dv, g);
-    return cuda_status(cudaGetLastError());
+    if (g.D == 64) return launch_simt_grads<8>(q, k, v, lse, dO, dq, dk, dv, delta_ws, g, tile_stats, stream);
+    if (g.D == 128) return launch_simt_grads<16>(q, k, v, lse, dO, dq, dk, dv, delta_ws, g, tile_stats, stream);
+    return launch_simt_grads<0>(q, k, v, lse, dO, dq, dk, dv, delta_ws, g, tile_stats, stream);
 }
 
 }  // namespace striped
