@@ -55,18 +55,37 @@ struct Dim {
     __device__ __forceinline__ explicit Dim(int64_t d) : dpt(DPT ? DPT : (int)d / kTPR), D(DPT ? DPT * kTPR : (int)d) {}
 };
 
-// Stage tile t of a stripe (T rows of D floats) into smem, zero beyond L;
-// 16-byte vectors (D is a multiple of 8).
+// One thread's share of tile t of a stripe (T rows of D floats, zero
+// beyond L) as 16-byte vectors (D is a multiple of 8): loaded into
+// registers while the previous tile is computed, then stored to shared
+// memory.
+constexpr int kMaxF4 = (T * kMaxDPT * kTPR / 4 + kThreads - 1) / kThreads;  // 4
 template <int DPT>
-__device__ __forceinline__ void stage_rows(float *dst, const float *src_stripe, int64_t L, const Dim<DPT> &dm,
-                                           int t) {
+struct TileRegs {
+    static constexpr int kN = DPT ? (T * DPT * kTPR / 4 + kThreads - 1) / kThreads : kMaxF4;
+    float4 v[kN];
+};
+
+template <int DPT>
+__device__ __forceinline__ void tile_load(TileRegs<DPT> &r, const float *src_stripe, int64_t L, const Dim<DPT> &dm,
+                                          int t) {
     const int rows = rows_in_tile(L, t);
     const int D4 = dm.D / 4;
     const float4 *src = reinterpret_cast<const float4 *>(src_stripe + (int64_t)t * T * dm.D);
+#pragma unroll
+    for (int k = 0; k < TileRegs<DPT>::kN; ++k) {
+        const int idx = threadIdx.x + k * kThreads;
+        r.v[k] = (idx < T * D4 && idx / D4 < rows) ? src[idx] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+template <int DPT>
+__device__ __forceinline__ void tile_store(const TileRegs<DPT> &r, float *dst, const Dim<DPT> &dm) {
     float4 *d4 = reinterpret_cast<float4 *>(dst);
-    for (int idx = threadIdx.x; idx < T * D4; idx += kThreads) {
-        const int r = idx / D4;
-        d4[idx] = (r < rows) ? src[idx] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < TileRegs<DPT>::kN; ++k) {
+        const int idx = threadIdx.x + k * kThreads;
+        if (idx < T * (dm.D / 4)) d4[idx] = r.v[k];
     }
 }
 
@@ -102,20 +121,46 @@ __device__ void fwd_tile(const float *__restrict__ q_stripe, const float *__rest
 #pragma unroll
     for (int c = 0; c < kMaxDPT; ++c) st.acc[c] = 0.f;
 
-    for (int r = r_lo; r < r_hi; ++r) {
-        const int e = e_fixed >= 0 ? e_fixed : (d - r + g.N) % g.N;
-        const RoundSpan sp = round_span(g.layout, d, e, a, nqs, rows_a);
-        const int ntiles = sp.nfull + sp.has_diag;
-        // tiles of this round processed below (full / partial), counted as
-        // they run and added to the round's counters once
-        int n_full = 0, n_part = 0;
-        const float *k_stripe = k_head + (int64_t)e * g.stripe_stride;
-        const float *v_stripe = v_head + (int64_t)e * g.stripe_stride;
-        for (int b = 0; b < ntiles; ++b) {
-            __syncthreads();
-            stage_rows(sK, k_stripe, L, dm, sq.start + b);
-            stage_rows(sV, v_stripe, L, dm, sq.start + b);
-            __syncthreads();
+    // the (round, key tile) sequence of this query tile; the next tile's K
+    // and V are loaded into registers while the current one is computed
+    struct Cur {
+        int r, b, e, ntiles;
+        RoundSpan sp;
+    };
+    auto seek = [&](Cur &c) -> bool {
+        for (; c.r < r_hi; ++c.r, c.b = 0) {
+            c.e = e_fixed >= 0 ? e_fixed : (d - c.r + g.N) % g.N;
+            c.sp = round_span(g.layout, d, c.e, a, nqs, rows_a);
+            c.ntiles = c.sp.nfull + c.sp.has_diag;
+            if (c.b < c.ntiles) return true;
+        }
+        return false;
+    };
+    Cur cur{r_lo, 0, 0, 0, RoundSpan{0, 0, 0}};
+    bool have = seek(cur);
+    TileRegs<DPT> rk, rv;
+    if (have) {
+        tile_load(rk, k_head + (int64_t)cur.e * g.stripe_stride, L, dm, sq.start + cur.b);
+        tile_load(rv, v_head + (int64_t)cur.e * g.stripe_stride, L, dm, sq.start + cur.b);
+    }
+    // tiles of the current round processed so far (full / partial), added to
+    // the round's counters when the round ends
+    int n_full = 0, n_part = 0;
+    while (have) {
+        __syncthreads();
+        tile_store(rk, sK, dm);
+        tile_store(rv, sV, dm);
+        __syncthreads();
+        Cur nxt = cur;
+        ++nxt.b;
+        const bool have_next = seek(nxt);
+        if (have_next) {
+            tile_load(rk, k_head + (int64_t)nxt.e * g.stripe_stride, L, dm, sq.start + nxt.b);
+            tile_load(rv, v_head + (int64_t)nxt.e * g.stripe_stride, L, dm, sq.start + nxt.b);
+        }
+        const RoundSpan &sp = cur.sp;
+        const int b = cur.b;
+        {
             const int rows_b = rows_in_tile(L, sq.start + b);
             const bool diag = sp.has_diag && b == sp.nfull;
             // the tile's scores; rows past the stripe end and masked pairs
@@ -159,11 +204,16 @@ __device__ void fwd_tile(const float *__restrict__ q_stripe, const float *__rest
             if (diag) ++n_part;
             else ++n_full;
         }
-        if (tile_stats && threadIdx.x == 0 && (n_full | n_part)) {
-            const int rr = ring_round_of(d, e, g.N);
-            atomicAdd((unsigned long long *)&tile_stats[rr * g.N + d], (unsigned long long)n_full);
-            atomicAdd((unsigned long long *)&tile_stats[g.N * g.N + rr * g.N + d], (unsigned long long)n_part);
+        if (!have_next || nxt.r != cur.r) {
+            if (tile_stats && threadIdx.x == 0) {
+                const int rr = ring_round_of(d, cur.e, g.N);
+                atomicAdd((unsigned long long *)&tile_stats[rr * g.N + d], (unsigned long long)n_full);
+                atomicAdd((unsigned long long *)&tile_stats[g.N * g.N + rr * g.N + d], (unsigned long long)n_part);
+            }
+            n_full = n_part = 0;
         }
+        cur = nxt;
+        have = have_next;
     }
 }
 
@@ -292,18 +342,44 @@ __global__ void __launch_bounds__(kThreads) simt_dq_kernel(
     const float lse_i = valid ? lse[soff] : 0.f;
     const float delta_i = valid ? delta[soff] : 0.f;
     const int rows_a = rows_in_tile(L, ag);
-    for (int r = 0; r < g.N; ++r) {
-        const int e = (d - r + g.N) % g.N;
-        const RoundSpan sp = round_span(g.layout, d, e, a, nqs, rows_a);
-        const int ntiles = sp.nfull + sp.has_diag;
-        int n_full = 0, n_part = 0;  // tiles processed below, counted as they run
-        const float *k_stripe = k + (bh / g.G) * g.stride_bh + (int64_t)e * g.stripe_stride;
-        const float *v_stripe = v + (bh / g.G) * g.stride_bh + (int64_t)e * g.stripe_stride;
-        for (int b = 0; b < ntiles; ++b) {
-            __syncthreads();
-            stage_rows(sK, k_stripe, L, dm, sq.start + b);
-            stage_rows(sV, v_stripe, L, dm, sq.start + b);
-            __syncthreads();
+    const float *k_head = k + (bh / g.G) * g.stride_bh, *v_head = v + (bh / g.G) * g.stride_bh;
+    // the (round, key tile) sequence, the next tile loading during this one
+    struct Cur {
+        int r, b, e, ntiles;
+        RoundSpan sp;
+    };
+    auto seek = [&](Cur &c) -> bool {
+        for (; c.r < g.N; ++c.r, c.b = 0) {
+            c.e = (d - c.r + g.N) % g.N;
+            c.sp = round_span(g.layout, d, c.e, a, nqs, rows_a);
+            c.ntiles = c.sp.nfull + c.sp.has_diag;
+            if (c.b < c.ntiles) return true;
+        }
+        return false;
+    };
+    Cur cur{0, 0, 0, 0, RoundSpan{0, 0, 0}};
+    bool have = seek(cur);
+    TileRegs<DPT> rk, rv;
+    if (have) {
+        tile_load(rk, k_head + (int64_t)cur.e * g.stripe_stride, L, dm, sq.start + cur.b);
+        tile_load(rv, v_head + (int64_t)cur.e * g.stripe_stride, L, dm, sq.start + cur.b);
+    }
+    int n_full = 0, n_part = 0;  // tiles of the current round, counted as they run
+    while (have) {
+        __syncthreads();
+        tile_store(rk, sK, dm);
+        tile_store(rv, sV, dm);
+        __syncthreads();
+        Cur nxt = cur;
+        ++nxt.b;
+        const bool have_next = seek(nxt);
+        if (have_next) {
+            tile_load(rk, k_head + (int64_t)nxt.e * g.stripe_stride, L, dm, sq.start + nxt.b);
+            tile_load(rv, v_head + (int64_t)nxt.e * g.stripe_stride, L, dm, sq.start + nxt.b);
+        }
+        const RoundSpan &sp = cur.sp;
+        {
+            const int b = cur.b;
             const int rows_b = rows_in_tile(L, sq.start + b);
             const bool diag = sp.has_diag && b == sp.nfull;
             // the tile's keys in chunks of kCh (a rolled loop bounds the
@@ -341,10 +417,15 @@ __global__ void __launch_bounds__(kThreads) simt_dq_kernel(
             if (diag) ++n_part;
             else ++n_full;
         }
-        if (tile_stats && threadIdx.x == 0 && (n_full | n_part)) {
-            atomicAdd((unsigned long long *)&tile_stats[r * g.N + d], (unsigned long long)n_full);
-            atomicAdd((unsigned long long *)&tile_stats[g.N * g.N + r * g.N + d], (unsigned long long)n_part);
+        if (!have_next || nxt.r != cur.r) {
+            if (tile_stats && threadIdx.x == 0) {
+                atomicAdd((unsigned long long *)&tile_stats[cur.r * g.N + d], (unsigned long long)n_full);
+                atomicAdd((unsigned long long *)&tile_stats[g.N * g.N + cur.r * g.N + d], (unsigned long long)n_part);
+            }
+            n_full = n_part = 0;
         }
+        cur = nxt;
+        have = have_next;
     }
     if (!valid) return;
 #pragma unroll
@@ -385,30 +466,67 @@ __global__ void __launch_bounds__(kThreads) simt_dkdv_kernel(
         ak[u] = av[u] = 0.f;
     }
     const int rows_b = rows_in_tile(L, bg);
-    for (int hr = 0; hr < g.G * g.N; ++hr) {
-        const int64_t bq = bh * g.G + hr / g.N;  // query head
-        const int r = (int)(hr % g.N);
-        const int d = (e + r) % g.N;
-        const QuerySpan sp = query_span(g.layout, d, e, b, nqs, rows_b);
-        const float *q_stripe = q + bq * g.stride_bh + (int64_t)d * g.stripe_stride;
-        const float *do_stripe = dO + bq * g.stride_bh + (int64_t)d * g.stripe_stride;
-        const float *l_stripe = lse + bq * g.lse_stride_bh + (int64_t)d * g.lse_stripe_stride;
-        const float *dl_stripe = delta + bq * g.lse_stride_bh + (int64_t)d * g.lse_stripe_stride;
-        for (int a = sp.a_lo; a < nqs; ++a) {
-            const int ag = sq.start + a;  // query tile in the slice
-            __syncthreads();
-            stage_rows(sQ, q_stripe, L, dm, ag);
-            stage_rows(sdO, do_stripe, L, dm, ag);
-            const int rows_a = rows_in_tile(L, ag);
-            if (threadIdx.x < T) {
-                sL[threadIdx.x] = threadIdx.x < rows_a ? l_stripe[(int64_t)ag * T + threadIdx.x] : 0.f;
-                sDel[threadIdx.x] =
-                    threadIdx.x < rows_a ? dl_stripe[(int64_t)ag * T + threadIdx.x] : 0.f;
+    // the (query head and round, query tile) sequence; the next tile's Q,
+    // dO and row statistics load during this one
+    struct Cur {
+        int hr, a;
+        QuerySpan sp;
+        const float *q, *dO, *lse, *del;
+    };
+    auto seek = [&](Cur &c) -> bool {
+        for (; c.hr < g.G * g.N; ++c.hr, c.a = -1) {
+            const int64_t bq = bh * g.G + c.hr / g.N;  // query head
+            const int d = (e + c.hr % g.N) % g.N;       // round r: the key stripe sits on device e + r
+            c.sp = query_span(g.layout, d, e, b, nqs, rows_b);
+            if (c.a < c.sp.a_lo) c.a = c.sp.a_lo;
+            if (c.a < nqs) {
+                c.q = q + bq * g.stride_bh + (int64_t)d * g.stripe_stride;
+                c.dO = dO + bq * g.stride_bh + (int64_t)d * g.stripe_stride;
+                c.lse = lse + bq * g.lse_stride_bh + (int64_t)d * g.lse_stripe_stride;
+                c.del = delta + bq * g.lse_stride_bh + (int64_t)d * g.lse_stripe_stride;
+                return true;
             }
-            __syncthreads();
-            const bool diag = sp.has_diag && a == sp.a_lo;
+        }
+        return false;
+    };
+    auto load_stats = [&](const Cur &c, float &lv, float &dv_) {
+        const int ag = sq.start + c.a;
+        const bool in = threadIdx.x < rows_in_tile(L, ag);
+        lv = (threadIdx.x < T && in) ? c.lse[(int64_t)ag * T + threadIdx.x] : 0.f;
+        dv_ = (threadIdx.x < T && in) ? c.del[(int64_t)ag * T + threadIdx.x] : 0.f;
+    };
+    Cur cur{0, -1, QuerySpan{0, 0, 0}, nullptr, nullptr, nullptr, nullptr};
+    bool have = seek(cur);
+    TileRegs<DPT> rq, ro;
+    float lv = 0.f, dlv = 0.f;
+    if (have) {
+        tile_load(rq, cur.q, L, dm, sq.start + cur.a);
+        tile_load(ro, cur.dO, L, dm, sq.start + cur.a);
+        load_stats(cur, lv, dlv);
+    }
+    while (have) {
+        __syncthreads();
+        tile_store(rq, sQ, dm);
+        tile_store(ro, sdO, dm);
+        if (threadIdx.x < T) {
+            sL[threadIdx.x] = lv;
+            sDel[threadIdx.x] = dlv;
+        }
+        __syncthreads();
+        Cur nxt = cur;
+        ++nxt.a;
+        const bool have_next = seek(nxt);
+        if (have_next) {
+            tile_load(rq, nxt.q, L, dm, sq.start + nxt.a);
+            tile_load(ro, nxt.dO, L, dm, sq.start + nxt.a);
+            load_stats(nxt, lv, dlv);
+        }
+        {
+            const QuerySpan &sp = cur.sp;
+            const int rows_a = rows_in_tile(L, sq.start + cur.a);
+            const bool diag = sp.has_diag && cur.a == sp.a_lo;
 #pragma unroll 1
-            for (int c0 = 0; c0 < T; c0 += kCh) {  // query rows c0 + c of tile a
+            for (int c0 = 0; c0 < T; c0 += kCh) {  // query rows c0 + c of the tile
                 float ps[kCh], pp[kCh];
 #pragma unroll
                 for (int c = 0; c < kCh; ++c) {
@@ -443,6 +561,8 @@ __global__ void __launch_bounds__(kThreads) simt_dkdv_kernel(
                         }
             }
         }
+        cur = nxt;
+        have = have_next;
     }
     if (!valid) return;
 #pragma unroll
