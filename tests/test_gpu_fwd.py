@@ -46,7 +46,9 @@ def _check_fwd(x, o, lse, stats, B, H, S, D, N, layout, dtype, heads=None):
 
 @pytest.mark.parametrize("layout", [sp.STRIPED, sp.CONTIGUOUS])
 @pytest.mark.parametrize("B,H,S,D,N", [(1, 1, 256, 64, 4), (1, 2, 4 * 37, 32, 4), (2, 1, 96, 128, 8),
-                                       (1, 1, 64, 64, 1), (1, 1, 16, 64, 16)])
+                                       (1, 1, 64, 64, 1), (1, 1, 16, 64, 16),
+                                       (1, 1, 4 * 45, 8, 4),    # D = 8: one element of a row per thread
+                                       (1, 2, 144, 96, 3)])     # D = 96: the run-time head width, 12 per thread
 def test_fwd_fp32(B, H, S, D, N, layout):
     x, o, lse, stats = _run_fwd(B, H, S, D, N, layout, torch.float32)
     _check_fwd(x, o, lse, stats, B, H, S, D, N, layout, torch.float32)

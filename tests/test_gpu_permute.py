@@ -27,6 +27,25 @@ def test_permute_bit_exact(B, H, S, D, N, dtype):
     assert torch.equal(z.cpu(), x)
 
 
+@pytest.mark.parametrize("layout", [sp.STRIPED, sp.CONTIGUOUS, sp.ZIGZAG])
+@pytest.mark.parametrize("B,H,S,D,N,dtype", [
+    (1, 2, 6 * 38, 96, 6, torch.float32),   # rows of 24 16-byte vectors (not a power of two)
+    (2, 1, 10 * 20, 24, 5, torch.bfloat16),  # rows of 3 vectors
+    (1, 1, 8 * 64, 96, 8, torch.bfloat16),   # rows of 12 vectors
+])
+def test_permute_rows_not_a_power_of_two(B, H, S, D, N, dtype, layout):
+    """Row sizes that are not a power of two of 16-byte vectors (the fp32
+    attention path accepts any head dimension that is a multiple of 8) take
+    the permutation's division path: bit-exact and a round trip."""
+    dev = torch.device("cuda")
+    g = torch.Generator(device="cpu").manual_seed(77)
+    x = torch.randn(B, H, S, D, generator=g).to(dtype)
+    pos = torch.as_tensor(positions(S, N, layout))
+    y = sp.layout_permute(x.to(dev), N, layout)
+    assert torch.equal(y.cpu(), x[:, :, pos])
+    assert torch.equal(sp.layout_unpermute(y, N, layout).cpu(), x)
+
+
 def test_permute_full_size_long_context():
     """Largest tensor of the benchmark workloads (B=1, H=32, S=262144,
     D=128, bf16, N=8): sampled rows bit-exact, round trip exact."""
