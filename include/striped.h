@@ -89,9 +89,10 @@ extern "C" {
  * Stripe permutation (§Summary "every N-th token"; §Key points: applied once
  * before the model).  y[b,h,d*L+i,:] = x[b,h,i*N+d,:] for every d < N,
  * i < L.  x and y are [B,H,S,D] device tensors of `dtype`; they must not
- * overlap.  Requires S % N == 0 and D * sizeof(dtype) a multiple of 16
- * bytes, at most 32 KB (STRIPED_ERR_ALIGN otherwise); 16-byte aligned
- * pointers.  Pure data movement: the result is a bit copy.
+ * overlap.  Requires S % N == 0, 16-byte aligned pointers and
+ * D * sizeof(dtype) a multiple of 16 bytes (STRIPED_ERR_ALIGN otherwise) of
+ * at most 32 KB (STRIPED_ERR_UNSUPPORTED otherwise).  Pure data movement:
+ * the result is a bit copy.
  */
 int striped_permute(const void *x, void *y, int64_t B, int64_t H, int64_t S, int64_t D, int N,
                     int dtype, void *stream);
