@@ -97,16 +97,11 @@ __device__ __forceinline__ int tile_rows(int64_t L, int t) {
     return r >= BT ? BT : (int)r;
 }
 
-#ifndef BWD_RING_ORDER
-#define BWD_RING_ORDER 0
-#endif
-#ifndef BWD_ASCENDING
-#define BWD_ASCENDING 0
-#endif
 // Order in which a key tile visits its query tiles: the G query heads that
 // read its key/value head (grouped-query attention; G = 1 otherwise), per
-// head the stripes d = d0, d0+1, ... (mod N), and within a stripe the tiles
-// that see the key tile, in ascending or descending order.
+// head the query stripes d = 0, 1, ..., N-1, and within a stripe the tiles
+// that see the key tile from the last one down (ascending order and ring
+// order across the stripes measured within 2% of this one).
 struct QTileIter {
     int h, k, d, a, a_lo, has_diag, diag_off;
 };
@@ -115,7 +110,7 @@ __device__ __forceinline__ void qiter_seek(QTileIter &it, int layout, int N, int
                                            int rows_b, int dsel) {
     while (it.h < G) {
         while (it.k < N) {
-            it.d = BWD_RING_ORDER ? (e + it.k) % N : it.k;
+            it.d = it.k;
             if (dsel >= 0 && it.d != dsel) {  // one ring round: only query stripe dsel
                 ++it.k;
                 continue;
@@ -125,7 +120,7 @@ __device__ __forceinline__ void qiter_seek(QTileIter &it, int layout, int N, int
                 it.a_lo = sp.a_lo;
                 it.has_diag = sp.has_diag;
                 it.diag_off = sp.diag_off;
-                it.a = BWD_ASCENDING ? sp.a_lo : nq - 1;
+                it.a = nq - 1;
                 return;
             }
             ++it.k;
@@ -144,8 +139,7 @@ __device__ __forceinline__ QTileIter qiter_begin(int layout, int N, int G, int e
 
 __device__ __forceinline__ void qiter_next(QTileIter &it, int layout, int N, int G, int e, int b, int nq,
                                            int rows_b, int dsel) {
-    const bool end = BWD_ASCENDING ? (++it.a >= nq) : (--it.a < it.a_lo);
-    if (end) {
+    if (--it.a < it.a_lo) {
         ++it.k;
         qiter_seek(it, layout, N, G, e, b, nq, rows_b, dsel);
     }
