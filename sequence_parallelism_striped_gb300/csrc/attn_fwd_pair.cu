@@ -11,16 +11,17 @@
 //     PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
 // so that while one group turns S into P the tensor core works for the
 // other group.  Used for the batched striped forward when every stripe is a
-// whole number of tiles, N is even, the head dimension is 128 and the grid
-// stays balanced (fwd_pair_eligible); the one-tile kernel serves every other
-// case.
+// whole number of tiles, N is even, the head dimension is 64 or 128 and the
+// grid stays balanced (fwd_pair_eligible); the one-tile kernel serves every
+// other case.
 //
-//   warp 0      TMA producer: Q_A, Q_B once, then K/V tiles (2 stages)
+//   warp 0      TMA producer: Q_A, Q_B once, then K/V tiles (2 stages at
+//               HD = 128, 4 at HD = 64)
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
 //   warps 2..5  softmax group A (stripe d), thread t owns query row t
 //   warps 6..9  softmax group B (stripe d + 1)
-// Tensor memory (512 columns): S_A [0,128), S_B [128,256), O_A [256,384),
-// O_B [384,512); P is written back over S as bf16 pairs.
+// Tensor memory (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+HD),
+// O_B [384,384+HD); P is written back over S as bf16 pairs.
 #include <math.h>
 
 #include "common.cuh"
@@ -31,22 +32,29 @@ namespace striped {
 namespace {
 
 constexpr int PB = 128;                         // tile edge (queries and keys)
-constexpr int PHD = 128;                        // head dimension
-constexpr int PNS = 2;                          // K/V stages
 constexpr uint32_t kPBox = 128 * 128;           // 128 rows x 64 bf16
-constexpr uint32_t kPTile = 2 * kPBox;          // 128 x 128 bf16
-constexpr uint32_t kPQOff = 0;                  // Q_A, then Q_B
-constexpr uint32_t kPKVOff = 2 * kPTile;        // stage s: K at kPKVOff + s*kPStage, V after
-constexpr uint32_t kPStage = 2 * kPTile;
-constexpr uint32_t kPBarOff = kPKVOff + PNS * kPStage;
-constexpr size_t kPSmemBytes = 1024 + kPBarOff + 256;
-static_assert(kPSmemBytes <= 232448, "shared memory over the per-block limit");
+constexpr int kPMaxNS = 4;
+
+// Shared-memory plan for head dimension HD (64 or 128): Q_A, Q_B, then PNS
+// stages of K and V, each tile HD/64 boxes.
+template <int HD>
+struct PairCfg {
+    static constexpr int PNS = HD == 128 ? 2 : 4;      // K/V stages
+    static constexpr uint32_t kPTile = (HD / 64) * kPBox;  // 128 x HD bf16
+    static constexpr uint32_t kPQOff = 0;                 // Q_A, then Q_B
+    static constexpr uint32_t kPKVOff = 2 * kPTile;       // stage s: K at kPKVOff + s*kPStage, V after
+    static constexpr uint32_t kPStage = 2 * kPTile;
+    static constexpr uint32_t kPBarOff = kPKVOff + PNS * kPStage;
+    static constexpr size_t kPSmemBytes = 1024 + kPBarOff + 256;
+    static_assert(kPSmemBytes <= 232448, "shared memory over the per-block limit");
+    static_assert(PNS <= kPMaxNS, "barrier array");
+};
 constexpr int kPThreads = 320;
 constexpr float kPRescale = 8.0f;  // lazy rescale threshold, log2 units
 
 struct PairBars {
     uint64_t q_full;
-    uint64_t kv_full[PNS], kv_empty[PNS];
+    uint64_t kv_full[kPMaxNS], kv_empty[kPMaxNS];
     uint64_t s_full[2], p_ready[2], o_done[2];  // per softmax group
     uint64_t drain;                             // every MMA of the issuer has completed
     uint32_t tmem_slot;
@@ -60,9 +68,15 @@ struct PairParams {
     WaitCtl wc;  // status word, wait bound, test hook
 };
 
+template <int HD>
 __global__ void __launch_bounds__(kPThreads, 1)
     tc_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const PairParams p) {
+    using Cfg = PairCfg<HD>;
+    constexpr int PNS = Cfg::PNS;
+    constexpr uint32_t kPTile = Cfg::kPTile, kPQOff = Cfg::kPQOff, kPKVOff = Cfg::kPKVOff,
+                       kPStage = Cfg::kPStage, kPBarOff = Cfg::kPBarOff;
+    constexpr int kBoxes = HD / 64;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
@@ -115,10 +129,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
         tma_prefetch_desc(&tmV);
         const uint32_t qb = smem_u32(&bars->q_full);
         mbar_arrive_expect_tx(qb, 2 * kPTile);
-        for (int x = 0; x < 2; ++x) {
-            tma_load_4d(sbase + kPQOff + x * kPTile, &tmQ, qb, 0, a * PB, d0 + x, (int)bh);
-            tma_load_4d(sbase + kPQOff + x * kPTile + kPBox, &tmQ, qb, 64, a * PB, d0 + x, (int)bh);
-        }
+        for (int x = 0; x < 2; ++x)
+#pragma unroll
+            for (int c = 0; c < kBoxes; ++c)
+                tma_load_4d(sbase + kPQOff + x * kPTile + c * kPBox, &tmQ, qb, 64 * c, a * PB, d0 + x, (int)bh);
         // test hook: the first K/V tile is never loaded, so every wait on it
         // runs out (the kernel must then record the timeout and return)
         const bool skip_first = p.wc.inject == kInjectFwdSkipKV;
@@ -136,10 +150,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 const uint32_t kdst = sbase + kPKVOff + s * kPStage;
                 const uint32_t vdst = kdst + kPTile;
                 mbar_arrive_expect_tx(fb, 2 * kPTile);
-                tma_load_4d(kdst, &tmK, fb, 0, b * PB, e, kvh);
-                tma_load_4d(kdst + kPBox, &tmK, fb, 64, b * PB, e, kvh);
-                tma_load_4d(vdst, &tmV, fb, 0, b * PB, e, kvh);
-                tma_load_4d(vdst + kPBox, &tmV, fb, 64, b * PB, e, kvh);
+#pragma unroll
+                for (int c = 0; c < kBoxes; ++c) {
+                    tma_load_4d(kdst + c * kPBox, &tmK, fb, 64 * c, b * PB, e, kvh);
+                    tma_load_4d(vdst + c * kPBox, &tmV, fb, 64 * c, b * PB, e, kvh);
+                }
             }
             if (!ok) break;
         }
@@ -151,7 +166,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
         constexpr uint32_t idesc_qk = idesc_bf16_f32(PB, PB, false, false);
-        constexpr uint32_t idesc_pv = idesc_bf16_f32(PB, PHD, false, true);
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(PB, HD, false, true);
         bool ok = mbar_wait(smem_u32(&bars->q_full), 0, p.wc);
         tc_fence_after();
         auto issue_s = [&](int x, int t) -> bool {
@@ -161,7 +176,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const uint32_t qaddr = sbase + kPQOff + x * kPTile;
             const uint32_t kaddr = sbase + kPKVOff + s * kPStage;
 #pragma unroll
-            for (int kk = 0; kk < PHD / 16; ++kk) {
+            for (int kk = 0; kk < HD / 16; ++kk) {
                 const uint32_t off = (kk >> 2) * kPBox + (kk & 3) * 32;
                 mma_ss(tmem + 128 * x, sdesc_sw128(qaddr + off, 16, 1024), sdesc_sw128(kaddr + off, 16, 1024),
                        idesc_qk, kk > 0 ? 1u : 0u);
@@ -290,7 +305,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         // rare (lazy rescale): one 32-column chunk at a time
                         // keeps the softmax thread within its registers
 #pragma unroll 1
-                        for (int c = 0; c < PHD / 32; ++c) {
+                        for (int c = 0; c < HD / 32; ++c) {
                             uint32_t rr[32];
                             tmem_ld32(tO + c * 32, rr);
                             tmem_ld_wait(rr);
@@ -325,9 +340,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const float inv_l = empty ? 0.f : 1.f / l;
         const float lse_row = empty ? -INFINITY : (m_ref + log2f(l)) * 0.6931471805599453f;
         p.lse[bh * g.lse_stride_bh + (int64_t)d * g.lse_stripe_stride + i] = lse_row;
-        const int64_t orow = (int64_t)bh * g.stride_bh + (int64_t)d * g.stripe_stride + i * PHD;
+        const int64_t orow = (int64_t)bh * g.stride_bh + (int64_t)d * g.stripe_stride + i * HD;
 #pragma unroll
-        for (int c = 0; c < PHD / 32; ++c) {
+        for (int c = 0; c < HD / 32; ++c) {
             uint32_t rr[32];
             tmem_ld32(tO + c * 32, rr);
             tmem_ld_wait(rr);
@@ -363,7 +378,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
 // N=8 the pair forward is 16% slower at S = 8192, where the rule declines
 // it, and 4.5% faster at S = 65536).
 bool fwd_pair_eligible(const AttnGeom &g, int num_sms) {
-    if (!(g.layout == STRIPED_LAYOUT_STRIPED && g.D == PHD && g.seqs.n == 0 && g.N % 2 == 0 && g.L > 0 &&
+    if (!(g.layout == STRIPED_LAYOUT_STRIPED && (g.D == 128 || g.D == 64) && g.seqs.n == 0 && g.N % 2 == 0 &&
+          g.L > 0 &&
           g.L % PB == 0) ||
         num_sms < 1)
         return false;
@@ -373,15 +389,22 @@ bool fwd_pair_eligible(const AttnGeom &g, int num_sms) {
     return 2.0 * heaviest * num_sms <= total;
 }
 
+template <int HD>
+static int launch_pair_hd(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const PairParams &p,
+                          int64_t nblocks, cudaStream_t stream) {
+    static PerDeviceOnce attr_once;
+    const int attr = attr_once.get([] {
+        return cuda_status(cudaFuncSetAttribute(tc_fwd_pair_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)PairCfg<HD>::kPSmemBytes));
+    });
+    if (attr != STRIPED_OK) return attr;
+    tc_fwd_pair_kernel<HD><<<(unsigned)nblocks, kPThreads, PairCfg<HD>::kPSmemBytes, stream>>>(mq, mk, mv, p);
+    return cuda_status(cudaGetLastError());
+}
+
 int launch_tc_fwd_pair(const void *q, const void *k, const void *v, void *o, float *lse, const AttnGeom &g,
                        int64_t *tile_stats, cudaStream_t stream) {
     if (!fwd_pair_eligible(g, device_sm_count())) return STRIPED_ERR_UNSUPPORTED;
-    static PerDeviceOnce attr_once;
-    const int attr = attr_once.get([] {
-        return cuda_status(
-            cudaFuncSetAttribute(tc_fwd_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmemBytes));
-    });
-    if (attr != STRIPED_OK) return attr;
     CUtensorMap mq, mk, mv;
     const int64_t bh_kv = g.BH / g.G;
     int st;
@@ -397,8 +420,8 @@ int launch_tc_fwd_pair(const void *q, const void *k, const void *v, void *o, flo
     p.wc = device_wait_ctl();
     const int64_t nblocks = (g.L / PB) * (g.N / 2) * g.BH;
     if (nblocks > 0x7fffffffll) return STRIPED_ERR_UNSUPPORTED;
-    tc_fwd_pair_kernel<<<(unsigned)nblocks, kPThreads, kPSmemBytes, stream>>>(mq, mk, mv, p);
-    return cuda_status(cudaGetLastError());
+    return g.D == 128 ? launch_pair_hd<128>(mq, mk, mv, p, nblocks, stream)
+                      : launch_pair_hd<64>(mq, mk, mv, p, nblocks, stream);
 }
 
 }  // namespace striped

@@ -78,7 +78,9 @@ def test_fwd_bf16_short_sequence_full(layout):
                                              (2, 24, 4096, 128, 2, 2),   # one stripe pair, 16 tiles a stripe
                                              (1, 24, 6144, 128, 6, 2),   # N = 6
                                              (1, 8, 8192, 128, 8, 1),    # too few tiles per SM for pairs
-                                             (1, 2, 1536, 128, 3, 1)])   # odd N
+                                             (1, 2, 1536, 128, 3, 1),    # odd N
+                                             (1, 24, 8192, 64, 8, 2),    # head dimension 64
+                                             (2, 24, 4096, 64, 2, 2)])
 def test_fwd_bf16_stripe_pairs(B, H, S, D, N, pairs):
     """Whole-tile stripes, an even N and enough work per multiprocessor: the
     forward runs the query tiles of stripes d and d + 1 in one CTA on one
