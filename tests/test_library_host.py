@@ -106,7 +106,7 @@ def test_kernel_tiles(lib):
 
 
 def test_forward_schedule_rule(lib):
-    """Stripe-pair forward (2 query tiles per CTA) only for bf16, D = 128,
+    """Stripe-pair forward (2 query tiles per CTA) only for bf16, D = 64 or 128,
     striped, whole-tile stripes, even N, and a balanced grid: twice the
     heaviest pair CTA's key tiles (2 * nq * N) at most the average key
     tiles per multiprocessor, the total taken from the oracle's table."""
@@ -136,7 +136,9 @@ def test_forward_schedule_rule(lib):
     # every other kernel configuration: one query tile per CTA
     for layout in (sp.CONTIGUOUS, sp.ZIGZAG):
         assert sp.fwd_query_tiles_per_cta(1, 32, 262144, 128, 8, layout, num_sms=sms) == 1
-    assert sp.fwd_query_tiles_per_cta(1, 32, 262144, 64, 8, num_sms=sms) == 1
+    # head dimension 64 follows the same rule as 128
+    assert sp.fwd_query_tiles_per_cta(1, 32, 262144, 64, 8, num_sms=sms) == 2
+    assert sp.fwd_query_tiles_per_cta(1, 8, 8192, 64, 8, num_sms=sms) == 1
     assert sp.fwd_query_tiles_per_cta(1, 4, 4096, 64, 8, dtype=torch.float32, num_sms=sms) == 1
     # more multiprocessors need more work per head before pairs pay
     assert sp.fwd_query_tiles_per_cta(1, 24, 8192, 128, 8, num_sms=1000) == 1
