@@ -315,10 +315,11 @@ int striped_kernel_tile(int dtype, int64_t D, int *Tq, int *Tk);
 /* Host-only: how many query tiles one CTA of striped_attn_fwd /
  * striped_attn_fwd_gqa runs for this problem on a GPU with `num_sms`
  * multiprocessors: 2 when the stripes d and d + 1 share one K/V stream (bf16,
- * D = 128, striped placement, L = S/N a whole number of 128-row tiles, N
- * even) and the grid stays balanced -- twice the heaviest CTA's key tiles,
+ * D = 64 or 128, striped placement, L = S/N a whole number of 128-row tiles,
+ * N even) and the grid stays balanced -- twice the heaviest CTA's key tiles,
  * 2 * (L/128) * N, at most the average key tiles per multiprocessor -- else
- * 1.  Both schedules compute the same result bit for bit.  Returns 1 or 2,
+ * 1.  Both schedules do the same arithmetic in the same order (measured
+ * bit-identical at D = 128).  Returns 1 or 2,
  * or STRIPED_ERR_INVALID_ARG / STRIPED_ERR_UNSUPPORTED for arguments the
  * forward rejects (num_sms < 1 is invalid). */
 int striped_fwd_query_tiles_per_cta(int64_t B, int64_t H, int64_t S, int64_t D, int N, int layout, int dtype,
