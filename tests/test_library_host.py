@@ -168,6 +168,10 @@ def test_invalid_arguments_rejected_on_host(lib):
     # permute: overlapping buffers, bad sizes
     assert lib.striped_permute(fake, fake, 1, 1, 64, 128, 4, 0, None) == -1
     assert lib.striped_permute(fake, P((1 << 24)), 1, 1, 64, 128, 0, 0, None) == -1
+    # permute: a row must be whole 16-byte vectors (bf16 D = 12: 24 bytes), at most 32 KB
+    # (fp32 D = 16384: 64 KB); any vector count in between is taken
+    assert lib.striped_permute(fake, P((1 << 24)), 1, 1, 64, 12, 4, 0, None) == -3
+    assert lib.striped_permute(fake, P((1 << 24)), 1, 1, 64, 16384, 4, 1, None) == -2
     # workspace too small
     assert lib.striped_attn_bwd(fake, fake, fake, fake, fake, fake, fake, fake, fake, fake, 16, 1, 1, 64, 128,
                                 4, 0, 0, 1.0, None, None) == -6
