@@ -29,18 +29,26 @@
 //                dP^T = V dO_i^T     SS, both K-major
 //                dV  += P^T dO_i     TS, A = P^T in TMEM, B = dO_i MN-major
 //                dK  += dS^T Q_i     SS, A = dS smem tile read K-major
-//                dQ_i = dS K         SS, A = the same smem tile read MN-major
+//                dQ_i^T = K^T dS^T   SS, A = K read MN-major, B = the dS
+//                                    tile read MN-major (HD = 128)
+//                dQ_i = dS K         SS, A = the dS tile read MN-major (HD 64)
 //              The dS tile ([key][query], 128-byte swizzle) is a valid
 //              operand both ways, so dS^T never goes through TMEM.  Issue
 //              order dV_i, S_{i+1}, dK_i, dQ_i, dP_{i+1} keeps the tensor core
 //              busy while the compute warps form dS_i, P_{i+1} and read dQ_i
 //              out; dK_i goes before dQ_i so that Q_i, whose last reader it
 //              is, returns to the producer one MMA earlier and the next Q
-//              tile loads early.  dQ_i goes to the fp32 accumulator half by
-//              vector reductions (warpgroup 0) and half by TMA bulk
-//              reduce-add from the dO_i buffer, dead by then (warpgroup 1;
-//              the wait for the reduce to read the buffer is deferred by one
-//              tile).
+//              tile loads early.
+//              dQ_i to the fp32 accumulator: at HD = 128 dQ_i is formed
+//              transposed (head dimension in TMEM lanes, queries in columns),
+//              so a warp's reduction for one query covers one whole 128-byte
+//              line of the accumulator, and dO_i returns to its producer as
+//              soon as dV_i completes.  At HD = 64 (an M = 64 transposed
+//              product would use another TMEM layout) warpgroup 0 adds its
+//              columns with vector reductions and warpgroup 1 stages its
+//              columns in the dO_i buffer, dead by then, and bulk
+//              reduce-adds them (the wait for the reduce to read the buffer
+//              is deferred by one tile).
 //   bwd_post   dQ = bf16(scale * accumulator)
 #include <math.h>
 
@@ -86,7 +94,7 @@ struct BwdParams {
 struct Bars {
     uint64_t kv_full;
     uint64_t q_full[QS], q_empty[QS];    // Q_i + statistics of tile i
-    uint64_t do_full[QS], do_empty[QS];  // dO_i (its buffer also stages half of dQ_i)
+    uint64_t do_full[QS], do_empty[QS];  // dO_i (HD 64: its buffer also stages half of dQ_i)
     uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, dq_free, acc_done;
     uint64_t drain;  // every MMA of the issuer has completed (before TMEM is freed)
     uint32_t tmem_slot;
@@ -206,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&bars->q_full[s]), 1);
             mbar_init(smem_u32(&bars->q_empty[s]), 1);   // released by dK_i's commit
             mbar_init(smem_u32(&bars->do_full[s]), 1);
-            mbar_init(smem_u32(&bars->do_empty[s]), 4);  // one arrival per warpgroup-1 warp
+            mbar_init(smem_u32(&bars->do_empty[s]), HD == 128 ? 1 : 4);  // dV_i's commit; HD 64: warpgroup-1 warps
         }
         mbar_init(smem_u32(&bars->s_full), 1);
         mbar_init(smem_u32(&bars->dp_full), 1);
@@ -267,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(skip_first && t == 0)) mbar_wait(smem_u32(&bars->q_full[t % QS]), (t / QS) & 1, p.wc);
     } else if (warp == 2 && lane == 0 && nt > 0) {
         // ---------------- TMA producer: dO_i (its own stream: the buffer is
-        // released later than Q_i's, after the dQ_i half staged in it is read)
+        // released at dV_i, or at HD 64 after the dQ_i half staged in it is read)
         tma_prefetch_desc(&tmdO);
         QTileIter it = qiter_begin(g.layout, N, G, e, b, nqs, rows_b, dsel);
         int i = 0;
@@ -293,6 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t id_kk = idesc_bf16_f32(BT, BT, false, false);
         constexpr uint32_t id_kmn = idesc_bf16_f32(BT, HD, false, true);
         constexpr uint32_t id_mnmn = idesc_bf16_f32(BT, HD, true, true);
+        constexpr uint32_t id_dqt = idesc_bf16_f32(HD, BT, true, true);  // dQ^T: M = HD, N = 128 queries
         auto issue_s = [&](int t) -> bool {
             const int s = t % QS;
             if (!mbar_wait(smem_u32(&bars->q_full[s]), (t / QS) & 1, p.wc)) return false;
@@ -346,6 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < BT / 16; ++kk)
                 mma_ts(tdV, tS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
                        sdesc_sw128(oaddr + kk * 2048, kBox, 1024), id_kmn, (i > 0 || kk > 0) ? 1u : 0u);
+            // HD 128: dO_i (read by dP_i and dV_i only) is free once dV_i completes
+            if (HD == 128 && i + QS < nt) mma_commit(smem_u32(&bars->do_empty[s]));
             if (i + 1 < nt && !issue_s(i + 1)) break;
             // dK += dS^T Q (A = dS^T, K-major view of the dS smem tile)
             if (!mbar_wait(smem_u32(&bars->ds_ready), i & 1, p.wc)) break;
@@ -356,11 +367,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                        sdesc_sw128(qaddr + kk * 2048, kBox, 1024), id_kmn, (i > 0 || kk > 0) ? 1u : 0u);
             // Q_i (and its statistics) are free once dK_i completes
             if (i + QS < nt) mma_commit(smem_u32(&bars->q_empty[s]));
-            // dQ_i = dS K (A = dS, MN-major view of the same tile) -> DP columns
+            if constexpr (HD == 128) {
+                // dQ_i^T = K^T dS^T (A = K, MN-major; B = the dS tile, MN-major)
+                // -> DP columns, head dimension in TMEM lanes, queries in columns
 #pragma unroll
-            for (int kk = 0; kk < BT / 16; ++kk)
-                mma_ss(tdP, sdesc_sw128(sbase + kDSOff + kk * 2048, kBox, 1024),
-                       sdesc_sw128(sbase + kKOff + kk * 2048, kBox, 1024), id_mnmn, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < BT / 16; ++kk)
+                    mma_ss(tdP, sdesc_sw128(sbase + kKOff + kk * 2048, kBox, 1024),
+                           sdesc_sw128(sbase + kDSOff + kk * 2048, kBox, 1024), id_dqt, kk > 0 ? 1u : 0u);
+            } else {
+                // dQ_i = dS K (A = dS, MN-major view of the same tile) -> DP columns
+#pragma unroll
+                for (int kk = 0; kk < BT / 16; ++kk)
+                    mma_ss(tdP, sdesc_sw128(sbase + kDSOff + kk * 2048, kBox, 1024),
+                           sdesc_sw128(sbase + kKOff + kk * 2048, kBox, 1024), id_mnmn, kk > 0 ? 1u : 0u);
+            }
             mma_commit(smem_u32(&bars->dq_full));
             if (it.d != cnt_d) {
                 flush_counts();
@@ -511,17 +531,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            // dQ_i -> fp32 accumulator, split over two paths so neither the
-            // TMA engine nor the load/store unit carries all of it: warpgroup 0
-            // adds its HD/2 columns with vector reductions; warpgroup 1 stages
-            // its HD/2 columns in the dO_i buffer (dead once dV_i, covered by
-            // dq_full, is done) as 128-byte-swizzled 32-column boxes and
-            // each warp bulk-reduces its own 32 rows, then returns the buffer.
-            // HD = 128 and HD = 64 are written out separately: a shared generic
-            // form compiled to a 1.4% slower schedule of this hot path at 128.
+            // dQ_i -> fp32 accumulator (the two forms are described at the
+            // top of this file).
             const int s = i % QS;
             const int64_t bq = bh * G + done.h;  // query head of tile i
             if constexpr (HD == 128) {
+                // dQ_i^T: lane = head-dimension column, TMEM column = query;
+                // this warp's 32 dimensions of the warpgroup's 64 queries.
+                // One reduction per query covers a whole 128-byte line of the
+                // accumulator across the warp.
                 uint32_t q0[32], q1[32];
                 tmem_ld32(tdP + lane_off + cbase, q0);
                 tmem_ld32(tdP + lane_off + cbase + 32, q1);
@@ -530,46 +548,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
-                if (wg == 0) {
-                    const int64_t qi = (int64_t)(qbase + done.a) * BT + row;
-                    if (qi < g.L) {
-                        float *dst =
-                            p.dq_acc + (bq * g.stride_bh + (int64_t)done.d * g.stripe_stride + qi * HD + cbase);
+                const int64_t q_first = (int64_t)(qbase + done.a) * BT + cbase;
+                const int64_t nv = g.L - q_first;  // real queries among the 64 (uniform per warp)
+                float *dst = p.dq_acc +
+                             (bq * g.stride_bh + (int64_t)done.d * g.stripe_stride + q_first * HD + quarter * 32 + lane);
+                if (nv >= 64) {
 #pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            red_add_v4(dst + 4 * v, __uint_as_float(q0[4 * v]), __uint_as_float(q0[4 * v + 1]),
-                                       __uint_as_float(q0[4 * v + 2]), __uint_as_float(q0[4 * v + 3]));
+                    for (int c = 0; c < 32; ++c) red_add_f32(dst + c * HD, __uint_as_float(q0[c]));
 #pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            red_add_v4(dst + 32 + 4 * v, __uint_as_float(q1[4 * v]), __uint_as_float(q1[4 * v + 1]),
-                                       __uint_as_float(q1[4 * v + 2]), __uint_as_float(q1[4 * v + 3]));
-                    }
+                    for (int c = 0; c < 32; ++c) red_add_f32(dst + (32 + c) * HD, __uint_as_float(q1[c]));
                 } else {
-                    const uint32_t stage = sbase + kQOff + s * 2 * kTile + kTile;
 #pragma unroll
-                    for (int box = 0; box < 2; ++box) {
-                        const uint32_t(&src)[32] = box ? q1 : q0;
+                    for (int c = 0; c < 32; ++c)
+                        if (c < nv) red_add_f32(dst + c * HD, __uint_as_float(q0[c]));
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const uint32_t addr = stage + box * kBox + row * 128 + ((j ^ (row & 7)) * 16);
-                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(src[4 * j]),
-                                         "r"(src[4 * j + 1]), "r"(src[4 * j + 2]), "r"(src[4 * j + 3])
-                                         : "memory");
-                        }
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        const uint32_t wofs = (uint32_t)quarter * 32 * 128;
-                        const int r0 = (qbase + done.a) * BT + quarter * 32;
-                        tma_reduce_add_4d(&tmdQ, stage + wofs, cbase, r0, kRound ? 0 : done.d, (int)bq);
-                        tma_reduce_add_4d(&tmdQ, stage + kBox + wofs, cbase + 32, r0, kRound ? 0 : done.d, (int)bq);
-                        bulk_commit_group();
-                        pending = s;
-                    }
+                    for (int c = 0; c < 32; ++c)
+                        if (32 + c < nv) red_add_f32(dst + (32 + c) * HD, __uint_as_float(q1[c]));
                 }
             } else {
-                // HD = 64: 32 columns per warpgroup, one box for the bulk path
+                // HD = 64: split over two paths so neither the TMA engine nor
+                // the load/store unit carries all of it: warpgroup 0 adds its 32
+                // columns with vector reductions; warpgroup 1 stages its 32
+                // columns in the dO_i buffer (dead once dV_i, covered by
+                // dq_full, is done) as one 128-byte-swizzled box and each warp
+                // bulk-reduces its own 32 rows, then returns the buffer.
                 uint32_t q0[32];
                 tmem_ld32(tdP + lane_off + dbase, q0);
                 tmem_ld_wait(q0);
@@ -784,7 +786,7 @@ int launch_bwd_hd(const void *q, const void *k, const void *v, const void *o, co
         (st = make_bf16_map(&mv, v, g.D, g.L, g.N, bh_kv, g.stripe_stride, g.stride_bh, 128)) ||
         (st = make_bf16_map(&mdo, dO, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 128)))
         return st;
-    CUtensorMap mdq;
+    CUtensorMap mdq;  // the dQ bulk reduce (read at HD = 64 only)
     if ((st = make_f32_map(&mdq, dq_acc, g.D, g.L, g.N, g.BH, g.stripe_stride, g.stride_bh, 32))) return st;
     BwdParams p{};
     p.g = g;

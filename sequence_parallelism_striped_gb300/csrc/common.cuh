@@ -519,4 +519,8 @@ __device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float 
                  : "memory");
 }
 
+__device__ __forceinline__ void red_add_f32(float *addr, float a) {
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
+}
+
 }  // namespace striped
