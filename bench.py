@@ -36,9 +36,9 @@ WORKLOAD = {"workload": "long-context striped causal attention fwd+bwd", "B": 1,
 
 
 # DRAM bytes (read + write) of one tc_bwd_kernel launch on this workload:
-# ncu capture of the same kernel on B=1, H=8, S=65536 (1.409 GB, see
+# ncu capture of the same kernel on B=1, H=8, S=65536 (1.406 GB, see
 # profiles/tc_bwd_kernel__B1_H8_S65536_N8.md) scaled by B*H*S (x16).
-BWD_TRAFFIC_BYTES = 16 * 1.4087e9
+BWD_TRAFFIC_BYTES = 16 * 1.4061e9
 BWD_TRAFFIC_NOTE = "ncu dram bytes of tc_bwd_kernel at B=1,H=8,S=65536 scaled by B*H*S"
 
 
