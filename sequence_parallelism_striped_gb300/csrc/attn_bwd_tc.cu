@@ -19,9 +19,11 @@
 //              Q_i with its statistics, 2 stages), warp 2 = TMA producer of
 //              dO_i (own 2-stage stream), warp 1 = TMEM allocator + MMA
 //              issuer, warps 4..11 = two compute warpgroups; thread t of a
-//              warpgroup owns key row t of S^T/dP^T (query row t of dQ),
-//              warpgroup 0 query columns 0..63 and head-dimension columns
-//              0..HD/2-1, warpgroup 1 the rest.  HD = 128 or 64.
+//              warpgroup owns key row t of S^T/dP^T and, for dQ_i, head-
+//              dimension column t of its 64 queries (HD = 128) or query row
+//              t (HD = 64); warpgroup 0 has query columns 0..63 and the
+//              head-dimension columns 0..HD/2-1 of dK, dV (and of dQ at
+//              HD = 64), warpgroup 1 the rest.  HD = 128 or 64.
 //              TMEM: S^T [0,128) (P^T bf16 pairs over it), dP^T [128,256)
 //              (dQ_i over it once dS_i is formed), dV [256,256+HD),
 //              dK [256+HD,256+2HD).
